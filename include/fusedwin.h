@@ -1,0 +1,172 @@
+/*
+ * fusedwin.h -- C ABI of libfusedwin: fused 2-D sliding-window operators on
+ * dense NCHW float32 tensors, computed by CUDA kernels for sm_103a (GB300).
+ *
+ * Operators (each one a PyTorch model from the POPCORNBENCH reasoning traces):
+ *   fw_conv2d_tanh_scale_bias_maxpool       -- trace "Kimi-K2.6 l2_p82":
+ *        Conv2d(k3, stride 1, pad 0) -> tanh -> *scale -> +bias[C,1,1] -> MaxPool2d(k)
+ *   fw_maxpool2d                             -- trace "Kimi-K2.6 l1_p42":
+ *        MaxPool2d(kernel k, stride s, padding p, dilation d)
+ *   fw_convtranspose2d_softmax_bias_scale_sigmoid -- trace "Kimi-K2.6 l2_p91":
+ *        ConvTranspose2d(k, s, p, output_padding) -> softmax(dim=1) -> +bias -> *scale -> sigmoid
+ *
+ * Conventions shared by every call:
+ *   - Tensors are caller-owned device pointers to dense, contiguous NCHW float32
+ *     (row-major, W fastest).  Pointers must be 4-byte aligned; 16-byte aligned
+ *     pointers (any cudaMalloc / torch allocation) enable the vectorised paths.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream).  They do not synchronise and allocate no memory.
+ *   - Arguments are checked on the host before any launch; a failed check
+ *     returns an error status and launches nothing.  `out` must not overlap any
+ *     input (FW_ERR_ALIAS).
+ *   - Element counts are limited to 2^62; each dimension to 2^31 - 1.
+ *   - Status codes are returned, never aborted on.  Errors raised inside a
+ *     kernel (a bounded wait that gave up) are recorded in a device-side error
+ *     word and reported by fw_check_device_errors().
+ */
+#ifndef FUSEDWIN_H
+#define FUSEDWIN_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fw_status {
+    FW_OK = 0,
+    FW_ERR_NULL = 1,        /* a required pointer is NULL */
+    FW_ERR_SHAPE = 2,       /* a size is < 1, the output would be empty, or too large */
+    FW_ERR_PARAM = 3,       /* kernel / stride / padding / dilation / output_padding out of range,
+                               or a non-finite scale */
+    FW_ERR_ALIAS = 4,       /* out overlaps an input tensor */
+    FW_ERR_ALIGN = 5,       /* a tensor pointer is not 4-byte aligned */
+    FW_ERR_UNSUPPORTED = 6, /* valid arguments that this library does not implement */
+    FW_ERR_LAUNCH = 7,      /* a CUDA call (attribute set-up or kernel launch) failed */
+    FW_ERR_TIMEOUT = 8,     /* a bounded wait inside a kernel gave up */
+    FW_ERR_INTERNAL = 9     /* a kernel reported an inconsistency */
+} fw_status;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *fw_status_string(fw_status s);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int fw_version(void);
+
+/* ------------------------------------------------------------------ shapes */
+
+/* Output size of fw_conv2d_tanh_scale_bias_maxpool.  The conv output is
+ * Hc = H - KH + 1 (stride 1, no padding); the pool (no padding, dilation 1,
+ * floor mode) gives Ho = floor((Hc - pool_k) / pool_s) + 1, pool_s <= 0 meaning
+ * pool_s = pool_k.  For H = 256, KH = 3, pool_k = 4: 254 -> 63
+ * (trace "Kimi-K2.6 l2_p82", problem statement). */
+fw_status fw_conv2d_pool_out_shape(int H, int W, int KH, int KW, int pool_k, int pool_s,
+                                   int *Ho, int *Wo);
+
+/* Output size of fw_maxpool2d: Ho = floor((H + 2p - d(k-1) - 1) / s) + 1
+ * (trace "Kimi-K2.6 l1_p42", output-dimension computation: 512 -> 511). */
+fw_status fw_maxpool2d_out_shape(int H, int W, int k, int s, int p, int d, int *Ho, int *Wo);
+
+/* Output size of fw_convtranspose2d_softmax_bias_scale_sigmoid:
+ * Ho = (H - 1) s - 2p + (k - 1) + op + 1 (trace "Kimi-K2.6 l2_p91",
+ * ConvTranspose2d output shape: 64 -> 129). */
+fw_status fw_convt_out_shape(int H, int W, int k, int s, int p, int op, int *Ho, int *Wo);
+
+/* --------------------------------------------------------------- operators */
+
+/*
+ * Fused conv3x3 -> tanh -> scale -> bias -> MaxPool2d (trace "Kimi-K2.6 l2_p82",
+ * the model's forward and the monotone-reorder argument):
+ *
+ *   y[n,co,h,w]  = conv_b[co] + sum_{ci,i,j} x[n,ci,h+i,w+j] * w[co,ci,i,j]
+ *   out[n,co,a,b] = max_{0<=u,v<pool_k} ( bias[co] + scale * tanh(y[n,co,a*pool_s+u, b*pool_s+v]) )
+ *
+ * x      [N, Cin, H, W]         input
+ * w      [Cout, Cin, KH, KW]    conv weight
+ * conv_b [Cout] or NULL         conv bias (NULL = zero)
+ * bias   [Cout]                 the extra bias of shape [Cout,1,1]
+ * scale  finite float           the scalar multiplier
+ * pool_k >= 1, pool_s >= 1 (or <= 0 for pool_s = pool_k); no pool padding, dilation 1,
+ *        floor mode: conv rows/cols past the last full window are dropped.
+ * out    [N, Cout, Ho, Wo]      see fw_conv2d_pool_out_shape
+ *
+ * The conv intermediate never reaches memory: the window max (min for
+ * scale < 0) is taken on y and the elementwise chain is applied once per
+ * pooled output, which gives the same value because tanh and the float32
+ * rounding of each stage are monotone.  KH = KW = 3 and pool_s = pool_k in
+ * {2, 4} with Cin <= 16 take the tiled kernel; other shapes take a direct one.
+ */
+fw_status fw_conv2d_tanh_scale_bias_maxpool(const float *x, int N, int Cin, int H, int W,
+                                            const float *w, const float *conv_b, int Cout,
+                                            int KH, int KW, float scale, const float *bias,
+                                            int pool_k, int pool_s, float *out, void *stream);
+
+/*
+ * MaxPool2d (trace "Kimi-K2.6 l1_p42", problem statement and the -inf padding
+ * semantics it quotes):
+ *
+ *   out[n,c,a,b] = max_{0<=i,j<k} xpad[n,c, a*s - p + i*d, b*s - p + j*d]
+ *
+ * where taps outside [0,H) x [0,W) are -inf (a window of padding only gives
+ * -inf).  Floor mode.  Ties keep the first tap in row-major (i, j) order (so
+ * the sign of a zero is that of the first zero of the maximum); a NaN tap makes
+ * the output NaN.
+ *
+ * x   [N, C, H, W];  out [N, C, Ho, Wo] (see fw_maxpool2d_out_shape)
+ * k >= 1, s >= 1, p >= 0, d >= 1.
+ * Stride 1, dilation 1, k <= 5, p <= 4 and W a multiple of 4 (16-byte rows) take
+ * the streaming kernel; other arguments take a direct one.
+ */
+fw_status fw_maxpool2d(const float *x, int N, int C, int H, int W, int k, int s, int p, int d,
+                       float *out, void *stream);
+
+/*
+ * ConvTranspose2d -> softmax over channels -> +bias -> *scale -> sigmoid
+ * (trace "Kimi-K2.6 l2_p91", the model and the index map oh = ih*s + kh - p):
+ *
+ *   y[n,co,oh,ow] = conv_b[co] + sum over ci and (kh,kw) with oh = ih*s - p + kh,
+ *                   ow = iw*s - p + kw, 0<=ih<H, 0<=iw<W, of x[n,ci,ih,iw] * w[ci,co,kh,kw]
+ *   p[n,c,oh,ow]  = exp(y[n,c,oh,ow]) / sum_j exp(y[n,j,oh,ow])
+ *   out           = 1 / (1 + exp(-(p + bias[c]) * scale))
+ *
+ * x      [N, Cin, H, W]
+ * w      [Cin, Cout, k, k]  (ConvTranspose2d weight layout)
+ * conv_b [Cout] or NULL;  bias [Cout];  scale finite
+ * k >= 1, s >= 1, p >= 0, 0 <= op < s, Cout <= 1024.
+ * out    [N, Cout, Ho, Wo] (see fw_convt_out_shape)
+ * workspace, workspace_bytes: caller-owned device scratch of at least
+ *        fw_convt_workspace_size(Cin, Cout, k, s, p) bytes, 256-byte aligned
+ *        (NULL/0 when that size is 0).  The call rewrites the weight into it
+ *        (one layout per output parity class); its contents are undefined
+ *        afterwards.  Two calls that overlap in time must not share it.
+ * k = 4, s = 2, p = 1 and Cout = 128 take the phase-decomposed tiled kernel
+ * (each output parity class is a 2x2 convolution); other arguments take a
+ * direct one.
+ */
+fw_status fw_convtranspose2d_softmax_bias_scale_sigmoid(const float *x, int N, int Cin, int H, int W,
+                                                        const float *w, const float *conv_b,
+                                                        int Cout, int k, int s, int p, int op,
+                                                        const float *bias, float scale, float *out,
+                                                        void *workspace, unsigned long long workspace_bytes,
+                                                        void *stream);
+
+/* Bytes of device workspace fw_convtranspose2d_softmax_bias_scale_sigmoid
+ * needs for these arguments (0 when it needs none). */
+unsigned long long fw_convt_workspace_size(int Cin, int Cout, int k, int s, int p);
+
+/* ------------------------------------------------------------- diagnostics */
+
+/*
+ * Synchronise `stream`, then read and clear the device-side error words the
+ * kernels set.  Returns FW_OK, FW_ERR_TIMEOUT (a bounded wait gave up),
+ * FW_ERR_INTERNAL, or FW_ERR_LAUNCH if the synchronisation itself failed.
+ */
+fw_status fw_check_device_errors(void *stream);
+
+/* Number of kernel launches this library has issued in this process (all
+ * devices, all calls).  Used to count launches inside a timed region. */
+unsigned long long fw_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FUSEDWIN_H */

@@ -1,0 +1,282 @@
+// convt.cu -- ConvTranspose2d -> softmax(dim=1) -> +bias -> *scale -> sigmoid
+// (trace "Kimi-K2.6 l2_p91").
+//
+// Phase decomposition (the page's sub-pixel view): for k = 4, s = 2, p = 1 an
+// output pixel (oh, ow) = (2m + py, 2n + px) receives exactly the taps
+//   rows: py = 0 -> (kh = 1, ih = m), (kh = 3, ih = m - 1)
+//         py = 1 -> (kh = 0, ih = m + 1), (kh = 2, ih = m)
+// and the same for columns, so each of the 4 parity classes ("phases") is a
+// dense 2x2 convolution: a GEMM with M = pixels of the phase, N = Cout and
+// K = 4 * Cin.
+//
+// Tiled FFMA kernel (k4 s2 p1, Cout = 128):
+//   * a prepack kernel rewrites the weight [Cin][Cout][4][4] into the caller's
+//     workspace as wp[phase][ci][tap][co], so a CTA streams exactly the weights
+//     of its phase with coalesced 16-byte loads;
+//   * a CTA owns one phase of an 8 x 16 block of phase-grid pixels (128 output
+//     pixels) of one image and all 128 channels; 256 threads, each 8 pixels
+//     (one row, 8 consecutive n) x 8 channels ({4g..4g+3} and {64+4g..64+4g+3});
+//   * Cin is streamed in chunks of 16: input rows m0-1..m0+8 are staged as three
+//     column-shifted copies (dx = -1, 0, +1) so that every tap's 8-pixel row
+//     segment is two aligned 16-byte shared loads;
+//   * the 16 lanes of a half-warp hold all 128 channels of the same 8 pixels, so
+//     the softmax max and sum are 4-step xor-shuffle reductions;
+//   * results are transposed through shared memory and stored row by row.
+// Direct kernel: one thread per output pixel, two passes over the channels
+// (online max/sum, then the outputs), any (k, s, p, op) and Cout <= 1024.
+#include "fw_common.cuh"
+
+namespace fw {
+
+namespace {
+
+constexpr int T_M = 8, T_N = 16;   // phase-grid pixels per CTA (rows, cols)
+constexpr int CK = 16;             // input channels per chunk
+constexpr int COUT_T = 128;        // channels of the tiled kernel
+constexpr int XS_ROWS = T_M + 2;   // staged input rows m0-1 .. m0+T_M
+constexpr int XS_CHUNK = XS_ROWS * 3 * T_N;  // floats per input channel in xs
+constexpr int WS_CHUNK = 4 * COUT_T;          // floats per input channel in ws
+constexpr int OS_PITCH = COUT_T + 1;          // output transpose pitch (conflict-free reads)
+
+// Tap tables of the k4 s2 p1 phase decomposition: for output parity q and tap
+// index t in {0, 1}: kernel index and input offset (ih = m + off).
+__host__ __device__ __forceinline__ int tap_k(int q, int t) { return q == 0 ? (t == 0 ? 1 : 3) : (t == 0 ? 0 : 2); }
+__host__ __device__ __forceinline__ int tap_off(int q, int t) { return q == 0 ? (t == 0 ? 0 : -1) : (t == 0 ? 1 : 0); }
+
+__global__ void convt_prepack_kernel(const float *__restrict__ w, float *__restrict__ wp, int Cin,
+                                     int Cout) {
+    const long long total = 16LL * Cin * Cout;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const int co = (int)(i % Cout);
+        long long r = i / Cout;
+        const int t = (int)(r % 4);
+        r /= 4;
+        const int ci = (int)(r % Cin);
+        const int ph = (int)(r / Cin);
+        const int py = ph >> 1, px = ph & 1;
+        const int kh = tap_k(py, t >> 1), kw = tap_k(px, t & 1);
+        wp[i] = __ldg(w + (((long long)ci * Cout + co) * 4 + kh) * 4 + kw);
+    }
+}
+
+__global__ void __launch_bounds__(256, 2)
+convt_k4s2_ffma_kernel(const float *__restrict__ x, const float *__restrict__ wp,
+                       const float *__restrict__ cb, const float *__restrict__ bias, float scale,
+                       float *__restrict__ out, int Cin, int H, int W, int Ho, int Wo, int tiles_n) {
+    extern __shared__ __align__(16) float sm[];
+    float *xs = sm;                       // [CK][XS_ROWS][3][T_N]
+    float *ws = sm + CK * XS_CHUNK;       // [CK][4][COUT_T]
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane & 15, h = lane >> 4;
+    const int phase = blockIdx.y, py = phase >> 1, px = phase & 1;
+    const int n_img = blockIdx.z;
+    const int tm = blockIdx.x / tiles_n, tn = blockIdx.x - tm * tiles_n;
+    const int m0 = tm * T_M, n0 = tn * T_N;
+    const float *xn = x + (long long)n_img * Cin * H * W;
+    const float *wph = wp + (long long)phase * Cin * WS_CHUNK;
+
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+
+    for (int c0 = 0; c0 < Cin; c0 += CK) {
+        const int ck = min(CK, Cin - c0);
+        __syncthreads();  // previous chunk fully consumed
+        for (int e = tid; e < CK * XS_CHUNK; e += blockDim.x) {
+            const int c = e % T_N;
+            int t = e / T_N;
+            const int sx = t % 3;
+            t /= 3;
+            const int r = t % XS_ROWS, ci = t / XS_ROWS;
+            const int ih = m0 - 1 + r, iw = n0 + c + sx - 1;
+            float v = 0.f;
+            if (ci < ck && ih >= 0 && ih < H && iw >= 0 && iw < W)
+                v = __ldg(xn + ((long long)(c0 + ci) * H + ih) * W + iw);
+            xs[e] = v;
+        }
+        {
+            const float4 *src = reinterpret_cast<const float4 *>(wph + (long long)c0 * WS_CHUNK);
+            float4 *dst = reinterpret_cast<float4 *>(ws);
+            const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int e = tid; e < CK * WS_CHUNK / 4; e += blockDim.x)
+                dst[e] = (e < ck * WS_CHUNK / 4) ? __ldg(src + e) : z;
+        }
+        __syncthreads();
+#pragma unroll 2
+        for (int ci = 0; ci < ck; ++ci) {
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const int dy = tap_off(py, t >> 1), dx = tap_off(px, t & 1);
+                const float *xr = xs + ((ci * XS_ROWS + warp + dy + 1) * 3 + (dx + 1)) * T_N + 8 * h;
+                const float4 xa = *reinterpret_cast<const float4 *>(xr);
+                const float4 xb = *reinterpret_cast<const float4 *>(xr + 4);
+                const float *wr = ws + (ci * 4 + t) * COUT_T + 4 * g;
+                const float4 wa = *reinterpret_cast<const float4 *>(wr);
+                const float4 wb = *reinterpret_cast<const float4 *>(wr + 64);
+                const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+                const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(xv[i], wv[j], acc[i][j]);
+            }
+        }
+    }
+
+    // Epilogue: conv bias, softmax over the 128 channels (16 lanes x 8), then
+    // +bias, *scale, sigmoid.
+    float cbv[8], bv[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int co = (j < 4 ? 4 * g + j : 64 + 4 * g + (j - 4));
+        cbv[j] = cb ? __ldg(cb + co) : 0.f;
+        bv[j] = __ldg(bias + co);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        float mx = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            acc[i][j] += cbv[j];
+            mx = fmaxf(mx, acc[i][j]);
+        }
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        float sum = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            acc[i][j] = expf(acc[i][j] - mx);
+            sum += acc[i][j];
+        }
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float p = __fdiv_rn(acc[i][j], sum);
+            const float r = __fmul_rn(__fadd_rn(p, bv[j]), scale);
+            acc[i][j] = __fdiv_rn(1.f, 1.f + expf(-r));
+        }
+    }
+
+    // Transpose through shared memory, pixel-major with an odd pitch:
+    // os[(m_local * T_N + n_local) * OS_PITCH + co].
+    __syncthreads();
+    float *os = sm;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int co = (j < 4 ? 4 * g + j : 64 + 4 * g + (j - 4));
+#pragma unroll
+        for (int i = 0; i < 8; ++i) os[(warp * T_N + 8 * h + i) * OS_PITCH + co] = acc[i][j];
+    }
+    __syncthreads();
+    float *on = out + (long long)n_img * COUT_T * Ho * Wo;
+    for (int e = tid; e < COUT_T * T_M * T_N; e += blockDim.x) {
+        const int nl = e % T_N, ml = (e / T_N) % T_M, co = e / (T_N * T_M);
+        const int oh = 2 * (m0 + ml) + py, ow = 2 * (n0 + nl) + px;
+        if (oh < Ho && ow < Wo) on[((long long)co * Ho + oh) * Wo + ow] = os[(ml * T_N + nl) * OS_PITCH + co];
+    }
+}
+
+// Gather form of one conv-transpose output.
+__device__ __forceinline__ float convt_gather(const float *__restrict__ xn, const float *__restrict__ w,
+                                              float cbv, int Cin, int H, int W, int Cout, int k, int s,
+                                              int p, int co, int oh, int ow) {
+    float y = cbv;
+    for (int kh = 0; kh < k; ++kh) {
+        const int th = oh + p - kh;
+        if (th < 0 || th % s) continue;
+        const int ih = th / s;
+        if (ih >= H) continue;
+        for (int kw = 0; kw < k; ++kw) {
+            const int tw = ow + p - kw;
+            if (tw < 0 || tw % s) continue;
+            const int iw = tw / s;
+            if (iw >= W) continue;
+            for (int ci = 0; ci < Cin; ++ci)
+                y = fmaf(__ldg(xn + ((long long)ci * H + ih) * W + iw),
+                         __ldg(w + (((long long)ci * Cout + co) * k + kh) * k + kw), y);
+        }
+    }
+    return y;
+}
+
+__global__ void convt_direct_kernel(const float *__restrict__ x, const float *__restrict__ w,
+                                    const float *__restrict__ cb, const float *__restrict__ bias,
+                                    float scale, float *__restrict__ out, int N, int Cin, int H, int W,
+                                    int Cout, int k, int s, int p, int Ho, int Wo) {
+    const long long total = (long long)N * Ho * Wo;
+    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const int ow = (int)(idx % Wo);
+        const long long t = idx / Wo;
+        const int oh = (int)(t % Ho);
+        const int n = (int)(t / Ho);
+        const float *xn = x + (long long)n * Cin * H * W;
+        float mx = -INFINITY, sum = 0.f;
+        for (int co = 0; co < Cout; ++co) {
+            const float y = convt_gather(xn, w, cb ? __ldg(cb + co) : 0.f, Cin, H, W, Cout, k, s, p, co, oh, ow);
+            if (y > mx) {
+                sum = sum * expf(mx - y) + 1.f;
+                mx = y;
+            } else {
+                sum += expf(y - mx);
+            }
+        }
+        for (int co = 0; co < Cout; ++co) {
+            const float y = convt_gather(xn, w, cb ? __ldg(cb + co) : 0.f, Cin, H, W, Cout, k, s, p, co, oh, ow);
+            const float pr = __fdiv_rn(expf(y - mx), sum);
+            const float r = __fmul_rn(__fadd_rn(pr, __ldg(bias + co)), scale);
+            out[(((long long)n * Cout + co) * Ho + oh) * Wo + ow] = __fdiv_rn(1.f, 1.f + expf(-r));
+        }
+    }
+}
+
+}  // namespace
+
+size_t convt_workspace_bytes(int Cin, int Cout, int k, int s, int p) {
+    if (k == 4 && s == 2 && p == 1 && Cout == COUT_T) return (size_t)16 * Cin * Cout * sizeof(float);
+    return 0;
+}
+
+fw_status convt_launch(const float *x, int N, int Cin, int H, int W, const float *w, const float *cb,
+                       int Cout, int k, int s, int p, int op, const float *bias, float scale, float *out,
+                       int Ho, int Wo, void *ws, size_t ws_bytes, cudaStream_t st) {
+    const size_t need = convt_workspace_bytes(Cin, Cout, k, s, p);
+    if (need > 0) {
+        if (!ws || ws_bytes < need) return FW_ERR_NULL;
+        float *wp = static_cast<float *>(ws);
+        convt_prepack_kernel<<<(unsigned)min(1024LL, (16LL * Cin * Cout + 255) / 256), 256, 0, st>>>(w, wp, Cin, Cout);
+        note_launch();
+        fw_status rc = launch_status(cudaGetLastError());
+        if (rc != FW_OK) return rc;
+        const int Mp = (Ho + 1) / 2, Np = (Wo + 1) / 2;  // phase-grid extent (phase 0)
+        const int tiles_m = (Mp + T_M - 1) / T_M, tiles_n = (Np + T_N - 1) / T_N;
+        const size_t smem = (size_t)CK * (XS_CHUNK + WS_CHUNK) * sizeof(float);
+        const size_t smem_out = (size_t)OS_PITCH * T_M * T_N * sizeof(float);
+        const size_t smem_all = smem > smem_out ? smem : smem_out;
+        cudaError_t e = cudaFuncSetAttribute(convt_k4s2_ffma_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_all);
+        if (e != cudaSuccess) return launch_status(e);
+        if (N > 65535) return FW_ERR_UNSUPPORTED;
+        dim3 grid(tiles_m * tiles_n, 4, N);
+        convt_k4s2_ffma_kernel<<<grid, 256, smem_all, st>>>(x, wp, cb, bias, scale, out, Cin, H, W, Ho, Wo,
+                                                            tiles_n);
+        note_launch();
+        return launch_status(cudaGetLastError());
+    }
+    (void)op;
+    const long long total = (long long)N * Ho * Wo;
+    const int threads = 128;
+    long long blocks = (total + threads - 1) / threads;
+    if (blocks > 152LL * 64) blocks = 152LL * 64;
+    convt_direct_kernel<<<(unsigned)blocks, threads, 0, st>>>(x, w, cb, bias, scale, out, N, Cin, H, W, Cout,
+                                                              k, s, p, Ho, Wo);
+    note_launch();
+    return launch_status(cudaGetLastError());
+}
+
+}  // namespace fw

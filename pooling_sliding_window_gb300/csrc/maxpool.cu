@@ -1,0 +1,255 @@
+// maxpool.cu -- MaxPool2d kernels (trace "Kimi-K2.6 l1_p42": MaxPool2d(k=4, s=1,
+// p=1, d=1) on [32,64,512,512], -inf padding, output 511x511).
+//
+// Streaming kernel (stride 1, dilation 1, W % 4 == 0):
+//   * one CTA per (plane, band of output rows); thread t owns input and output
+//     columns [4t, 4t+4) (threads past the row read -inf guard columns);
+//   * input rows of the band stream HBM -> shared memory through the TMA bulk-copy
+//     engine (one cp.async.bulk per row) into a ring of NSTAGE slots, each slot
+//     holding `rps` rows; an mbarrier per slot completes on the copied bytes;
+//   * each row is read once from shared memory (float4 + edge scalars from -inf
+//     guard columns, which realise the padding), reduced horizontally, and kept
+//     in a K-deep register ring; every new row completes one output row, reduced
+//     vertically in kh order (separable max: the page's row-max-then-column-max
+//     decomposition, exact for max);
+//   * output rows (W odd in general, so not 16-byte aligned) are transposed
+//     through a per-warp shared buffer so that each store instruction writes 32
+//     consecutive floats.
+// Direct kernel: one thread per output, taps read through the read-only cache;
+// covers every other (k, s, p, d, W).
+#include "fw_common.cuh"
+
+namespace fw {
+
+__device__ unsigned g_err_maxpool = 0;
+
+namespace {
+
+constexpr int NSTAGE = 4;   // ring slots
+constexpr int GUARD = 4;    // -inf columns on each side of a shared-memory row
+
+// Shared-memory row pitch (floats): GUARD -inf columns, the W data columns, and
+// -inf columns up to and past the last column any thread of the block reads.
+__host__ __device__ inline int stream_pitch(int threads) { return 4 * threads + 4 * GUARD; }
+
+template <int K, int P>
+__global__ void __launch_bounds__(1024) maxpool_s1_stream_kernel(const float *__restrict__ x,
+                                                                 float *__restrict__ out, int H, int W,
+                                                                 int Ho, int Wo, int band, int nbands,
+                                                                 int rps) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem_raw);
+    const int pitch = stream_pitch(blockDim.x);           // floats per shared row
+    float *ring = reinterpret_cast<float *>(smem_raw + 64);  // NSTAGE * rps rows
+    float *ostage = ring + (size_t)NSTAGE * rps * pitch;  // 128 floats per warp
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const long long plane = blockIdx.x / nbands;
+    const int b = blockIdx.x - (int)(plane * nbands);
+    const int r0 = b * band, r1 = min(Ho, r0 + band);       // output rows [r0, r1)
+    const int la = max(0, r0 - P), lb = min(H, r1 - 1 - P + K);  // input rows [la, lb)
+    const int nrows = max(0, lb - la);
+    const int nst = (nrows + rps - 1) / rps;               // stages of this band
+    const float *src = x + plane * (long long)H * W;
+    float *dst = out + plane * (long long)Ho * Wo;
+
+    // -inf guard columns of every slot row (never touched by the bulk copies).
+    const int nguard = pitch - W;
+    for (int i = tid; i < NSTAGE * rps * nguard; i += blockDim.x) {
+        const int row = i / nguard, g = i % nguard;
+        ring[(size_t)row * pitch + (g < GUARD ? g : W + g)] = -INFINITY;
+    }
+    if (tid == 0) {
+        for (int s = 0; s < NSTAGE; ++s) mbar_init(smem_u32(&bars[s]), 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    auto issue = [&](int st) {  // thread 0 only: copy stage `st` into its slot
+        const int slot = st % NSTAGE;
+        const int row0 = la + st * rps, cnt = min(rps, lb - row0);
+        const uint32_t bar = smem_u32(&bars[slot]);
+        const uint32_t row_bytes = (uint32_t)W * 4u;
+        mbar_arrive_expect_tx(bar, row_bytes * cnt);
+        for (int r = 0; r < cnt; ++r)
+            bulk_g2s(smem_u32(ring + ((size_t)slot * rps + r) * pitch + GUARD),
+                     src + (long long)(row0 + r) * W, row_bytes, bar);
+    };
+    if (tid == 0) {
+        fence_proxy_async_smem();
+        for (int st = 0; st < min(NSTAGE, nst); ++st) issue(st);
+    }
+
+    // Register ring of the last K horizontal-max rows (4 columns each).
+    float4 hist[K];
+#pragma unroll
+    for (int i = 0; i < K; ++i) hist[i] = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+
+    const int c0 = 4 * tid + GUARD;  // this thread's first column in a shared row
+    bool err = false, any_err = false;
+    int cur_stage = -1;
+    // Walk input rows ir = r0-P .. r1-2-P+K (rows outside [0,H) are all -inf).
+    const int ir_begin = r0 - P, ir_end = r1 - 1 - P + K;
+    for (int ir = ir_begin; ir < ir_end; ++ir) {
+        float4 h = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        if (ir >= la && ir < lb) {
+            const int st = (ir - la) / rps;
+            const int slot = st % NSTAGE;
+            if (st != cur_stage) {
+                cur_stage = st;
+                if (!mbar_wait_bounded(smem_u32(&bars[slot]), (uint32_t)(st / NSTAGE) & 1u)) err = true;
+            }
+            const float *row = ring + ((size_t)slot * rps + (ir - la - st * rps)) * pitch;
+            // window of 3+K values: columns 4t-P .. 4t+2-P+K
+            float v[K + 3];
+            const float4 mid = *reinterpret_cast<const float4 *>(row + c0);
+#pragma unroll
+            for (int i = 0; i < K + 3; ++i) {
+                const int c = i - P;  // offset from 4t
+                if (c == 0) v[i] = mid.x;
+                else if (c == 1) v[i] = mid.y;
+                else if (c == 2) v[i] = mid.z;
+                else if (c == 3) v[i] = mid.w;
+                else v[i] = row[c0 + c];
+            }
+            float hv[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float m = v[j];
+#pragma unroll
+                for (int kw = 1; kw < K; ++kw) m = max_update(m, v[j + kw]);
+                hv[j] = m;
+            }
+            h = make_float4(hv[0], hv[1], hv[2], hv[3]);
+            // Last row of this stage consumed: release the slot, refill it.
+            const int st_last = min(lb, la + (st + 1) * rps) - 1;
+            if (ir == st_last) {
+                if (__syncthreads_or(err)) {
+                    if (tid == 0) atomicOr(&g_err_maxpool, DEVERR_TIMEOUT);
+                    any_err = true;
+                    break;
+                }
+                if (tid == 0 && st + NSTAGE < nst) {
+                    fence_proxy_async_smem();
+                    issue(st + NSTAGE);
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < K - 1; ++i) hist[i] = hist[i + 1];
+        hist[K - 1] = h;
+        const int oh = ir + P - (K - 1);  // output row whose last window row is ir
+        if (oh >= r0) {
+            float4 m = hist[0];
+#pragma unroll
+            for (int i = 1; i < K; ++i) {
+                m.x = max_update(m.x, hist[i].x);
+                m.y = max_update(m.y, hist[i].y);
+                m.z = max_update(m.z, hist[i].z);
+                m.w = max_update(m.w, hist[i].w);
+            }
+            float *os = ostage + warp * 128;
+            __syncwarp();
+            *reinterpret_cast<float4 *>(os + lane * 4) = m;
+            __syncwarp();
+            float *orow = dst + (long long)oh * Wo + warp * 128;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int c = q * 32 + lane;
+                if (warp * 128 + c < Wo) orow[c] = os[c];
+            }
+        }
+    }
+    if (any_err && tid == 0) {
+        // Drain copies still in flight into this CTA's shared memory (bounded).
+        for (int st = max(0, cur_stage); st < min(nst, cur_stage + NSTAGE); ++st)
+            mbar_wait_bounded(smem_u32(&bars[st % NSTAGE]), (uint32_t)(st / NSTAGE) & 1u);
+    }
+}
+
+__global__ void maxpool_direct_kernel(const float *__restrict__ x, float *__restrict__ out,
+                                      long long NC, int H, int W, int Ho, int Wo, int k, int s, int p,
+                                      int d) {
+    const long long total = NC * Ho * Wo;
+    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const int ow = (int)(idx % Wo);
+        const long long t = idx / Wo;
+        const int oh = (int)(t % Ho);
+        const long long nc = t / Ho;
+        const float *plane = x + nc * (long long)H * W;
+        float m = -INFINITY;
+        for (int i = 0; i < k; ++i) {
+            const int ih = oh * s - p + i * d;
+            const bool rin = ih >= 0 && ih < H;
+            for (int j = 0; j < k; ++j) {
+                const int iw = ow * s - p + j * d;
+                const float v = (rin && iw >= 0 && iw < W) ? __ldg(plane + (long long)ih * W + iw) : -INFINITY;
+                m = max_update(m, v);
+            }
+        }
+        out[idx] = m;
+    }
+}
+
+template <int K, int P>
+fw_status launch_stream(const float *x, float *out, long long NC, int H, int W, int Ho, int Wo,
+                        cudaStream_t st) {
+    // Threads cover every output column group; those past W/4 read -inf guards.
+    const int threads = ((max(W, Wo) + 3) / 4 + 31) / 32 * 32;
+    if (threads > 1024) return FW_ERR_UNSUPPORTED;
+    const int pitch = stream_pitch(threads);
+    const int row_bytes = W * 4;
+    const int rps = max(1, min(8, 8192 / row_bytes));
+    const size_t smem = 64 + (size_t)NSTAGE * rps * pitch * 4 + (size_t)(threads / 32) * 128 * 4;
+    // Bands of output rows: long enough that the K-1 halo rows re-read per band
+    // (mostly from L2) stay a few percent of the band.
+    const int band = Ho <= 128 ? Ho : 128;
+    const int nbands = (Ho + band - 1) / band;
+    const long long blocks = NC * nbands;
+    if (blocks > 0x7fffffffLL) return FW_ERR_SHAPE;
+    cudaError_t e = cudaFuncSetAttribute(maxpool_s1_stream_kernel<K, P>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return launch_status(e);
+    maxpool_s1_stream_kernel<K, P><<<(unsigned)blocks, threads, smem, st>>>(x, out, H, W, Ho, Wo, band,
+                                                                           nbands, rps);
+    note_launch();
+    return launch_status(cudaGetLastError());
+}
+
+using StreamFn = fw_status (*)(const float *, float *, long long, int, int, int, int, cudaStream_t);
+
+StreamFn stream_fn(int k, int p) {
+#define FW_MP_CASE(KK, PP) \
+    if (k == KK && p == PP) return launch_stream<KK, PP>;
+    FW_MP_CASE(1, 0) FW_MP_CASE(2, 0) FW_MP_CASE(2, 1) FW_MP_CASE(3, 0) FW_MP_CASE(3, 1)
+    FW_MP_CASE(4, 0) FW_MP_CASE(4, 1) FW_MP_CASE(4, 2) FW_MP_CASE(5, 0) FW_MP_CASE(5, 1) FW_MP_CASE(5, 2)
+#undef FW_MP_CASE
+    return nullptr;
+}
+
+}  // namespace
+
+fw_status maxpool2d_launch(const float *x, long long NC, int H, int W, int k, int s, int p, int d,
+                           int Ho, int Wo, float *out, cudaStream_t st) {
+    const bool aligned = ((reinterpret_cast<uintptr_t>(x) & 15u) == 0);
+    if (s == 1 && d == 1 && aligned && W % 4 == 0 && W >= 32 && W <= 4000) {
+        if (StreamFn f = stream_fn(k, p)) return f(x, out, NC, H, W, Ho, Wo, st);
+    }
+    const long long total = NC * Ho * Wo;
+    const int threads = 256;
+    long long blocks = (total + threads - 1) / threads;
+    if (blocks > 152LL * 64) blocks = 152LL * 64;
+    maxpool_direct_kernel<<<(unsigned)blocks, threads, 0, st>>>(x, out, NC, H, W, Ho, Wo, k, s, p, d);
+    note_launch();
+    return launch_status(cudaGetLastError());
+}
+
+unsigned maxpool_read_and_clear_error() {
+    unsigned v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_err_maxpool, sizeof(v)) != cudaSuccess) return DEVERR_INTERNAL;
+    if (v) cudaMemcpyToSymbol(g_err_maxpool, &zero, sizeof(zero));
+    return v;
+}
+
+}  // namespace fw

@@ -1,0 +1,209 @@
+"""Python binding of libfusedwin (ctypes; argument marshalling only).
+
+Each function has the name of the C entry point it calls and takes torch
+tensors.  Device tensors are passed straight through (the call is enqueued on
+torch's current CUDA stream and returns without synchronising).  Host tensors
+are accepted too: they are copied to the device, the C entry point runs there,
+and the result is copied back into a host tensor; this is the path an end-to-end
+caller with host buffers takes.  Every operator runs in the library's CUDA
+kernels; if the library cannot be loaded the call raises -- there is no other
+implementation to fall back on.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import torch
+
+from . import build as _build
+
+_lib = None
+
+STATUS = {0: "FW_OK", 1: "FW_ERR_NULL", 2: "FW_ERR_SHAPE", 3: "FW_ERR_PARAM", 4: "FW_ERR_ALIAS",
+          5: "FW_ERR_ALIGN", 6: "FW_ERR_UNSUPPORTED", 7: "FW_ERR_LAUNCH", 8: "FW_ERR_TIMEOUT",
+          9: "FW_ERR_INTERNAL"}
+
+# Every symbol include/fusedwin.h declares.
+EXPORTS = ("fw_status_string", "fw_version", "fw_conv2d_pool_out_shape", "fw_maxpool2d_out_shape",
+           "fw_convt_out_shape", "fw_conv2d_tanh_scale_bias_maxpool", "fw_maxpool2d",
+           "fw_convtranspose2d_softmax_bias_scale_sigmoid", "fw_convt_workspace_size",
+           "fw_check_device_errors", "fw_launch_count")
+
+
+class FusedWinError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        msg = lib().fw_status_string(code).decode()
+        super().__init__(f"{where}: {msg}")
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """Load libfusedwin.so (building it first if the sources are newer)."""
+    global _lib
+    if _lib is None:
+        path = _build.build() if os.environ.get("FUSEDWIN_NO_BUILD") is None else _build.LIB
+        L = C.CDLL(path)
+        I, P, F, U64 = C.c_int, C.c_void_p, C.c_float, C.c_ulonglong
+        IP = C.POINTER(C.c_int)
+        L.fw_status_string.restype = C.c_char_p
+        L.fw_status_string.argtypes = [I]
+        L.fw_version.restype = I
+        L.fw_launch_count.restype = U64
+        for name, n in (("fw_conv2d_pool_out_shape", 6), ("fw_maxpool2d_out_shape", 6),
+                        ("fw_convt_out_shape", 6)):
+            f = getattr(L, name)
+            f.restype = I
+            f.argtypes = [I] * n + [IP, IP]
+        L.fw_conv2d_tanh_scale_bias_maxpool.restype = I
+        L.fw_conv2d_tanh_scale_bias_maxpool.argtypes = [P, I, I, I, I, P, P, I, I, I, F, P, I, I, P, P]
+        L.fw_maxpool2d.restype = I
+        L.fw_maxpool2d.argtypes = [P, I, I, I, I, I, I, I, I, P, P]
+        L.fw_convtranspose2d_softmax_bias_scale_sigmoid.restype = I
+        L.fw_convtranspose2d_softmax_bias_scale_sigmoid.argtypes = [
+            P, I, I, I, I, P, P, I, I, I, I, I, P, F, P, P, U64, P]
+        L.fw_convt_workspace_size.restype = U64
+        L.fw_convt_workspace_size.argtypes = [I, I, I, I, I]
+        L.fw_check_device_errors.restype = I
+        L.fw_check_device_errors.argtypes = [P]
+        _lib = L
+    return _lib
+
+
+def _check(code: int, where: str):
+    if code != 0:
+        raise FusedWinError(code, where)
+
+
+def _shape2(fn, *args):
+    ho, wo = C.c_int(0), C.c_int(0)
+    _check(getattr(lib(), fn)(*args, C.byref(ho), C.byref(wo)), fn)
+    return ho.value, wo.value
+
+
+def fw_conv2d_pool_out_shape(H, W, KH, KW, pool_k, pool_s=0):
+    return _shape2("fw_conv2d_pool_out_shape", H, W, KH, KW, pool_k, pool_s)
+
+
+def fw_maxpool2d_out_shape(H, W, k, s, p, d):
+    return _shape2("fw_maxpool2d_out_shape", H, W, k, s, p, d)
+
+
+def fw_convt_out_shape(H, W, k, s, p, op):
+    return _shape2("fw_convt_out_shape", H, W, k, s, p, op)
+
+
+def fw_convt_workspace_size(Cin, Cout, k, s, p) -> int:
+    return int(lib().fw_convt_workspace_size(Cin, Cout, k, s, p))
+
+
+def fw_launch_count() -> int:
+    return int(lib().fw_launch_count())
+
+
+def fw_check_device_errors(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    _check(lib().fw_check_device_errors(C.c_void_p(s.cuda_stream)), "fw_check_device_errors")
+
+
+# ----------------------------------------------------------------- helpers --
+
+def _dev(t, name, device):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.float32:
+        raise TypeError(f"{name} must be a float32 torch.Tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous (dense NCHW)")
+    if t.device.type != "cuda":
+        t = t.to(device, non_blocking=True)
+    return t
+
+
+def _ptr(t):
+    return C.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _device_of(x):
+    if x.device.type == "cuda":
+        return x.device
+    if not torch.cuda.is_available():
+        raise RuntimeError("libfusedwin needs a CUDA device; none is available")
+    return torch.device("cuda", torch.cuda.current_device())
+
+
+def _finish(out_dev, out, host):
+    if not host:
+        return out_dev
+    if out is None:
+        out = torch.empty(out_dev.shape, dtype=torch.float32, pin_memory=True)
+    out.copy_(out_dev, non_blocking=True)
+    torch.cuda.current_stream(out_dev.device).synchronize()
+    return out
+
+
+# --------------------------------------------------------------- operators --
+
+def fw_conv2d_tanh_scale_bias_maxpool(x, w, conv_b, bias, scale, pool_k, pool_s=0, out=None):
+    """out = MaxPool2d(pool_k, pool_s)(bias + scale * tanh(conv2d(x, w, conv_b)))."""
+    host = x.device.type != "cuda"
+    dev = _device_of(x)
+    xd, wd = _dev(x, "x", dev), _dev(w, "w", dev)
+    cbd, bd = _dev(conv_b, "conv_b", dev), _dev(bias.reshape(-1), "bias", dev)
+    N, Cin, H, W = xd.shape
+    Cout, _, KH, KW = wd.shape
+    Ho, Wo = fw_conv2d_pool_out_shape(H, W, KH, KW, pool_k, pool_s)
+    od = out if (out is not None and not host) else torch.empty((N, Cout, Ho, Wo), device=dev,
+                                                                 dtype=torch.float32)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    with torch.cuda.device(dev):
+        _check(lib().fw_conv2d_tanh_scale_bias_maxpool(
+            _ptr(xd), N, Cin, H, W, _ptr(wd), _ptr(cbd), Cout, KH, KW, float(scale), _ptr(bd),
+            pool_k, pool_s, _ptr(od), C.c_void_p(stream)), "fw_conv2d_tanh_scale_bias_maxpool")
+    return _finish(od, out, host)
+
+
+def fw_maxpool2d(x, k, s=None, p=0, d=1, out=None):
+    """MaxPool2d(kernel k, stride s (default k), padding p (-inf), dilation d)."""
+    s = k if s is None else s
+    host = x.device.type != "cuda"
+    dev = _device_of(x)
+    xd = _dev(x, "x", dev)
+    N, Cc, H, W = xd.shape
+    Ho, Wo = fw_maxpool2d_out_shape(H, W, k, s, p, d)
+    od = out if (out is not None and not host) else torch.empty((N, Cc, Ho, Wo), device=dev,
+                                                                 dtype=torch.float32)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    with torch.cuda.device(dev):
+        _check(lib().fw_maxpool2d(_ptr(xd), N, Cc, H, W, k, s, p, d, _ptr(od), C.c_void_p(stream)),
+               "fw_maxpool2d")
+    return _finish(od, out, host)
+
+
+def fw_convtranspose2d_softmax_bias_scale_sigmoid(x, w, conv_b, bias, scale, stride=2, padding=1,
+                                                  output_padding=1, out=None, workspace=None):
+    """out = sigmoid((softmax(conv_transpose2d(x, w, conv_b), dim=1) + bias) * scale)."""
+    host = x.device.type != "cuda"
+    dev = _device_of(x)
+    xd, wd = _dev(x, "x", dev), _dev(w, "w", dev)
+    cbd, bd = _dev(conv_b, "conv_b", dev), _dev(bias.reshape(-1), "bias", dev)
+    N, Cin, H, W = xd.shape
+    _, Cout, K, _ = wd.shape
+    Ho, Wo = fw_convt_out_shape(H, W, K, stride, padding, output_padding)
+    need = fw_convt_workspace_size(Cin, Cout, K, stride, padding)
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty((need + 3) // 4, device=dev, dtype=torch.float32)
+    od = out if (out is not None and not host) else torch.empty((N, Cout, Ho, Wo), device=dev,
+                                                                 dtype=torch.float32)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    with torch.cuda.device(dev):
+        _check(lib().fw_convtranspose2d_softmax_bias_scale_sigmoid(
+            _ptr(xd), N, Cin, H, W, _ptr(wd), _ptr(cbd), Cout, K, stride, padding, output_padding,
+            _ptr(bd), float(scale), _ptr(od), _ptr(workspace), ws_bytes, C.c_void_p(stream)),
+            "fw_convtranspose2d_softmax_bias_scale_sigmoid")
+    return _finish(od, out, host)

@@ -1,0 +1,63 @@
+"""Shared helpers of the GPU parity tests (CUDA path through the C ABI vs the oracle)."""
+from __future__ import annotations
+
+import os
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+import torch
+
+from oracle import oracle as O
+from pooling_sliding_window_gb300 import fusedwin as FW
+from pooling_sliding_window_gb300 import synth
+
+# Tolerance of the FP32-FMA conv paths against the oracle (max abs error).
+TOL_FFMA = 1e-5
+
+POOL = ThreadPoolExecutor(max(1, min(16, os.cpu_count() or 1)))  # oracle calls release the GIL
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def host(t):
+    torch.cuda.synchronize()
+    return t.cpu().numpy()
+
+
+def bits_equal(a, b):
+    """Bit-exact float32 equality, treating any two NaNs as equal."""
+    a = np.asarray(a, np.float32)
+    b = np.asarray(b, np.float32)
+    nan = np.isnan(a) & np.isnan(b)
+    same = a.view(np.uint32) == b.view(np.uint32)
+    return bool(np.all(same | nan)), int(np.sum(~(same | nan)))
+
+
+def assert_bits_equal(a, b, what=""):
+    ok, bad = bits_equal(a, b)
+    assert ok, f"{what}: {bad} elements differ bitwise"
+
+
+def assert_close(got, want, tol, what=""):
+    got, want = np.asarray(got), np.asarray(want)
+    assert got.shape == want.shape, (got.shape, want.shape)
+    err = np.abs(got.astype(np.float64) - want.astype(np.float64))
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    m = float(err.max()) if err.size else 0.0
+    assert m <= tol, f"{what}: max abs err {m:.3e} > {tol:.1e} at {np.unravel_index(err.argmax(), err.shape)}"
+    return m
+
+
+def pmap(fn, items):
+    return list(POOL.map(fn, items))
+
+
+def sample_indices(shape, count, seed):
+    rng = np.random.default_rng(seed)
+    return [tuple(int(rng.integers(0, s)) for s in shape) for _ in range(count)]
+
+
+__all__ = ["O", "FW", "synth", "TOL_FFMA", "dev", "host", "assert_bits_equal", "assert_close", "pmap",
+           "sample_indices", "bits_equal"]

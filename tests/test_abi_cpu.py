@@ -1,0 +1,120 @@
+"""C-ABI checks that need no GPU: the library builds and loads, exports every
+symbol the header declares, computes output shapes like the oracle, and rejects
+bad arguments on the host with the documented status before any launch."""
+import ctypes as C
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle as O
+from pooling_sliding_window_gb300 import fusedwin as FW
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fusedwin.h")
+P = C.c_void_p
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fw_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_and_exports():
+    names = declared_functions()
+    assert set(names) == set(FW.EXPORTS)
+    L = FW.lib()
+    for n in names:
+        assert hasattr(L, n), n
+    assert L.fw_version() >= 100
+    for code, name in FW.STATUS.items():
+        assert L.fw_status_string(code).decode().startswith(name)
+
+
+def test_library_is_in_tree_and_sm103a_only():
+    assert FW.library_path().startswith(os.path.join(ROOT, "pooling_sliding_window_gb300"))
+    from pooling_sliding_window_gb300 import build
+    assert build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+@pytest.mark.parametrize("H,k,s,p,d", [(512, 4, 1, 1, 1), (13, 3, 2, 1, 2), (7, 5, 3, 2, 1), (1, 1, 1, 1, 1)])
+def test_maxpool_shape_matches_oracle(H, k, s, p, d):
+    assert FW.fw_maxpool2d_out_shape(H, H + 1, k, s, p, d) == (O.pool_out_size(H, k, s, p, d),
+                                                              O.pool_out_size(H + 1, k, s, p, d))
+
+
+@pytest.mark.parametrize("H,pk,ps", [(256, 4, 0), (127, 2, 2), (255, 4, 4), (64, 4, 0), (20, 3, 2)])
+def test_convpool_shape_matches_oracle(H, pk, ps):
+    hc = O.conv2d_out_size(H, 3)
+    want = O.pool_out_size(hc, pk, ps or pk)
+    assert FW.fw_conv2d_pool_out_shape(H, H, 3, 3, pk, ps) == (want, want)
+
+
+@pytest.mark.parametrize("H,k,s,p,op", [(64, 4, 2, 1, 1), (5, 3, 2, 0, 1), (9, 5, 3, 2, 2), (4, 4, 2, 1, 0)])
+def test_convt_shape_matches_oracle(H, k, s, p, op):
+    want = O.convt_out_size(H, k, s, p, op)
+    assert FW.fw_convt_out_shape(H, H, k, s, p, op) == (want, want)
+
+
+def test_shape_errors():
+    L = FW.lib()
+    a, b = C.c_int(), C.c_int()
+    assert L.fw_maxpool2d_out_shape(512, 512, 4, 1, 1, 1, None, None) == 1  # NULL out pointers
+    assert L.fw_maxpool2d_out_shape(0, 5, 2, 1, 0, 1, C.byref(a), C.byref(b)) == 2
+    assert L.fw_maxpool2d_out_shape(5, 5, 0, 1, 0, 1, C.byref(a), C.byref(b)) == 3
+    assert L.fw_maxpool2d_out_shape(5, 5, 2, 0, 0, 1, C.byref(a), C.byref(b)) == 3
+    assert L.fw_maxpool2d_out_shape(5, 5, 2, 1, -1, 1, C.byref(a), C.byref(b)) == 3
+    assert L.fw_maxpool2d_out_shape(2, 2, 3, 1, 0, 1, C.byref(a), C.byref(b)) == 2  # window > input
+    assert L.fw_conv2d_pool_out_shape(4, 4, 3, 3, 4, 4, C.byref(a), C.byref(b)) == 2
+    assert L.fw_convt_out_shape(4, 4, 4, 2, 1, 2, C.byref(a), C.byref(b)) == 3  # op >= s
+
+
+def test_operator_argument_errors_without_launch():
+    """Every check runs on the host before a launch; none of these calls needs a GPU."""
+    L = FW.lib()
+    x, w, b, o = P(0x10000), P(0x20000), P(0x30000), P(0x40000000)
+    # maxpool
+    assert L.fw_maxpool2d(None, 1, 1, 8, 8, 2, 2, 0, 1, o, None) == 1
+    assert L.fw_maxpool2d(x, 0, 1, 8, 8, 2, 2, 0, 1, o, None) == 2
+    assert L.fw_maxpool2d(x, 1, 1, 8, 8, 2, 2, 0, 0, o, None) == 3
+    assert L.fw_maxpool2d(P(0x10002), 1, 1, 8, 8, 2, 2, 0, 1, o, None) == 5
+    assert L.fw_maxpool2d(x, 1, 1, 8, 8, 2, 2, 0, 1, P(0x10000 + 64), None) == 4  # out inside x
+    # conv+pool
+    args = lambda **kw: dict(dict(x=x, N=1, Cin=8, H=16, W=16, w=w, cb=None, Cout=4, KH=3, KW=3,
+                                  scale=2.0, bias=b, pk=4, ps=0, out=o), **kw)
+    call = lambda a: L.fw_conv2d_tanh_scale_bias_maxpool(a["x"], a["N"], a["Cin"], a["H"], a["W"], a["w"],
+                                                          a["cb"], a["Cout"], a["KH"], a["KW"], a["scale"],
+                                                          a["bias"], a["pk"], a["ps"], a["out"], None)
+    assert call(args(bias=None)) == 1
+    assert call(args(Cout=0)) == 2
+    assert call(args(H=4)) == 2
+    assert call(args(scale=float("inf"))) == 3
+    assert call(args(scale=float("nan"))) == 3
+    assert call(args(pk=0)) == 3
+    assert call(args(out=P(0x20000 + 16))) == 4  # out overlaps w
+    assert call(args(out=b)) == 4
+    assert call(args(w=P(0x20001))) == 5
+    # conv-transpose
+    need = FW.fw_convt_workspace_size(64, 128, 4, 2, 1)
+    assert need == 16 * 64 * 128 * 4
+    ws = P(0x80000000)
+    ct = lambda **kw: L.fw_convtranspose2d_softmax_bias_scale_sigmoid(
+        kw.get("x", x), 1, 64, 8, 8, w, None, kw.get("Cout", 128), 4, 2, 1, kw.get("op", 1), b, 2.0,
+        kw.get("out", o), kw.get("ws", ws), kw.get("wsb", need), None)
+    assert ct(ws=None) == 1          # workspace required for the tiled path
+    assert ct(wsb=need - 4) == 1     # too small
+    assert ct(ws=P(0x80000004)) == 5  # workspace not 16-byte aligned
+    assert ct(op=2) == 3
+    assert ct(Cout=2048) == 6
+    assert ct(out=P(0x80000000 + 4096)) == 4  # out overlaps workspace
+
+
+def test_product_path_fails_loudly_without_gpu():
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    x = torch.zeros(1, 1, 8, 8)
+    with pytest.raises(RuntimeError, match="CUDA"):
+        FW.fw_maxpool2d(x, 2)
