@@ -1,0 +1,485 @@
+"""Benchmark of the fused sliding-window hot path on GB300.
+
+One step = one pass of the whole path, each operator on its full workload:
+  conv+pool : x [128,8,256,256] -> Conv2d(8->64,k3) -> tanh -> *2 -> +bias -> MaxPool2d(4) -> [128,64,63,63]
+  maxpool   : x [32,64,512,512] -> MaxPool2d(k4,s1,p1,d1) -> [32,64,511,511]
+  convT     : x [128,64,64,64] -> ConvTranspose2d(64->128,k4,s2,p1,op1) -> softmax(1) -> +bias -> *2
+              -> sigmoid -> [128,128,129,129]
+all three enqueued on one CUDA stream through the C ABI (ctypes binding).
+
+`value` is the fused conv+pool throughput in TFLOP/s (algorithmic FLOPs: the
+conv outputs the pool consumes, 2*72 FLOP each); the maxpool's HBM GB/s and the
+conv-transpose's TFLOP/s are reported beside it, each with its roofline
+fraction.  Inputs are larger than L2 (268 MB, 2.15 GB, 134 MB), so no flush is
+needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun every rank runs the full per-GPU workload (weak scaling, no data
+exchange); rank 0 prints one JSON line with the max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused conv+pool TFLOP/s & maxpool2d HBM GB/s, % of GB300 roofline"
+UNIT = "TFLOP/s"
+
+# Workloads
+CP = dict(N=128, Cin=8, H=256, W=256, Cout=64, k=3, pool=4, scale=2.0)
+MP = dict(N=32, C=64, H=512, W=512, k=4, s=1, p=1, d=1)
+CT = dict(N=128, Cin=64, H=64, W=64, Cout=128, k=4, s=2, p=1, op=1, scale=2.0)
+
+
+def cp_flops(N=CP["N"], Cout=CP["Cout"], Cin=CP["Cin"], ho=63, pool=4, k=3):
+    """Algorithmic FLOPs of conv+pool: the conv outputs the pool windows consume."""
+    return 2.0 * N * Cout * (pool * ho) ** 2 * Cin * k * k
+
+
+def mp_bytes(N=MP["N"], C=MP["C"], H=512, W=512, ho=511, wo=511):
+    return 4.0 * N * C * (H * W + ho * wo)
+
+
+def ct_flops(N=CT["N"], Cin=CT["Cin"], Cout=CT["Cout"], H=64, W=64, k=4, s=2, p=1, op=1):
+    """Algorithmic FLOPs of the conv-transpose: valid taps only (2 FLOP per MAC)."""
+    Ho = (H - 1) * s - 2 * p + k - 1 + op + 1
+
+    def taps(n_in, n_out):
+        t = 0
+        for i in range(n_in):
+            for kk in range(k):
+                o = i * s - p + kk
+                t += 0 <= o < n_out
+        return t
+
+    return 2.0 * N * Cin * Cout * taps(H, Ho) * taps(W, Ho)
+
+
+CP_FLOPS, MP_BYTES, CT_FLOPS = cp_flops(), mp_bytes(), ct_flops()
+CT_BYTES = 4.0 * (CT["N"] * CT["Cin"] * 64 * 64 + CT["N"] * CT["Cout"] * 129 * 129)
+CP_BYTES = 4.0 * (CP["N"] * CP["Cin"] * 256 * 256 + CP["N"] * CP["Cout"] * 63 * 63)
+
+
+# ---------------------------------------------------------------- helpers --
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def peaks():
+    """Roofline denominators: measured HBM copy GB/s; FP32 FMA peak from unit counts and clock."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    src = "measured"
+    try:
+        mp = json.load(open(path))
+        hbm = float(mp["hbm_gbs"])
+        sm_max = float(mp.get("sm_max_mhz", 2070.0))
+    except Exception:  # noqa: BLE001
+        hbm, sm_max, src = 6800.0, 2070.0, "fallback"
+    return dict(hbm_gbs=hbm, hbm_src=src, sm_max_mhz=sm_max)
+
+
+def fp32_peak_tflops(sm_count, mhz):
+    # 128 FP32 FMA lanes per SM, 2 FLOP per FMA.
+    return sm_count * 128 * 2 * mhz * 1e6 / 1e12
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms in the background."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:  # noqa: BLE001
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:  # noqa: BLE001
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def traffic_for(kernel_key):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel's source
+    is unchanged since that capture (else None)."""
+    try:
+        t = json.load(open(os.path.join(ROOT, "profiles", "ncu_traffic.json")))
+        ent = t[kernel_key]
+        src = os.path.join(ROOT, "pooling_sliding_window_gb300", "csrc", ent["source"])
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        if h != ent["source_sha"]:
+            return None
+        return float(ent["dram_bytes_per_launch"])
+    except Exception:  # noqa: BLE001
+        return None
+
+
+# ------------------------------------------------------------------ inputs --
+
+def make_inputs(seed=0, only=None):
+    from pooling_sliding_window_gb300 import synth
+    want = lambda n: only is None or only == n
+    cp = synth.convpool_inputs(CP["N"], CP["Cin"], CP["H"], CP["W"], CP["Cout"], seed=seed) if want("convpool") else {}
+    mp = synth.maxpool_inputs(MP["N"], MP["C"], MP["H"], MP["W"], seed=seed) if want("maxpool") else {}
+    ct = synth.convt_inputs(CT["N"], CT["Cin"], CT["H"], CT["W"], CT["Cout"], seed=seed) if want("convt") else {}
+    return cp, mp, ct
+
+
+def reduce_max(values, ws, device=None):
+    """Element-wise max of a list of floats over all ranks (identity when ws == 1)."""
+    if ws == 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.cpu()]
+
+
+def weak_value(units_per_rank, ws, ms):
+    """Whole-job throughput: every rank processed `units_per_rank`; `ms` is the max over ranks."""
+    return ws * units_per_rank / (ms * 1e-3)
+
+
+# -------------------------------------------------------------- CPU oracle --
+
+def oracle_sample(cp, mp, ct, budget_s=12.0):
+    """Time the oracle (single-threaded C) on bounded samples of each workload.
+    Returns per-op throughputs in the benchmark's units."""
+    from oracle import oracle as O
+    res = {}
+    # conv+pool: whole images until ~budget/2 seconds
+    t0 = time.perf_counter()
+    n = 0
+    while n < CP["N"] and (n == 0 or time.perf_counter() - t0 < budget_s / 2):
+        O.conv2d_tanh_scale_bias_maxpool(cp["x"][n:n + 1], cp["w"], cp["conv_b"], CP["scale"], cp["bias"], 4)
+        n += 1
+    dt = time.perf_counter() - t0
+    res["convpool"] = dict(tflops=cp_flops(N=n) / dt / 1e12, images=n, seconds=dt)
+    # maxpool: whole planes for ~budget/4 seconds
+    t0 = time.perf_counter()
+    planes = 0
+    while planes < MP["N"] * MP["C"] and (planes == 0 or time.perf_counter() - t0 < budget_s / 4):
+        nn, c = divmod(planes, MP["C"])
+        O.maxpool2d(mp["x"][nn:nn + 1, c:c + 1], 4, 1, 1, 1)
+        planes += 1
+    dt = time.perf_counter() - t0
+    res["maxpool"] = dict(gbs=mp_bytes(N=1, C=planes) / dt / 1e9, planes=planes, seconds=dt)
+    # conv-transpose: whole images for ~budget/4 seconds
+    t0 = time.perf_counter()
+    n = 0
+    while n < CT["N"] and (n == 0 or time.perf_counter() - t0 < budget_s / 4):
+        O.convtranspose2d_softmax_bias_scale_sigmoid(ct["x"][n:n + 1], ct["w"], ct["conv_b"], ct["bias"],
+                                                     CT["scale"])
+        n += 1
+    dt = time.perf_counter() - t0
+    res["convt"] = dict(tflops=ct_flops(N=n) / dt / 1e12, images=n, seconds=dt)
+    return res
+
+
+def cpu_baseline_obj(res):
+    cp, mpr, ctr = res["convpool"], res["maxpool"], res["convt"]
+    return {"value": cp["tflops"], "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": (f"conv+pool on {cp['images']} of 128 images ({cp['seconds']:.1f} s); "
+                       f"maxpool on {mpr['planes']} of 2048 planes ({mpr['gbs']:.3f} GB/s); "
+                       f"convT on {ctr['images']} of 128 images ({ctr['tflops'] * 1e3:.3f} GFLOP/s); "
+                       "single-threaded C, float64 sums")}
+
+
+# ---------------------------------------------------------------- reference --
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    cp, mp, ct = make_inputs()
+    for _ in range(args.warmup):
+        oracle_sample(cp, mp, ct, budget_s=2.0)
+    vals, steps = [], []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        r = oracle_sample(cp, mp, ct, budget_s=8.0)
+        steps.append(r)
+        vals.append(r["convpool"]["tflops"])
+    wall = time.perf_counter() - t0
+    v = statistics.median(vals)
+    cpu = cpu_baseline_obj(steps[-1])
+    cpu["value"] = v
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": wall * 1e3 / max(1, args.steps),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 sums, f32 stages",
+            "data": "synthetic (seeded SplitMix64 / Box-Muller, the pages' shapes)",
+            "config": config_obj(), "cpu_baseline": cpu,
+            "maxpool_hbm_gbs": statistics.median(s["maxpool"]["gbs"] for s in steps),
+            "convt_tflops": statistics.median(s["convt"]["tflops"] for s in steps),
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_obj():
+    return {"workload": ("conv+pool x[128,8,256,256] Conv2d(8->64,k3)+tanh+*2+bias+MaxPool2d(4)->[128,64,63,63]; "
+                         "maxpool x[32,64,512,512] MaxPool2d(k4,s1,p1,d1)->[32,64,511,511]; "
+                         "convT x[128,64,64,64] ConvTranspose2d(64->128,k4,s2,p1,op1)+softmax(1)+bias+*2+sigmoid"
+                         "->[128,128,129,129]"),
+            "seed": 0, "l2": "inputs larger than L2 (268 MB, 2.15 GB, 134 MB); no flush",
+            "precision": "fp32 FFMA, accurate tanhf/expf", "parallelism": "weak scaling over GPUs, no collective"}
+
+
+# ---------------------------------------------------------------- GPU arm --
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        dist.init_process_group("nccl" if args.backend == "nccl" else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from pooling_sliding_window_gb300 import fusedwin as FW
+
+    cp, mp, ct = make_inputs(seed=0, only=args.only)
+    if args.batch:  # a smaller batch of every workload (profiling cases)
+        cp = {k: (v[:args.batch] if k == "x" else v) for k, v in cp.items()}
+        mp = {k: (v[:max(1, args.batch // 4)] if k == "x" else v) for k, v in mp.items()}
+        ct = {k: (v[:args.batch] if k == "x" else v) for k, v in ct.items()}
+    pinned = {(name, k): torch.from_numpy(np.ascontiguousarray(v)).pin_memory()
+              for name, dct in (("cp", cp), ("mp", mp), ("ct", ct)) for k, v in dct.items()}
+    d = {key: t.to(dev) for key, t in pinned.items()}
+    stream = torch.cuda.current_stream(dev)
+
+    specs = []  # (name, units per rank, device op, host op, out shape)
+    if cp:
+        n = cp["x"].shape[0]
+        out_cp = torch.empty(n, CP["Cout"], 63, 63, device=dev)
+        h_cp = torch.empty(tuple(out_cp.shape), pin_memory=True)
+
+        def op_cp(src, out):
+            FW.fw_conv2d_tanh_scale_bias_maxpool(src[("cp", "x")], src[("cp", "w")], src[("cp", "conv_b")],
+                                                 src[("cp", "bias")], CP["scale"], 4, out=out)
+        specs.append(dict(name="convpool", work=cp_flops(N=n), unit="TFLOP/s", scale=1e12, bound="alu",
+                          run=lambda: op_cp(d, out_cp), e2e=lambda: op_cp(pinned, h_cp), out=h_cp,
+                          kernel="convpool3x3_ffma_kernel<4>", source="convpool.cu"))
+    if mp:
+        n = mp["x"].shape[0]
+        out_mp = torch.empty(n, MP["C"], 511, 511, device=dev)
+        h_mp = torch.empty(tuple(out_mp.shape), pin_memory=True)
+
+        def op_mp(src, out):
+            FW.fw_maxpool2d(src[("mp", "x")], 4, 1, 1, 1, out=out)
+        specs.append(dict(name="maxpool", work=mp_bytes(N=n), unit="GB/s", scale=1e9, bound="hbm",
+                          run=lambda: op_mp(d, out_mp), e2e=lambda: op_mp(pinned, h_mp), out=h_mp,
+                          kernel="maxpool_s1_stream_kernel<4,1>", source="maxpool.cu"))
+    if ct:
+        n = ct["x"].shape[0]
+        out_ct = torch.empty(n, CT["Cout"], 129, 129, device=dev)
+        h_ct = torch.empty(tuple(out_ct.shape), pin_memory=True)
+        wsz = FW.fw_convt_workspace_size(CT["Cin"], CT["Cout"], 4, 2, 1)
+        wsp = torch.empty(max(1, wsz // 4), device=dev)
+
+        def op_ct(src, out):
+            FW.fw_convtranspose2d_softmax_bias_scale_sigmoid(src[("ct", "x")], src[("ct", "w")],
+                                                             src[("ct", "conv_b")], src[("ct", "bias")],
+                                                             CT["scale"], out=out, workspace=wsp)
+        specs.append(dict(name="convt", work=ct_flops(N=n), unit="TFLOP/s", scale=1e12, bound="alu",
+                          run=lambda: op_ct(d, out_ct), e2e=lambda: op_ct(pinned, h_ct), out=h_ct,
+                          kernel="convt_k4s2_ffma_kernel (+ weight prepack)", source="convt.cu"))
+
+    def barrier():
+        if ws > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        for sp in specs:
+            sp["run"]()
+    torch.cuda.synchronize()
+    FW.fw_check_device_errors()
+
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in specs]
+          for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    launches0 = FW.fw_launch_count()
+    with ClockSampler(local) as clk:
+        time.sleep(0.3)
+        t_start.record(stream)
+        for i in range(args.steps):
+            for j, sp in enumerate(specs):
+                ev[i][j][0].record(stream)
+                sp["run"]()
+                ev[i][j][1].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    launches = FW.fw_launch_count() - launches0
+    FW.fw_check_device_errors()
+    local_ms = [t_start.elapsed_time(t_end)] + [
+        statistics.mean(ev[i][j][0].elapsed_time(ev[i][j][1]) for i in range(args.steps)) for j in range(len(specs))]
+
+    # End to end through the public API: pinned host tensors in, H2D + kernels + D2H per op.
+    for sp in specs:
+        sp["e2e"]()
+    torch.cuda.synchronize()
+    barrier()
+    e2e_steps = max(2, min(args.steps, 5))
+    e2e_local = []
+    for sp in specs:
+        ts = []
+        for _ in range(e2e_steps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            sp["e2e"]()  # returns once the result is in host memory
+            b.record(stream)
+            b.synchronize()
+            ts.append(a.elapsed_time(b))
+        e2e_local.append(statistics.mean(ts))
+    red = reduce_max(local_ms + e2e_local, ws, device=dev if args.backend == "nccl" else None)
+    total_ms, op_ms, e2e_ms = red[0], red[1:1 + len(specs)], red[1 + len(specs):]
+    h2d = sum(t.numel() * t.element_size() for t in pinned.values())
+    d2h = sum(sp["out"].numel() * 4 for sp in specs)
+
+    if rank != 0:
+        if ws > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return 0
+
+    pk = peaks()
+    props = torch.cuda.get_device_properties(dev)
+    fp32_peak = fp32_peak_tflops(props.multi_processor_count, pk["sm_max_mhz"])
+    ops = {}
+    for sp, ms in zip(specs, op_ms):
+        ach = sp["work"] / (ms * 1e-3) / sp["scale"]
+        peak = fp32_peak if sp["bound"] == "alu" else pk["hbm_gbs"]
+        ops[sp["name"]] = dict(ms=ms, achieved=ach, unit=sp["unit"], bound=sp["bound"], peak=peak,
+                               frac=ach / peak, work_per_launch=sp["work"], kernel=sp["kernel"])
+    dom_i = max(range(len(specs)), key=lambda j: op_ms[j])
+    dom = specs[dom_i]
+    dv = ops[dom["name"]]
+    roofline = {"bound": dv["bound"], "achieved": dv["achieved"], "peak": dv["peak"], "unit": dv["unit"],
+                "frac": dv["frac"], "traffic": traffic_for(dom["name"]), "kernel": dv["kernel"],
+                "peak_source": ("FP32 FMA pipe: SMs x 128 lanes x 2 FLOP x max SM clock "
+                                f"({props.multi_processor_count} x 128 x 2 x {pk['sm_max_mhz']:.0f} MHz)"
+                                if dv["bound"] == "alu" else
+                                f"HBM copy GB/s, {pk['hbm_src']} (MEASURED_PEAKS.json)")}
+    by = {sp["name"]: (sp, ms, ems) for sp, ms, ems in zip(specs, op_ms, e2e_ms)}
+    head = "convpool" if "convpool" in by else specs[0]["name"]
+    hs, hms, hems = by[head]
+    cpu = None
+    if not args.no_cpu_baseline and args.only is None and not args.batch:
+        cpu = cpu_baseline_obj(oracle_sample(cp, mp, ct, budget_s=args.cpu_budget))
+    line = {
+        "metric": METRIC, "value": weak_value(hs["work"], ws, hms) / hs["scale"], "unit": hs["unit"],
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded SplitMix64 / Box-Muller, the pages' shapes)", "config": config_obj(),
+    }
+    if "maxpool" in by:
+        sp, ms, _ = by["maxpool"]
+        line["maxpool_hbm_gbs"] = weak_value(sp["work"], ws, ms) / 1e9
+        line["maxpool_hbm_frac"] = ops["maxpool"]["frac"]
+    if "convpool" in by:
+        line["convpool_fp32_frac"] = ops["convpool"]["frac"]
+    if "convt" in by:
+        sp, ms, _ = by["convt"]
+        line["convt_tflops"] = weak_value(sp["work"], ws, ms) / 1e12
+    line.update({
+        "ops": ops, "roofline": roofline, "cpu_baseline": cpu,
+        "e2e": {"value": weak_value(hs["work"], ws, hems) / hs["scale"], "unit": hs["unit"],
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ops_ms": {sp["name"]: e for sp, e in zip(specs, e2e_ms)},
+                "note": "public API with pinned host tensors: H2D copy, kernels, D2H copy of each op's result"},
+        "gpu_launches": launches, "launches_per_step": launches / args.steps,
+        "clocks": clk.summary(), "device": props.name,
+    })
+    if args.only or args.batch:
+        line["config"]["subset"] = {"only": args.only, "batch": args.batch}
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=16.0)
+    ap.add_argument("--backend", default="nccl", choices=["nccl", "gloo"])
+    ap.add_argument("--only", default=None, choices=["convpool", "maxpool", "convt"],
+                    help="time one operator only (profiling)")
+    ap.add_argument("--batch", type=int, default=0, help="smaller batch for every workload (profiling)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl != "reference":
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
