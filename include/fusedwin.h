@@ -152,6 +152,34 @@ fw_status fw_convtranspose2d_softmax_bias_scale_sigmoid(const float *x, int N, i
  * needs for these arguments (0 when it needs none). */
 unsigned long long fw_convt_workspace_size(int Cin, int Cout, int k, int s, int p);
 
+/*
+ * Allocation-free variant of fw_convtranspose2d_softmax_bias_scale_sigmoid (no
+ * counterpart on the pages: it exists for callers that cannot allocate device
+ * memory -- plugins that a host framework hands only input and output buffers
+ * because it owns all device memory, real-time loops that may not allocate
+ * after start-up, code where an allocation would implicitly synchronise the
+ * device).  Same arguments and result, minus the workspace: the weight rewrite
+ * goes into a fixed device array of FW_CONVT_STATIC_WS_BYTES inside the library,
+ * which every device that loads the library holds until the process exits.
+ *   - Allocates nothing: no cudaMalloc/cudaFree, no allocating library routine.
+ *   - Returns FW_ERR_UNSUPPORTED, launching nothing, when the rewrite needs more
+ *     than FW_CONVT_STATIC_WS_BYTES (fw_convt_workspace_size(Cin, Cout, k, s, p)
+ *     bytes; 16*Cin*Cout*4 for the tiled k4 s2 p1 Cout=128 path, so Cin <= 128).
+ *   - The first call on a device looks up the array's device address (with that
+ *     device current) and caches it; make that first call before any stream
+ *     capture.
+ *   - Every call shares the one array and leaves its contents behind (each call
+ *     rewrites all it reads, nothing has to start at zero); calls that overlap on
+ *     the GPU -- on different streams, or from different host threads -- race on
+ *     it and must be serialised by the caller.
+ */
+#define FW_CONVT_STATIC_WS_BYTES (1u << 20)
+fw_status fw_convtranspose2d_softmax_bias_scale_sigmoid_noalloc(const float *x, int N, int Cin, int H, int W,
+                                                                const float *w, const float *conv_b,
+                                                                int Cout, int k, int s, int p, int op,
+                                                                const float *bias, float scale, float *out,
+                                                                void *stream);
+
 /* ------------------------------------------------------------- diagnostics */
 
 /*

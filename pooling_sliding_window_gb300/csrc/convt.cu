@@ -24,6 +24,8 @@
 //   * results are transposed through shared memory and stored row by row.
 // Direct kernel: one thread per output pixel, two passes over the channels
 // (online max/sum, then the outputs), any (k, s, p, op) and Cout <= 1024.
+#include <mutex>
+
 #include "fw_common.cuh"
 
 namespace fw {
@@ -280,3 +282,57 @@ fw_status convt_launch(const float *x, int N, int Cin, int H, int W, const float
 }
 
 }  // namespace fw
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of the conv-transpose call.
+//
+// Some callers cannot call cudaMalloc (or any allocator): plugins that a host
+// framework hands only input and output buffers because it owns all device
+// memory, real-time loops that may not allocate after start-up, and code where
+// an allocation would implicitly synchronise the device.  For them the weight
+// rewrite that the tiled kernel needs goes into this fixed array instead of a
+// caller workspace.  Every device that loads the library holds it until the
+// process exits.
+// ---------------------------------------------------------------------------
+namespace fw {
+
+static __device__ __align__(256) unsigned char g_convt_static_ws[FW_CONVT_STATIC_WS_BYTES];
+
+namespace {
+std::mutex g_static_ws_mu;
+void *g_static_ws_ptr[FW_MAX_DEVICES] = {};
+}  // namespace
+
+// Device address of g_convt_static_ws on the current device.  In host code the
+// array's name is only a host-side stand-in, so the address is looked up once
+// per device with cudaGetSymbolAddress (with that device current) and cached.
+static fw_status convt_static_workspace(void **ptr) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FW_ERR_LAUNCH;
+    if (dev < 0 || dev >= FW_MAX_DEVICES) return FW_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_static_ws_mu);
+    if (!g_static_ws_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_convt_static_ws) != cudaSuccess || !p) return FW_ERR_LAUNCH;
+        g_static_ws_ptr[dev] = p;
+    }
+    *ptr = g_static_ws_ptr[dev];
+    return FW_OK;
+}
+
+}  // namespace fw
+
+extern "C" fw_status fw_convtranspose2d_softmax_bias_scale_sigmoid_noalloc(
+    const float *x, int N, int Cin, int H, int W, const float *w, const float *conv_b, int Cout, int k, int s,
+    int p, int op, const float *bias, float scale, float *out, void *stream) {
+    const unsigned long long need = fw_convt_workspace_size(Cin, Cout, k, s, p);
+    if (need > FW_CONVT_STATIC_WS_BYTES) return FW_ERR_UNSUPPORTED;
+    void *ws = nullptr;
+    if (need > 0) {
+        const fw_status rc = fw::convt_static_workspace(&ws);
+        if (rc != FW_OK) return rc;
+    }
+    return fw_convtranspose2d_softmax_bias_scale_sigmoid(x, N, Cin, H, W, w, conv_b, Cout, k, s, p, op, bias,
+                                                         scale, out, ws, need > 0 ? FW_CONVT_STATIC_WS_BYTES : 0,
+                                                         stream);
+}

@@ -15,6 +15,9 @@ enum : unsigned {
     DEVERR_INTERNAL = 2u,  // an internal consistency check failed
 };
 
+// Devices for which per-device state is cached.
+constexpr int FW_MAX_DEVICES = 64;
+
 // Wall-clock limit of a bounded wait inside a kernel.
 constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;  // 2 s
 

@@ -28,7 +28,8 @@ STATUS = {0: "FW_OK", 1: "FW_ERR_NULL", 2: "FW_ERR_SHAPE", 3: "FW_ERR_PARAM", 4:
 EXPORTS = ("fw_status_string", "fw_version", "fw_conv2d_pool_out_shape", "fw_maxpool2d_out_shape",
            "fw_convt_out_shape", "fw_conv2d_tanh_scale_bias_maxpool", "fw_maxpool2d",
            "fw_convtranspose2d_softmax_bias_scale_sigmoid", "fw_convt_workspace_size",
-           "fw_check_device_errors", "fw_launch_count")
+           "fw_check_device_errors", "fw_launch_count",
+           "fw_convtranspose2d_softmax_bias_scale_sigmoid_noalloc")
 
 
 class FusedWinError(RuntimeError):
@@ -70,6 +71,9 @@ def lib():
         L.fw_convt_workspace_size.argtypes = [I, I, I, I, I]
         L.fw_check_device_errors.restype = I
         L.fw_check_device_errors.argtypes = [P]
+        L.fw_convtranspose2d_softmax_bias_scale_sigmoid_noalloc.restype = I
+        L.fw_convtranspose2d_softmax_bias_scale_sigmoid_noalloc.argtypes = [
+            P, I, I, I, I, P, P, I, I, I, I, I, P, F, P, P]
         _lib = L
     return _lib
 
@@ -207,3 +211,28 @@ def fw_convtranspose2d_softmax_bias_scale_sigmoid(x, w, conv_b, bias, scale, str
             _ptr(bd), float(scale), _ptr(od), _ptr(workspace), ws_bytes, C.c_void_p(stream)),
             "fw_convtranspose2d_softmax_bias_scale_sigmoid")
     return _finish(od, out, host)
+
+
+def fw_convtranspose2d_softmax_bias_scale_sigmoid_noalloc(x, w, conv_b, bias, scale, out, stride=2, padding=1,
+                                                          output_padding=1):
+    """The conv-transpose model through the allocation-free entry point.
+
+    For callers that cannot allocate device memory: every tensor, `out`
+    included, must already be on the device (nothing is copied or allocated
+    here), and the library uses its own fixed device array for the weight
+    rewrite instead of a workspace.  Calls that overlap on the GPU race on that
+    array.
+    """
+    for name, t in (("x", x), ("w", w), ("bias", bias), ("out", out)) + ((("conv_b", conv_b),) if conv_b is not None else ()):
+        if not isinstance(t, torch.Tensor) or t.device.type != "cuda" or t.dtype != torch.float32 \
+                or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous float32 CUDA tensor")
+    N, Cin, H, W = x.shape
+    _, Cout, K, _ = w.shape
+    stream = torch.cuda.current_stream(x.device).cuda_stream
+    with torch.cuda.device(x.device):
+        _check(lib().fw_convtranspose2d_softmax_bias_scale_sigmoid_noalloc(
+            _ptr(x), N, Cin, H, W, _ptr(w), _ptr(conv_b), Cout, K, stride, padding, output_padding,
+            _ptr(bias), float(scale), _ptr(out), C.c_void_p(stream)),
+            "fw_convtranspose2d_softmax_bias_scale_sigmoid_noalloc")
+    return out
