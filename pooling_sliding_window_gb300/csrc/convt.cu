@@ -24,6 +24,7 @@
 //   * results are transposed through shared memory and stored row by row.
 // Direct kernel: one thread per output pixel, two passes over the channels
 // (online max/sum, then the outputs), any (k, s, p, op) and Cout <= 1024.
+#include <cstdlib>
 #include <mutex>
 
 #include "fw_common.cuh"
@@ -237,7 +238,21 @@ __global__ void convt_direct_kernel(const float *__restrict__ x, const float *__
     }
 }
 
+// FUSEDWIN_CONVT_FFMA=1 in the environment selects the FP32-FMA tiled kernel
+// instead of the tensor-core one (used to cross-check the two).
+bool force_ffma() {
+    static const bool v = [] {
+        const char *e = getenv("FUSEDWIN_CONVT_FFMA");
+        return e && e[0] == '1';
+    }();
+    return v;
+}
+
 }  // namespace
+
+bool convt_tc_eligible(int Cin, int Cout, int k, int s, int p);
+fw_status convt_tc_launch(const float *x, int N, int Cin, int H, int W, const float *w, const float *cb,
+                          const float *bias, float scale, float *out, int Ho, int Wo, void *ws, cudaStream_t st);
 
 size_t convt_workspace_bytes(int Cin, int Cout, int k, int s, int p) {
     if (k == 4 && s == 2 && p == 1 && Cout == COUT_T) return (size_t)16 * Cin * Cout * sizeof(float);
@@ -250,6 +265,8 @@ fw_status convt_launch(const float *x, int N, int Cin, int H, int W, const float
     const size_t need = convt_workspace_bytes(Cin, Cout, k, s, p);
     if (need > 0) {
         if (!ws || ws_bytes < need) return FW_ERR_NULL;
+        if (convt_tc_eligible(Cin, Cout, k, s, p) && !force_ffma())
+            return convt_tc_launch(x, N, Cin, H, W, w, cb, bias, scale, out, Ho, Wo, ws, st);
         float *wp = static_cast<float *>(ws);
         convt_prepack_kernel<<<(unsigned)min(1024LL, (16LL * Cin * Cout + 255) / 256), 256, 0, st>>>(w, wp, Cin, Cout);
         note_launch();

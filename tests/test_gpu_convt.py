@@ -68,3 +68,27 @@ def test_errors_raise():
     b = torch.zeros(8, device="cuda")
     with pytest.raises(FW.FusedWinError, match="FW_ERR_PARAM"):
         FW.fw_convtranspose2d_softmax_bias_scale_sigmoid(x, w, None, b, 2.0, 2, 1, 2)
+
+
+def test_ffma_kernel_when_forced():
+    """The FP32-FMA tiled kernel (selected with FUSEDWIN_CONVT_FFMA=1) on the same
+    shapes the tensor-core kernel takes, in a fresh process."""
+    import subprocess
+    import sys
+    import textwrap
+    code = textwrap.dedent("""
+        import numpy as np, torch
+        from tests.parity import FW, O, TOL_FFMA, assert_close, dev, host, synth
+        for (N, Cin, H, W) in ((2, 64, 9, 10), (1, 32, 17, 33)):
+            d = synth.convt_inputs(N, Cin, H, W, 128, seed=H)
+            got = host(FW.fw_convtranspose2d_softmax_bias_scale_sigmoid(
+                dev(d["x"]), dev(d["w"]), dev(d["conv_b"]), dev(d["bias"]), 2.0))
+            want = O.convtranspose2d_softmax_bias_scale_sigmoid(d["x"], d["w"], d["conv_b"], d["bias"], 2.0)
+            assert_close(got, want, TOL_FFMA, str((N, Cin, H, W)))
+        print("ok")
+    """)
+    import os
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, capture_output=True, text=True,
+                       env=dict(os.environ, FUSEDWIN_CONVT_FFMA="1"), timeout=600)
+    assert r.returncode == 0 and "ok" in r.stdout, r.stdout + r.stderr
