@@ -20,15 +20,20 @@
 //     matrices whose 8-row groups are 128 bytes apart), a horizontal tap is a start
 //     address 16 bytes further on and a vertical tap a second "slab".
 //
-// CTA roles (288 threads, one CTA per SM, persistent over the tiles of one phase):
-//   warps 0-3  producers: gather the 129 positions x Cin channels a slab needs from
-//              NCHW x, round to TF32, write the planar shared layout (2 stages);
-//   warp  8    allocates TMEM; one lane issues the MMAs: per tile 2 slabs (vertical
-//              taps) x 2 horizontal taps x Cin/8 K-steps into one of two 128-column
-//              accumulators;
-//   warps 4-7  epilogue: each thread owns one pixel (a TMEM lane), reads its 128
-//              channel sums, adds the conv bias, takes the softmax in registers and
-//              writes sigmoid((p + bias) * scale).
+// CTA roles (640 threads, one CTA per SM, persistent over the tiles of one phase):
+//   warps 0-6   producers: gather the positions x Cin channels a slab needs from
+//               NCHW x (all channel loads of a position in flight at once), round
+//               to TF32, write the planar shared layout (2 stages); a slab covers
+//               both vertical taps of the tile when it fits, else one each;
+//   warp  19    allocates TMEM; one lane issues the MMAs: 4 taps x Cin/8 K-steps
+//               per tile into one of three 128-column accumulators (round robin);
+//   warps 7-18  epilogue, three groups of 4 warps, group g serving accumulator g:
+//               each thread owns one pixel (a TMEM lane) and walks its 128 channel
+//               sums three times in 32-column chunks: the max, then exp(y - max)
+//               written back to TMEM with the running sum, then
+//               sigmoid((p + bias) * scale) to global memory.  The exponentials run
+//               as base-2 exponentials with the per-channel constants (conv bias,
+//               bias * scale) folded into one multiply-add each.
 // The phase's weights (TF32, 2*Cin KB) stay resident in shared memory; they are
 // rewritten into the caller's workspace by convt_tc_prepack_kernel.
 // TF32 operands (10-bit mantissa) are enough here: the channel softmax scales an
@@ -44,12 +49,16 @@ namespace {
 
 constexpr int COUT = 128;
 constexpr int MT = 128;            // anchors per tile
-constexpr int SLAB_POS = MT + 1;   // positions per slab (two horizontal taps)
 constexpr int NSTAGE = 2;          // slab stages
-constexpr int NTHREADS = 288;
-constexpr int MMA_WARP = 8;
+constexpr int PROD_WARPS = 7;      // warps 0-6
+constexpr int EPI_WARP0 = PROD_WARPS;  // NACC groups of 4 warps (each covers TMEM lane quarters 0-3)
+constexpr int NACC = 3;            // TMEM accumulators (128 columns each), one epilogue group each
+constexpr int MMA_WARP = EPI_WARP0 + 4 * NACC;
+constexpr int NTHREADS = (MMA_WARP + 1) * 32;
+constexpr float LOG2E = 1.4426950408889634f;
 constexpr uint32_t IDESC = tc::idesc_tf32(128, COUT);
 constexpr size_t MIN_SMEM = 116 * 1024;  // > half an SM: one CTA per SM
+constexpr size_t SMEM_LIMIT = 232448;    // 227 KB of dynamic shared memory per CTA
 
 // Tap tables of the k4 s2 p1 decomposition (output parity q, tap index t in {0,1}):
 // kernel index and input offset (input row = m + offset).
@@ -79,27 +88,42 @@ struct Bars {
     uint64_t b_full;
     uint64_t slab_full[NSTAGE];
     uint64_t slab_empty[NSTAGE];
-    uint64_t acc_full[2];
-    uint64_t acc_empty[2];
+    uint64_t acc_full[NACC];
+    uint64_t acc_empty[NACC];
     uint32_t tmem_base;
     int abort;
 };
 
+// Shared memory of one CTA: resident weights, NSTAGE slabs of G planes x L
+// positions x 16 B, two per-channel constant vectors, barriers.
+__host__ __device__ inline size_t tc_smem_bytes(int G, int L) {
+    return (size_t)4 * G * COUT * 16 + (size_t)NSTAGE * G * L * 16 + 2 * COUT * 4 + sizeof(Bars);
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// A slab holds the positions one tile reads for the vertical taps it covers:
+// nslab == 1 -> both vertical taps (L = 129 + (W+1) positions), nslab == 2 ->
+// one vertical tap per slab (L = 129).
 template <int G>  // input channels / 4
 __global__ void __launch_bounds__(NTHREADS, 1)
 convt_k4s2_tc_kernel(const float *__restrict__ x, const float *__restrict__ wtc, const float *__restrict__ cb,
                      const float *__restrict__ bias, float scale, float *__restrict__ out, int N, int H, int W,
-                     int Ho, int Wo) {
+                     int Ho, int Wo, int nslab, int L) {
     constexpr int CIN = 4 * G;
     constexpr int B_BYTES = 4 * G * COUT * 16;  // 4 taps x G planes x 128 co x 16 B
-    constexpr int SLAB_PLANE = SLAB_POS * 16;   // bytes per plane in a slab
-    constexpr int SLAB_BYTES = G * SLAB_PLANE;
     extern __shared__ __align__(1024) unsigned char smem[];
+    const int slab_plane = L * 16;  // bytes per plane in a slab
+    const int slab_bytes = G * slab_plane;
     unsigned char *sB = smem;
     unsigned char *sSlab = smem + B_BYTES;
-    float *sCb = reinterpret_cast<float *>(sSlab + NSTAGE * SLAB_BYTES);
-    float *sBias = sCb + COUT;
-    Bars &bars = *reinterpret_cast<Bars *>(sBias + COUT);
+    float *sCb = reinterpret_cast<float *>(sSlab + NSTAGE * slab_bytes);  // conv_b * log2(e)
+    float *sKb = sCb + COUT;                                              // -bias * scale * log2(e)
+    Bars &bars = *reinterpret_cast<Bars *>(sKb + COUT);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int phase = blockIdx.x & 3, py = phase >> 1, px = phase & 1;
@@ -109,25 +133,26 @@ convt_k4s2_tc_kernel(const float *__restrict__ x, const float *__restrict__ wtc,
     const long long n_pos = ((long long)N * BH + 1) * BW;
     const int n_tiles = (int)((n_anchor + MT - 1) / MT);
     const int dx0 = px == 0 ? -1 : 0;  // smaller horizontal tap offset of the phase
+    const int dy0 = py == 0 ? -1 : 0;  // smaller vertical tap offset of the phase
 
     for (int i = tid; i < COUT; i += NTHREADS) {
-        sCb[i] = cb ? __ldg(cb + i) : 0.f;
-        sBias[i] = __ldg(bias + i);
+        sCb[i] = cb ? __ldg(cb + i) * LOG2E : 0.f;
+        sKb[i] = -__ldg(bias + i) * scale * LOG2E;
     }
     if (tid == 0) {
         mbar_init(smem_u32(&bars.b_full), 1);
         for (int s = 0; s < NSTAGE; ++s) {
-            mbar_init(smem_u32(&bars.slab_full[s]), 4);
+            mbar_init(smem_u32(&bars.slab_full[s]), PROD_WARPS);
             mbar_init(smem_u32(&bars.slab_empty[s]), 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < NACC; ++b) {
             mbar_init(smem_u32(&bars.acc_full[b]), 1);
             mbar_init(smem_u32(&bars.acc_empty[b]), 4);
         }
         bars.abort = 0;
         fence_mbar_init();
     }
-    if (warp == MMA_WARP) tc::alloc(smem_u32(&bars.tmem_base), 256);
+    if (warp == MMA_WARP) tc::alloc(smem_u32(&bars.tmem_base), 512);
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
@@ -139,21 +164,21 @@ convt_k4s2_tc_kernel(const float *__restrict__ x, const float *__restrict__ wtc,
         atomicOr(&g_err_convt_tc, DEVERR_TIMEOUT);
     };
 
-    if (warp < 4) {
+    if (warp < PROD_WARPS) {
         // ------------------------------------------------------------ producers
         const long long plane_stride = (long long)H * W;
         int k = 0;
         for (int tile = rank; tile < n_tiles && !*abort_flag; tile += nct) {
-            for (int s = 0; s < 2; ++s, ++k) {
+            for (int s = 0; s < nslab; ++s, ++k) {
                 const int stage = k & 1, use = k >> 1;
                 if (use > 0 && !mbar_wait_bounded(smem_u32(&bars.slab_empty[stage]), (use - 1) & 1)) {
                     fail();
                     break;
                 }
-                const int dy = tap_off(py, s);
-                const long long pbase = (long long)tile * MT + BW + (long long)dy * BW + dx0;
-                unsigned char *slab = sSlab + stage * SLAB_BYTES;
-                for (int pos = tid; pos < SLAB_POS; pos += 128) {
+                const int dy_lo = nslab == 1 ? dy0 : tap_off(py, s);
+                const long long pbase = (long long)tile * MT + BW + (long long)dy_lo * BW + dx0;
+                unsigned char *slab = sSlab + stage * slab_bytes;
+                for (int pos = tid; pos < L; pos += PROD_WARPS * 32) {
                     const long long q = pbase + pos;
                     const float *src = nullptr;
                     if (q >= 0 && q < n_pos) {
@@ -165,16 +190,15 @@ convt_k4s2_tc_kernel(const float *__restrict__ x, const float *__restrict__ wtc,
                             if (row < H) src = x + ((n * CIN) * H + row) * (long long)W + c;
                         }
                     }
+                    // all channel loads in flight before any is converted
+                    float r[CIN];
+#pragma unroll
+                    for (int ci = 0; ci < CIN; ++ci) r[ci] = src ? __ldg(src + ci * plane_stride) : 0.f;
 #pragma unroll
                     for (int g = 0; g < G; ++g) {
-                        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                        if (src) {
-                            v.x = tc::to_tf32(__ldg(src + (4 * g + 0) * plane_stride));
-                            v.y = tc::to_tf32(__ldg(src + (4 * g + 1) * plane_stride));
-                            v.z = tc::to_tf32(__ldg(src + (4 * g + 2) * plane_stride));
-                            v.w = tc::to_tf32(__ldg(src + (4 * g + 3) * plane_stride));
-                        }
-                        *reinterpret_cast<float4 *>(slab + g * SLAB_PLANE + pos * 16) = v;
+                        const float4 v = make_float4(tc::to_tf32(r[4 * g]), tc::to_tf32(r[4 * g + 1]),
+                                                     tc::to_tf32(r[4 * g + 2]), tc::to_tf32(r[4 * g + 3]));
+                        *reinterpret_cast<float4 *>(slab + g * slab_plane + pos * 16) = v;
                     }
                 }
                 fence_proxy_async_smem();
@@ -196,14 +220,15 @@ convt_k4s2_tc_kernel(const float *__restrict__ x, const float *__restrict__ wtc,
             const uint32_t sB_addr = smem_u32(sB), sSlab_addr = smem_u32(sSlab);
             int k = 0, u = 0;
             for (int tile = rank; ok && tile < n_tiles && !*abort_flag; tile += nct, ++u) {
-                const int b = u & 1, ause = u >> 1;
+                const int b = u % NACC, ause = u / NACC;
                 if (ause > 0 && !mbar_wait_bounded(smem_u32(&bars.acc_empty[b]), (ause - 1) & 1)) {
                     fail();
                     break;
                 }
                 tc::fence_after_sync();
                 const uint32_t d = tmem + (uint32_t)(b * COUT);
-                for (int s = 0; s < 2; ++s, ++k) {
+                uint32_t acc = 0;
+                for (int s = 0; s < nslab; ++s, ++k) {
                     const int stage = k & 1, use = k >> 1;
                     if (!mbar_wait_bounded(smem_u32(&bars.slab_full[stage]), use & 1)) {
                         fail();
@@ -211,17 +236,22 @@ convt_k4s2_tc_kernel(const float *__restrict__ x, const float *__restrict__ wtc,
                         break;
                     }
                     tc::fence_after_sync();
-                    const uint32_t slab = sSlab_addr + stage * SLAB_BYTES;
+                    const uint32_t slab = sSlab_addr + stage * slab_bytes;
+                    const int dy_lo = nslab == 1 ? dy0 : tap_off(py, s);
+                    for (int ty = (nslab == 1 ? 0 : s); ty <= (nslab == 1 ? 1 : s); ++ty) {
 #pragma unroll
-                    for (int tx = 0; tx < 2; ++tx) {
-                        const int o = tap_off(px, tx) - dx0;  // 0 or 1 position
-                        const int tap = 2 * s + tx;
+                        for (int tx = 0; tx < 2; ++tx) {
+                            const int o = (tap_off(py, ty) - dy_lo) * BW + (tap_off(px, tx) - dx0);
+                            const int tap = 2 * ty + tx;
 #pragma unroll
-                        for (int j = 0; j < G / 2; ++j) {
-                            const uint64_t ad = tc::smem_desc(slab + (2 * j * SLAB_POS + o) * 16, SLAB_PLANE, 128);
-                            const uint64_t bd =
-                                tc::smem_desc(sB_addr + (tap * G + 2 * j) * (COUT * 16), COUT * 16, 128);
-                            tc::mma_tf32(d, ad, bd, IDESC, (s | tx | j) != 0);
+                            for (int j = 0; j < G / 2; ++j) {
+                                const uint64_t ad =
+                                    tc::smem_desc(slab + (2 * j * L + o) * 16, (uint32_t)slab_plane, 128);
+                                const uint64_t bd =
+                                    tc::smem_desc(sB_addr + (tap * G + 2 * j) * (COUT * 16), COUT * 16, 128);
+                                tc::mma_tf32(d, ad, bd, IDESC, acc);
+                                acc = 1;
+                            }
                         }
                     }
                     tc::commit(smem_u32(&bars.slab_empty[stage]));
@@ -233,53 +263,66 @@ convt_k4s2_tc_kernel(const float *__restrict__ x, const float *__restrict__ wtc,
         __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue
-        const int q = warp & 3;  // TMEM lane quarter of this warp
+        // Group eg handles the tiles u = eg, eg + NACC, ... of this CTA (accumulator eg).
+        const int q = warp & 3;                     // TMEM lane quarter of this warp
+        const int eg = (warp - EPI_WARP0) >> 2;     // epilogue group = accumulator buffer
         const long long img_anchors = (long long)BH * BW;
         const long long plane_out = (long long)Ho * Wo;
-        int u = 0;
-        for (int tile = rank; tile < n_tiles && !*abort_flag; tile += nct, ++u) {
-            const int b = u & 1;
-            if (!mbar_wait_bounded(smem_u32(&bars.acc_full[b]), (u >> 1) & 1)) {
+        const float ks = -scale * LOG2E;
+        int u = eg;
+        for (int tile = rank + eg * nct; tile < n_tiles && !*abort_flag; tile += NACC * nct, u += NACC) {
+            if (!mbar_wait_bounded(smem_u32(&bars.acc_full[eg]), (u / NACC) & 1)) {
                 fail();
                 break;
             }
             tc::fence_after_sync();
-            float v[COUT];
-            const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * COUT);
+            const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(eg * COUT);
+            float v[32];
+            // pass 1: max over channels of z = (acc + conv_b) * log2(e)
+            float mx = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < COUT / 32; ++c) tc::ld32(taddr + 32 * c, v + 32 * c);
-            tc::wait_ld();
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&bars.acc_empty[b]));
-
+            for (int c = 0; c < COUT / 32; ++c) {
+                tc::ld32(taddr + 32 * c, v);
+                tc::wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) mx = fmaxf(mx, fmaf(v[i], LOG2E, sCb[32 * c + i]));
+            }
+            // pass 2: e = 2^(z - max) written back to TMEM, and their sum
+            float sum = 0.f;
+#pragma unroll
+            for (int c = 0; c < COUT / 32; ++c) {
+                tc::ld32(taddr + 32 * c, v);
+                tc::wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    v[i] = ex2_approx(fmaf(v[i], LOG2E, sCb[32 * c + i]) - mx);
+                    sum += v[i];
+                }
+                tc::st32(taddr + 32 * c, v);
+            }
+            tc::wait_st();
+            // softmax p = e / sum; out = 1 / (1 + 2^(-(p + bias) * scale * log2(e)))
+            const float kp = ks / sum;
             const long long a = (long long)tile * MT + 32 * q + lane;
             const long long n = a / img_anchors;
             const int rem = (int)(a - n * img_anchors);
             const int m = rem / BW, nn = rem - m * BW;
             const int oh = 2 * m + py, ow = 2 * nn + px;
             const bool valid = a < n_anchor && oh < Ho && ow < Wo;
-            float mx = -INFINITY;
+            float *o = out + (n * COUT) * plane_out + (long long)oh * Wo + ow;
 #pragma unroll
-            for (int c = 0; c < COUT; ++c) {
-                v[c] += sCb[c];
-                mx = fmaxf(mx, v[c]);
-            }
-            float sum = 0.f;
+            for (int c = 0; c < COUT / 32; ++c) {
+                tc::ld32(taddr + 32 * c, v);
+                tc::wait_ld();
+                if (valid) {
 #pragma unroll
-            for (int c = 0; c < COUT; ++c) {
-                v[c] = __expf(v[c] - mx);
-                sum += v[c];
-            }
-            const float inv = __frcp_rn(sum);
-            if (valid) {
-                float *o = out + (n * COUT) * plane_out + (long long)oh * Wo + ow;
-#pragma unroll
-                for (int c = 0; c < COUT; ++c) {
-                    const float r = __fmul_rn(__fadd_rn(v[c] * inv, sBias[c]), scale);
-                    o[c * plane_out] = __frcp_rn(1.f + __expf(-r));
+                    for (int i = 0; i < 32; ++i)
+                        o[(32 * c + i) * plane_out] = __fdividef(1.f, 1.f + ex2_approx(fmaf(v[i], kp, sKb[32 * c + i])));
                 }
             }
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bars.acc_empty[eg]));
         }
     }
 
@@ -287,27 +330,36 @@ convt_k4s2_tc_kernel(const float *__restrict__ x, const float *__restrict__ wtc,
     __syncthreads();
     if (warp == MMA_WARP) {
         tc::fence_after_sync();
-        tc::dealloc(tmem, 256);
+        tc::dealloc(tmem, 512);
     }
 }
 
 template <int G>
 fw_status launch_g(const float *x, int N, int H, int W, const float *wtc, const float *cb, const float *bias,
                    float scale, float *out, int Ho, int Wo, cudaStream_t st) {
-    constexpr int B_BYTES = 4 * G * COUT * 16;
-    constexpr int SLAB_BYTES = G * SLAB_POS * 16;
-    size_t smem = (size_t)B_BYTES + NSTAGE * SLAB_BYTES + 2 * COUT * 4 + sizeof(Bars);
+    int dev = 0, sms = 0, optin = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+        return FW_ERR_LAUNCH;
+    const size_t limit = (size_t)optin < SMEM_LIMIT ? (size_t)optin : SMEM_LIMIT;
+    int nslab = 1, L = MT + 1 + (W + 1);
+    size_t smem = tc_smem_bytes(G, L);
+    if (smem > limit) {
+        nslab = 2;
+        L = MT + 1;
+        smem = tc_smem_bytes(G, L);
+    }
+    if (smem > limit) return FW_ERR_UNSUPPORTED;
     if (smem < MIN_SMEM) smem = MIN_SMEM;
     cudaError_t e = cudaFuncSetAttribute(convt_k4s2_tc_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return launch_status(e);
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return FW_ERR_LAUNCH;
     const long long tiles = ((long long)N * (H + 1) * (W + 1) + MT - 1) / MT;
     int per_phase = sms / 4 > 0 ? sms / 4 : 1;
     if (per_phase > tiles) per_phase = (int)tiles;
-    convt_k4s2_tc_kernel<G><<<4 * per_phase, NTHREADS, smem, st>>>(x, wtc, cb, bias, scale, out, N, H, W, Ho, Wo);
+    convt_k4s2_tc_kernel<G><<<4 * per_phase, NTHREADS, smem, st>>>(x, wtc, cb, bias, scale, out, N, H, W, Ho, Wo,
+                                                                   nslab, L);
     note_launch();
     return launch_status(cudaGetLastError());
 }
