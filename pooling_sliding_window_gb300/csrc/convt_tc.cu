@@ -166,34 +166,44 @@ convt_k4s2_tc_kernel(const float *__restrict__ x, const float *__restrict__ wtc,
 
     if (warp < PROD_WARPS) {
         // ------------------------------------------------------------ producers
+        // Each thread owns at most one position of a slab (L <= 224 when one slab
+        // covers both vertical taps; two positions otherwise).  Its channel loads
+        // are issued before the wait for the stage to be free, so their latency
+        // overlaps the tensor cores still reading that stage.
         const long long plane_stride = (long long)H * W;
         int k = 0;
         for (int tile = rank; tile < n_tiles && !*abort_flag; tile += nct) {
             for (int s = 0; s < nslab; ++s, ++k) {
                 const int stage = k & 1, use = k >> 1;
-                if (use > 0 && !mbar_wait_bounded(smem_u32(&bars.slab_empty[stage]), (use - 1) & 1)) {
-                    fail();
-                    break;
-                }
                 const int dy_lo = nslab == 1 ? dy0 : tap_off(py, s);
                 const long long pbase = (long long)tile * MT + BW + (long long)dy_lo * BW + dx0;
                 unsigned char *slab = sSlab + stage * slab_bytes;
+                bool waited = use == 0;
                 for (int pos = tid; pos < L; pos += PROD_WARPS * 32) {
                     const long long q = pbase + pos;
                     const float *src = nullptr;
                     if (q >= 0 && q < n_pos) {
-                        const long long R = q / BW;
-                        const int c = (int)(q - R * BW);
+                        int R, c;
+                        if (n_pos < 0x7fffffffLL) {
+                            R = (int)q / BW;
+                            c = (int)q - R * BW;
+                        } else {
+                            R = (int)(q / BW);
+                            c = (int)(q - (long long)R * BW);
+                        }
                         if (c < W && R > 0) {
-                            const long long n = (R - 1) / BH;
-                            const int row = (int)(R - 1 - n * BH);
-                            if (row < H) src = x + ((n * CIN) * H + row) * (long long)W + c;
+                            const int n = (R - 1) / BH;
+                            const int row = R - 1 - n * BH;
+                            if (row < H) src = x + (((long long)n * CIN) * H + row) * (long long)W + c;
                         }
                     }
-                    // all channel loads in flight before any is converted
                     float r[CIN];
 #pragma unroll
                     for (int ci = 0; ci < CIN; ++ci) r[ci] = src ? __ldg(src + ci * plane_stride) : 0.f;
+                    if (!waited) {
+                        if (!mbar_wait_bounded(smem_u32(&bars.slab_empty[stage]), (use - 1) & 1)) fail();
+                        waited = true;
+                    }
 #pragma unroll
                     for (int g = 0; g < G; ++g) {
                         const float4 v = make_float4(tc::to_tf32(r[4 * g]), tc::to_tf32(r[4 * g + 1]),
@@ -201,9 +211,12 @@ convt_k4s2_tc_kernel(const float *__restrict__ x, const float *__restrict__ wtc,
                         *reinterpret_cast<float4 *>(slab + g * slab_plane + pos * 16) = v;
                     }
                 }
+                // threads without a position still wait, so the whole warp arrives in order
+                if (!waited && !mbar_wait_bounded(smem_u32(&bars.slab_empty[stage]), (use - 1) & 1)) fail();
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&bars.slab_full[stage]));
+                if (*abort_flag) break;
             }
         }
     } else if (warp == MMA_WARP) {
