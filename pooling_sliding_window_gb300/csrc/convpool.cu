@@ -19,6 +19,8 @@
 //   * the window max (min when scale < 0) is taken in registers, the conv bias
 //     is added, and tanh / scale / bias run once per pooled output.
 // Direct kernel: one thread per pooled output, every other shape.
+#include <cstdlib>
+
 #include "fw_common.cuh"
 
 namespace fw {
@@ -192,9 +194,25 @@ fw_status launch_tiled(const float *x, int N, int Cin, int H, int W, const float
 
 }  // namespace
 
+bool convpool_tc_eligible(int Cin, int Cout, int KH, int KW, int pk, int ps);
+fw_status convpool_tc_launch(const float *x, int N, int H, int W, const float *w, const float *cb, int Cout,
+                             float scale, const float *bias, int pk, float *out, int Ho, int Wo, cudaStream_t st);
+
+// FUSEDWIN_CONVPOOL_FFMA=1 in the environment selects the FP32-FMA tiled kernel
+// instead of the tensor-core one (used to cross-check the two).
+static bool convpool_force_ffma() {
+    static const bool v = [] {
+        const char *e = getenv("FUSEDWIN_CONVPOOL_FFMA");
+        return e && e[0] == '1';
+    }();
+    return v;
+}
+
 fw_status convpool_launch(const float *x, int N, int Cin, int H, int W, const float *w,
                           const float *cb, int Cout, int KH, int KW, float scale, const float *bias,
                           int pk, int ps, float *out, int Ho, int Wo, cudaStream_t st) {
+    if (convpool_tc_eligible(Cin, Cout, KH, KW, pk, ps) && !convpool_force_ffma())
+        return convpool_tc_launch(x, N, H, W, w, cb, Cout, scale, bias, pk, out, Ho, Wo, st);
     if (KH == 3 && KW == 3 && pk == ps && Cin <= MAX_CIN && N <= 65535 && (pk == 4 || pk == 2)) {
         if (pk == 4) return launch_tiled<4>(x, N, Cin, H, W, w, cb, Cout, scale, bias, out, Ho, Wo, st);
         return launch_tiled<2>(x, N, Cin, H, W, w, cb, Cout, scale, bias, out, Ho, Wo, st);

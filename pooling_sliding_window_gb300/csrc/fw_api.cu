@@ -12,6 +12,7 @@ fw_status maxpool2d_launch(const float *x, long long NC, int H, int W, int k, in
                            int Wo, float *out, cudaStream_t st);
 unsigned maxpool_read_and_clear_error();
 unsigned convt_tc_read_and_clear_error();
+unsigned convpool_tc_read_and_clear_error();
 fw_status convpool_launch(const float *x, int N, int Cin, int H, int W, const float *w, const float *cb,
                           int Cout, int KH, int KW, float scale, const float *bias, int pk, int ps,
                           float *out, int Ho, int Wo, cudaStream_t st);
@@ -208,7 +209,8 @@ fw_status fw_convtranspose2d_softmax_bias_scale_sigmoid(const float *x, int N, i
 
 fw_status fw_check_device_errors(void *stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FW_ERR_LAUNCH;
-    const unsigned e = maxpool_read_and_clear_error() | convt_tc_read_and_clear_error();
+    const unsigned e = maxpool_read_and_clear_error() | convt_tc_read_and_clear_error() |
+                         convpool_tc_read_and_clear_error();
     if (e & DEVERR_TIMEOUT) return FW_ERR_TIMEOUT;
     if (e) return FW_ERR_INTERNAL;
     return FW_OK;

@@ -107,3 +107,26 @@ def test_errors_raise():
         FW.fw_conv2d_tanh_scale_bias_maxpool(x, w, None, b, float("nan"), 4)
     with pytest.raises(FW.FusedWinError, match="FW_ERR_SHAPE"):
         FW.fw_conv2d_tanh_scale_bias_maxpool(x[:, :, :4, :4].contiguous(), w, None, b, 2.0, 4)
+
+
+def test_ffma_kernel_when_forced():
+    """The FP32-FMA tiled kernel (selected with FUSEDWIN_CONVPOOL_FFMA=1) on shapes the
+    tensor-core kernel takes, in a fresh process."""
+    import os
+    import subprocess
+    import sys
+    import textwrap
+    code = textwrap.dedent("""
+        from tests.parity import FW, O, TOL_FFMA, assert_close, dev, host, synth
+        for (N, H, W, Cout, pk) in ((2, 64, 64, 64, 4), (1, 41, 33, 16, 2)):
+            d = synth.convpool_inputs(N, 8, H, W, Cout, seed=H)
+            got = host(FW.fw_conv2d_tanh_scale_bias_maxpool(dev(d["x"]), dev(d["w"]), dev(d["conv_b"]),
+                                                            dev(d["bias"]), 2.0, pk))
+            want = O.conv2d_tanh_scale_bias_maxpool(d["x"], d["w"], d["conv_b"], 2.0, d["bias"], pk)
+            assert_close(got, want, TOL_FFMA, str((N, H, W, Cout, pk)))
+        print("ok")
+    """)
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, capture_output=True, text=True,
+                       env=dict(os.environ, FUSEDWIN_CONVPOOL_FFMA="1"), timeout=600)
+    assert r.returncode == 0 and "ok" in r.stdout, r.stdout + r.stderr
