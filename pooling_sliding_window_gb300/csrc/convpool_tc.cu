@@ -18,11 +18,13 @@
 //     positions), so tap (kh, kw) of conv row j is the start address of the MMA's
 //     A operand moved by (j+kh)*130 + kw positions;
 //   * the weights, split into hi/lo in the CTA prologue, stay resident.
-// CTA roles (288 threads, one CTA per SM, persistent over items):
-//   warps 0-3  producers: load and split a slab (two stages);
-//   warp  8    allocates TMEM; one lane issues 3 x 9 x P MMAs per item into one of
-//              two accumulator sets;
-//   warps 4-7  epilogue: a thread owns one conv column (TMEM lane); the max over
+// CTA roles (416 threads, one CTA per SM, persistent over items):
+//   warps 0-3   producers: load and split a slab (two stages);
+//   warp  12    allocates TMEM; one lane issues 3 x 9 x P MMAs per item into one of
+//               two accumulator sets;
+//   warps 4-11  epilogue, every warp on every item (warps 4-7 and 8-11 take
+//              alternate 16-channel chunks): a thread owns one conv column (TMEM
+//              lane) of one TMEM lane quarter; the max over
 //              the P rows is taken in registers, the max over the P columns of a
 //              window by a butterfly over lanes that halves the channels each lane
 //              keeps at every step, then out = bias + scale*tanh(m + conv_b).
@@ -38,8 +40,10 @@ namespace {
 constexpr int MT = 128;       // conv columns per item (MMA M)
 constexpr int SW = MT + 2;    // slab row pitch in positions
 constexpr int NSTAGE = 2;
-constexpr int NTHREADS = 288;
-constexpr int MMA_WARP = 8;
+constexpr int EPI_WARP0 = 4;     // warps 4-11: epilogue
+constexpr int MMA_WARP = 12;
+constexpr int NTHREADS = (MMA_WARP + 1) * 32;
+constexpr float LOG2E = 1.4426950408889634f;
 constexpr int ACC_STRIDE = 256;  // TMEM columns between the two accumulator sets
 
 struct Bars {
@@ -61,11 +65,20 @@ struct Cfg {
     static constexpr int BPLANE = N * 16;             // bytes per (split, tap, plane) of B
     static constexpr int B_BYTES = 2 * 9 * G * BPLANE;
     static constexpr int NITER = (ROWS * SW + 127) / 128;
-    static constexpr size_t SMEM = (size_t)B_BYTES + NSTAGE * SLAB + sizeof(Bars);
+    static constexpr size_t SMEM = (size_t)B_BYTES + NSTAGE * SLAB + 2 * N * 4 + sizeof(Bars);
 };
 
 __device__ __forceinline__ float upd(float m, float v, bool use_min) {
     return use_min ? min_update(m, v) : max_update(m, v);
+}
+
+// tanh(z) = 1 - 2 / (1 + e^(2z)) with a base-2 exponential and a fast reciprocal:
+// absolute error a few 1e-7 over all z (e^(2z) overflows to inf for large z and
+// gives exactly 1; underflows to 0 for very negative z and gives exactly -1).
+__device__ __forceinline__ float tanh_fast(float z) {
+    float e;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(z * (2.f * LOG2E)));
+    return 1.f - __fdividef(2.f, 1.f + e);
 }
 
 template <int G, int P, int N>
@@ -77,12 +90,18 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
     extern __shared__ __align__(1024) unsigned char smem[];
     unsigned char *sB = smem;
     unsigned char *sSlab = smem + C::B_BYTES;
-    Bars &bars = *reinterpret_cast<Bars *>(sSlab + NSTAGE * C::SLAB);
+    float *sCb = reinterpret_cast<float *>(sSlab + NSTAGE * C::SLAB);
+    float *sBias = sCb + N;
+    Bars &bars = *reinterpret_cast<Bars *>(sBias + N);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const long long n_items = (long long)Nimg * Ho * ncb;
     const bool use_min = scale < 0.f;
 
+    for (int i = tid; i < N; i += NTHREADS) {
+        sCb[i] = cb ? __ldg(cb + i) : 0.f;
+        sBias[i] = __ldg(bias + i);
+    }
     // Weights split into TF32 hi/lo: B[split][tap][plane][co][c4].
     for (int e = tid; e < 9 * C::CIN * N; e += NTHREADS) {
         const int co = e % N, t = e / N, ci = t % C::CIN, tap = t / C::CIN;
@@ -99,7 +118,7 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&bars.acc_full[b]), 1);
-            mbar_init(smem_u32(&bars.acc_empty[b]), 4);
+            mbar_init(smem_u32(&bars.acc_empty[b]), 8);  // the 8 epilogue warps
         }
         bars.abort = 0;
         fence_mbar_init();
@@ -181,7 +200,11 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
                     break;
                 }
                 tc::fence_after_sync();
-                const uint32_t slab = sSlab_addr + stage * C::SLAB;
+                // Base descriptors; every tap / K step / split only moves the start
+                // address, i.e. adds (bytes >> 4) to the low field (no carry: shared
+                // addresses stay below 2^18).
+                const uint64_t a0 = tc::smem_desc(sSlab_addr + stage * C::SLAB, C::PLANE, 128);
+                const uint64_t b0 = tc::smem_desc(sB_addr, C::BPLANE, 128);
 #pragma unroll
                 for (int j = 0; j < P; ++j) {
                     const uint32_t d = tmem + (uint32_t)(buf * ACC_STRIDE + j * N);
@@ -191,12 +214,10 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
                         const int off = ((j + tap / 3) * SW + tap % 3) * 16;
 #pragma unroll
                         for (int s = 0; s < G / 2; ++s) {
-                            const uint32_t a_hi = slab + 2 * s * C::PLANE + off;
-                            const uint32_t b_hi = sB_addr + (tap * G + 2 * s) * C::BPLANE;
-                            const uint64_t ah = tc::smem_desc(a_hi, C::PLANE, 128);
-                            const uint64_t al = tc::smem_desc(a_hi + C::SPLIT, C::PLANE, 128);
-                            const uint64_t bh = tc::smem_desc(b_hi, C::BPLANE, 128);
-                            const uint64_t bl = tc::smem_desc(b_hi + 9 * G * C::BPLANE, C::BPLANE, 128);
+                            const uint64_t ah = a0 + (uint64_t)((2 * s * C::PLANE + off) >> 4);
+                            const uint64_t al = ah + (uint64_t)(C::SPLIT >> 4);
+                            const uint64_t bh = b0 + (uint64_t)(((tap * G + 2 * s) * C::BPLANE) >> 4);
+                            const uint64_t bl = bh + (uint64_t)((9 * G * C::BPLANE) >> 4);
                             tc::mma_tf32(d, al, bh, IDESC, acc);
                             tc::mma_tf32(d, ah, bl, IDESC, 1);
                             tc::mma_tf32(d, ah, bh, IDESC, 1);
@@ -211,7 +232,10 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
         __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue
+        // All 8 epilogue warps serve every item: warp w reads TMEM lane quarter w % 4
+        // and the 16-channel chunks c with c % 2 == (w - 4) / 4.
         const int q = warp & 3;
+        const int half = (warp - EPI_WARP0) >> 2;
         int k = 0;
         for (long long item = blockIdx.x; item < n_items && !*abort_flag; item += gridDim.x, ++k) {
             const int buf = k & 1;
@@ -229,16 +253,17 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
             const bool valid = pw < Wo;
             const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * ACC_STRIDE);
 #pragma unroll
-            for (int c0 = 0; c0 < N; c0 += 16) {
-                float m[16], v[16];
-                tc::ld16(taddr + c0, m);
+            for (int c0 = 16 * half; c0 < N; c0 += 32) {
+                float v[P][16];
+#pragma unroll
+                for (int j = 0; j < P; ++j) tc::ld16(taddr + j * N + c0, v[j]);
                 tc::wait_ld();
+                float m[16];
 #pragma unroll
-                for (int j = 1; j < P; ++j) {
-                    tc::ld16(taddr + j * N + c0, v);
-                    tc::wait_ld();
+                for (int i = 0; i < 16; ++i) {
+                    m[i] = v[0][i];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) m[i] = upd(m[i], v[i], use_min);
+                    for (int j = 1; j < P; ++j) m[i] = upd(m[i], v[j][i], use_min);
                 }
                 // butterfly over the P lanes of a window: keep half the channels per step
                 const int b0 = lane & 1;
@@ -271,10 +296,8 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
                     for (int i = 0; i < 8; ++i) {
                         if (i < nres) {
                             const int co = cbase + i;
-                            const float cbv = cb ? __ldg(cb + co) : 0.f;
-                            const float tv = tanhf(res[i] + cbv);
-                            out[((n * N + co) * Ho + pr) * (long long)Wo + pw] =
-                                __fadd_rn(__fmul_rn(tv, scale), __ldg(bias + co));
+                            const float tv = tanh_fast(res[i] + sCb[co]);
+                            out[((n * N + co) * Ho + pr) * (long long)Wo + pw] = __fadd_rn(__fmul_rn(tv, scale), sBias[co]);
                         }
                     }
                 }
