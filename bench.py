@@ -82,17 +82,23 @@ def dist_env():
     return ws, rank, local
 
 
+# Nominal dense tensor-core ratio TF32 : BF16 on GB300 (1.1 : 2.25 PFLOP/s).
+TF32_PER_BF16 = 1.1 / 2.25
+
+
 def peaks():
-    """Roofline denominators: measured HBM copy GB/s; FP32 FMA peak from unit counts and clock."""
+    """Roofline denominators: measured HBM copy GB/s and measured bf16 tensor TFLOP/s
+    (the TF32 peak is the bf16 one times the nominal TF32:BF16 ratio)."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     src = "measured"
     try:
         mp = json.load(open(path))
         hbm = float(mp["hbm_gbs"])
+        bf16 = float(mp["bf16_tflops"])
         sm_max = float(mp.get("sm_max_mhz", 2070.0))
     except Exception:  # noqa: BLE001
-        hbm, sm_max, src = 6800.0, 2070.0, "fallback"
-    return dict(hbm_gbs=hbm, hbm_src=src, sm_max_mhz=sm_max)
+        hbm, bf16, sm_max, src = 6800.0, 1900.0, 2070.0, "fallback"
+    return dict(hbm_gbs=hbm, hbm_src=src, sm_max_mhz=sm_max, tf32_tflops=bf16 * TF32_PER_BF16)
 
 
 def fp32_peak_tflops(sm_count, mhz):
@@ -281,7 +287,9 @@ def config_obj():
                          "convT x[128,64,64,64] ConvTranspose2d(64->128,k4,s2,p1,op1)+softmax(1)+bias+*2+sigmoid"
                          "->[128,128,129,129]"),
             "seed": 0, "l2": "inputs larger than L2 (268 MB, 2.15 GB, 134 MB); no flush",
-            "precision": "fp32 FFMA, accurate tanhf/expf", "parallelism": "weak scaling over GPUs, no collective"}
+            "precision": ("fp32 in/out; conv+pool on tensor cores with a 3xTF32 split, convT on TF32 tensor "
+                          "cores (both within 1e-5 of the float64 oracle); maxpool exact"),
+            "parallelism": "weak scaling over GPUs, no collective"}
 
 
 # ---------------------------------------------------------------- GPU arm --
@@ -316,9 +324,10 @@ def run_gpu(args):
         def op_cp(src, out):
             FW.fw_conv2d_tanh_scale_bias_maxpool(src[("cp", "x")], src[("cp", "w")], src[("cp", "conv_b")],
                                                  src[("cp", "bias")], CP["scale"], 4, out=out)
-        specs.append(dict(name="convpool", work=cp_flops(N=n), unit="TFLOP/s", scale=1e12, bound="alu",
+        specs.append(dict(name="convpool", work=cp_flops(N=n), unit="TFLOP/s", scale=1e12, bound="tensor",
                           run=lambda: op_cp(d, out_cp), e2e=lambda: op_cp(pinned, h_cp), out=h_cp,
-                          kernel="convpool3x3_ffma_kernel<4>", source="convpool.cu"))
+                          kernel="convpool_tc_kernel<2,4,64> (tcgen05 kind::tf32, 3xTF32 split: "
+                                 "executed tensor FLOPs = 3 x algorithmic)", source="convpool_tc.cu"))
     if mp:
         n = mp["x"].shape[0]
         out_mp = torch.empty(n, MP["C"], 511, 511, device=dev)
@@ -340,9 +349,10 @@ def run_gpu(args):
             FW.fw_convtranspose2d_softmax_bias_scale_sigmoid(src[("ct", "x")], src[("ct", "w")],
                                                              src[("ct", "conv_b")], src[("ct", "bias")],
                                                              CT["scale"], out=out, workspace=wsp)
-        specs.append(dict(name="convt", work=ct_flops(N=n), unit="TFLOP/s", scale=1e12, bound="alu",
+        specs.append(dict(name="convt", work=ct_flops(N=n), unit="TFLOP/s", scale=1e12, bound="tensor",
                           run=lambda: op_ct(d, out_ct), e2e=lambda: op_ct(pinned, h_ct), out=h_ct,
-                          kernel="convt_k4s2_ffma_kernel (+ weight prepack)", source="convt.cu"))
+                          kernel="convt_k4s2_tc_kernel<16> (tcgen05 kind::tf32) + weight prepack",
+                          source="convt_tc.cu"))
 
     def barrier():
         if ws > 1:
@@ -410,7 +420,7 @@ def run_gpu(args):
     ops = {}
     for sp, ms in zip(specs, op_ms):
         ach = sp["work"] / (ms * 1e-3) / sp["scale"]
-        peak = fp32_peak if sp["bound"] == "alu" else pk["hbm_gbs"]
+        peak = {"alu": fp32_peak, "tensor": pk["tf32_tflops"], "hbm": pk["hbm_gbs"]}[sp["bound"]]
         ops[sp["name"]] = dict(ms=ms, achieved=ach, unit=sp["unit"], bound=sp["bound"], peak=peak,
                                frac=ach / peak, work_per_launch=sp["work"], kernel=sp["kernel"])
     dom_i = max(range(len(specs)), key=lambda j: op_ms[j])
@@ -418,10 +428,12 @@ def run_gpu(args):
     dv = ops[dom["name"]]
     roofline = {"bound": dv["bound"], "achieved": dv["achieved"], "peak": dv["peak"], "unit": dv["unit"],
                 "frac": dv["frac"], "traffic": traffic_for(dom["name"]), "kernel": dv["kernel"],
-                "peak_source": ("FP32 FMA pipe: SMs x 128 lanes x 2 FLOP x max SM clock "
-                                f"({props.multi_processor_count} x 128 x 2 x {pk['sm_max_mhz']:.0f} MHz)"
-                                if dv["bound"] == "alu" else
-                                f"HBM copy GB/s, {pk['hbm_src']} (MEASURED_PEAKS.json)")}
+                "peak_source": {
+                    "alu": "FP32 FMA pipe: SMs x 128 lanes x 2 FLOP x max SM clock "
+                           f"({props.multi_processor_count} x 128 x 2 x {pk['sm_max_mhz']:.0f} MHz)",
+                    "tensor": f"dense TF32 = measured bf16 burst x {TF32_PER_BF16:.4f} (nominal 1.1/2.25), "
+                              f"{pk['hbm_src']} (MEASURED_PEAKS.json)",
+                    "hbm": f"HBM copy GB/s, {pk['hbm_src']} (MEASURED_PEAKS.json)"}[dv["bound"]]}
     by = {sp["name"]: (sp, ms, ems) for sp, ms, ems in zip(specs, op_ms, e2e_ms)}
     head = "convpool" if "convpool" in by else specs[0]["name"]
     hs, hms, hems = by[head]
@@ -431,7 +443,7 @@ def run_gpu(args):
     line = {
         "metric": METRIC, "value": weak_value(hs["work"], ws, hms) / hs["scale"], "unit": hs["unit"],
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "tf32+f32",
         "data": "synthetic (seeded SplitMix64 / Box-Muller, the pages' shapes)", "config": config_obj(),
     }
     if "maxpool" in by:
@@ -439,7 +451,7 @@ def run_gpu(args):
         line["maxpool_hbm_gbs"] = weak_value(sp["work"], ws, ms) / 1e9
         line["maxpool_hbm_frac"] = ops["maxpool"]["frac"]
     if "convpool" in by:
-        line["convpool_fp32_frac"] = ops["convpool"]["frac"]
+        line["convpool_tensor_frac"] = ops["convpool"]["frac"]
     if "convt" in by:
         sp, ms, _ = by["convt"]
         line["convt_tflops"] = weak_value(sp["work"], ws, ms) / 1e12
