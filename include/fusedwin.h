@@ -112,8 +112,9 @@ fw_status fw_conv2d_tanh_scale_bias_maxpool(const float *x, int N, int Cin, int 
  *
  * x   [N, C, H, W];  out [N, C, Ho, Wo] (see fw_maxpool2d_out_shape)
  * k >= 1, s >= 1, p >= 0, d >= 1.
- * Stride 1, dilation 1, k <= 5, p <= 4 and W a multiple of 4 (16-byte rows) take
- * the streaming kernel; other arguments take a direct one.
+ * Stride 1, dilation 1, k <= 5, p <= min(2, k-1), W a multiple of 4 (16-byte rows)
+ * from 32 to 2040 and a 16-byte aligned x take the streaming kernel; other
+ * arguments take a direct one.
  */
 fw_status fw_maxpool2d(const float *x, int N, int C, int H, int W, int k, int s, int p, int d,
                        float *out, void *stream);

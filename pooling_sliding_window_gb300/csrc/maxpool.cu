@@ -8,10 +8,12 @@
 //     engine (one cp.async.bulk per row) into a ring of NSTAGE slots, each slot
 //     holding `rps` rows; an mbarrier per slot completes on the copied bytes;
 //   * each row is read once from shared memory (float4 + edge scalars from -inf
-//     guard columns, which realise the padding), reduced horizontally, and kept
-//     in a K-deep register ring; every new row completes one output row, reduced
-//     vertically in kh order (separable max: the page's row-max-then-column-max
-//     decomposition, exact for max);
+//     guard columns, which realise the padding), reduced horizontally (a pairwise
+//     tree for k = 4), and kept in a K-deep register ring; every new row
+//     completes one output row, reduced vertically (separable max: the page's
+//     row-max-then-column-max decomposition, exact for max).  The reductions use
+//     the single-instruction max.NaN (NaN propagates); a zero maximum, whose sign
+//     the definition fixes by tap order, is recomputed tap by tap;
 //   * output rows (W odd in general, so not 16-byte aligned) are transposed
 //     through a per-warp shared buffer so that each store instruction writes 32
 //     consecutive floats.
@@ -28,12 +30,35 @@ namespace {
 constexpr int NSTAGE = 4;   // ring slots
 constexpr int GUARD = 4;    // -inf columns on each side of a shared-memory row
 
+// max.NaN: the larger value, or a canonical NaN when either input is NaN.
+__device__ __forceinline__ float max_nan(float a, float b) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+
+// The definition's window maximum for one output (taps in row-major order,
+// -inf padding, first of equal values kept), read from global memory.
+template <int K, int P>
+__device__ __noinline__ float window_max_exact(const float *__restrict__ plane, int H, int W, int oh, int ow) {
+    float m = -INFINITY;
+    for (int i = 0; i < K; ++i) {
+        const int ih = oh - P + i;
+        for (int j = 0; j < K; ++j) {
+            const int iw = ow - P + j;
+            const float v = (ih >= 0 && ih < H && iw >= 0 && iw < W) ? __ldg(plane + (long long)ih * W + iw) : -INFINITY;
+            m = max_update(m, v);
+        }
+    }
+    return m;
+}
+
 // Shared-memory row pitch (floats): GUARD -inf columns, the W data columns, and
 // -inf columns up to and past the last column any thread of the block reads.
 __host__ __device__ inline int stream_pitch(int threads) { return 4 * threads + 4 * GUARD; }
 
 template <int K, int P>
-__global__ void __launch_bounds__(1024) maxpool_s1_stream_kernel(const float *__restrict__ x,
+__global__ void __launch_bounds__(512) maxpool_s1_stream_kernel(const float *__restrict__ x,
                                                                  float *__restrict__ out, int H, int W,
                                                                  int Ho, int Wo, int band, int nbands,
                                                                  int rps) {
@@ -80,90 +105,113 @@ __global__ void __launch_bounds__(1024) maxpool_s1_stream_kernel(const float *__
         for (int st = 0; st < min(NSTAGE, nst); ++st) issue(st);
     }
 
-    // Register ring of the last K horizontal-max rows (4 columns each).
+    // Register ring of the last K horizontal-max rows (4 columns each); row ir
+    // lives in hist[(ir - ir_begin) % K], so the unrolled loop below indexes it
+    // statically.
     float4 hist[K];
 #pragma unroll
     for (int i = 0; i < K; ++i) hist[i] = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
 
     const int c0 = 4 * tid + GUARD;  // this thread's first column in a shared row
+    const float *xplane = src;
     bool err = false, any_err = false;
-    int cur_stage = -1;
+    int st = 0, r_in_st = 0, st_rows = min(rps, lb - la);
     // Walk input rows ir = r0-P .. r1-2-P+K (rows outside [0,H) are all -inf).
     const int ir_begin = r0 - P, ir_end = r1 - 1 - P + K;
-    for (int ir = ir_begin; ir < ir_end; ++ir) {
-        float4 h = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-        if (ir >= la && ir < lb) {
-            const int st = (ir - la) / rps;
-            const int slot = st % NSTAGE;
-            if (st != cur_stage) {
-                cur_stage = st;
-                if (!mbar_wait_bounded(smem_u32(&bars[slot]), (uint32_t)(st / NSTAGE) & 1u)) err = true;
-            }
-            const float *row = ring + ((size_t)slot * rps + (ir - la - st * rps)) * pitch;
-            // window of 3+K values: columns 4t-P .. 4t+2-P+K
-            float v[K + 3];
-            const float4 mid = *reinterpret_cast<const float4 *>(row + c0);
+    for (int base = ir_begin; base < ir_end && !any_err; base += K) {
 #pragma unroll
-            for (int i = 0; i < K + 3; ++i) {
-                const int c = i - P;  // offset from 4t
-                if (c == 0) v[i] = mid.x;
-                else if (c == 1) v[i] = mid.y;
-                else if (c == 2) v[i] = mid.z;
-                else if (c == 3) v[i] = mid.w;
-                else v[i] = row[c0 + c];
-            }
-            float hv[4];
+        for (int u = 0; u < K; ++u) {
+            const int ir = base + u;
+            if (ir >= ir_end) break;
+            float4 h = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            if (ir >= la && ir < lb) {
+                const int slot = st % NSTAGE;
+                if (r_in_st == 0 && !mbar_wait_bounded(smem_u32(&bars[slot]), (uint32_t)(st / NSTAGE) & 1u))
+                    err = true;
+                const float *row = ring + ((size_t)slot * rps + r_in_st) * pitch;
+                // window of 3+K values: columns 4t-P .. 4t+2-P+K
+                float v[K + 3];
+                const float4 mid = *reinterpret_cast<const float4 *>(row + c0);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                float m = v[j];
-#pragma unroll
-                for (int kw = 1; kw < K; ++kw) m = max_update(m, v[j + kw]);
-                hv[j] = m;
-            }
-            h = make_float4(hv[0], hv[1], hv[2], hv[3]);
-            // Last row of this stage consumed: release the slot, refill it.
-            const int st_last = min(lb, la + (st + 1) * rps) - 1;
-            if (ir == st_last) {
-                if (__syncthreads_or(err)) {
-                    if (tid == 0) atomicOr(&g_err_maxpool, DEVERR_TIMEOUT);
-                    any_err = true;
-                    break;
+                for (int i = 0; i < K + 3; ++i) {
+                    const int c = i - P;  // offset from 4t
+                    if (c == 0) v[i] = mid.x;
+                    else if (c == 1) v[i] = mid.y;
+                    else if (c == 2) v[i] = mid.z;
+                    else if (c == 3) v[i] = mid.w;
+                    else v[i] = row[c0 + c];
                 }
-                if (tid == 0 && st + NSTAGE < nst) {
-                    fence_proxy_async_smem();
-                    issue(st + NSTAGE);
+                float hv[4];
+                if (K == 4) {  // pairwise tree: 10 max for 4 outputs
+                    float a[6];
+#pragma unroll
+                    for (int i = 0; i < 6; ++i) a[i] = max_nan(v[i], v[i + 1]);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) hv[j] = max_nan(a[j], a[j + 2]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        float m = v[j];
+#pragma unroll
+                        for (int kw = 1; kw < K; ++kw) m = max_nan(m, v[j + kw]);
+                        hv[j] = m;
+                    }
+                }
+                h = make_float4(hv[0], hv[1], hv[2], hv[3]);
+                if (++r_in_st == st_rows) {  // stage consumed: release the slot, refill it
+                    if (__syncthreads_or(err)) {
+                        if (tid == 0) atomicOr(&g_err_maxpool, DEVERR_TIMEOUT);
+                        any_err = true;
+                        break;
+                    }
+                    if (tid == 0 && st + NSTAGE < nst) {
+                        fence_proxy_async_smem();
+                        issue(st + NSTAGE);
+                    }
+                    ++st;
+                    r_in_st = 0;
+                    st_rows = min(rps, lb - (la + st * rps));
                 }
             }
-        }
+            hist[u] = h;
+            const int oh = ir + P - (K - 1);  // output row whose last window row is ir
+            if (oh >= r0) {
+                float4 m = hist[(u + 1) % K];
 #pragma unroll
-        for (int i = 0; i < K - 1; ++i) hist[i] = hist[i + 1];
-        hist[K - 1] = h;
-        const int oh = ir + P - (K - 1);  // output row whose last window row is ir
-        if (oh >= r0) {
-            float4 m = hist[0];
+                for (int i = 2; i <= K; ++i) {
+                    const float4 g = hist[(u + i) % K];
+                    m.x = max_nan(m.x, g.x);
+                    m.y = max_nan(m.y, g.y);
+                    m.z = max_nan(m.z, g.z);
+                    m.w = max_nan(m.w, g.w);
+                }
+                // max.NaN leaves the sign of a zero maximum to the hardware; the
+                // definition keeps the first zero of the window, so a zero result
+                // is recomputed tap by tap (rare).
+                if (m.x == 0.f || m.y == 0.f || m.z == 0.f || m.w == 0.f) {
+                    float r[4] = {m.x, m.y, m.z, m.w};
 #pragma unroll
-            for (int i = 1; i < K; ++i) {
-                m.x = max_update(m.x, hist[i].x);
-                m.y = max_update(m.y, hist[i].y);
-                m.z = max_update(m.z, hist[i].z);
-                m.w = max_update(m.w, hist[i].w);
-            }
-            float *os = ostage + warp * 128;
-            __syncwarp();
-            *reinterpret_cast<float4 *>(os + lane * 4) = m;
-            __syncwarp();
-            float *orow = dst + (long long)oh * Wo + warp * 128;
+                    for (int j = 0; j < 4; ++j)
+                        if (r[j] == 0.f) r[j] = window_max_exact<K, P>(xplane, H, W, oh, 4 * tid + j);
+                    m = make_float4(r[0], r[1], r[2], r[3]);
+                }
+                float *os = ostage + warp * 128;
+                __syncwarp();
+                *reinterpret_cast<float4 *>(os + lane * 4) = m;
+                __syncwarp();
+                float *orow = dst + (long long)oh * Wo + warp * 128;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int c = q * 32 + lane;
-                if (warp * 128 + c < Wo) orow[c] = os[c];
+                for (int q = 0; q < 4; ++q) {
+                    const int c = q * 32 + lane;
+                    if (warp * 128 + c < Wo) orow[c] = os[c];
+                }
             }
         }
     }
     if (any_err && tid == 0) {
         // Drain copies still in flight into this CTA's shared memory (bounded).
-        for (int st = max(0, cur_stage); st < min(nst, cur_stage + NSTAGE); ++st)
-            mbar_wait_bounded(smem_u32(&bars[st % NSTAGE]), (uint32_t)(st / NSTAGE) & 1u);
+        for (int s2 = st; s2 < min(nst, st + NSTAGE); ++s2)
+            mbar_wait_bounded(smem_u32(&bars[s2 % NSTAGE]), (uint32_t)(s2 / NSTAGE) & 1u);
     }
 }
 
@@ -197,7 +245,7 @@ fw_status launch_stream(const float *x, float *out, long long NC, int H, int W, 
                         cudaStream_t st) {
     // Threads cover every output column group; those past W/4 read -inf guards.
     const int threads = ((max(W, Wo) + 3) / 4 + 31) / 32 * 32;
-    if (threads > 1024) return FW_ERR_UNSUPPORTED;
+    if (threads > 512) return FW_ERR_UNSUPPORTED;
     const int pitch = stream_pitch(threads);
     const int row_bytes = W * 4;
     const int rps = max(1, min(8, 8192 / row_bytes));
@@ -233,7 +281,7 @@ StreamFn stream_fn(int k, int p) {
 fw_status maxpool2d_launch(const float *x, long long NC, int H, int W, int k, int s, int p, int d,
                            int Ho, int Wo, float *out, cudaStream_t st) {
     const bool aligned = ((reinterpret_cast<uintptr_t>(x) & 15u) == 0);
-    if (s == 1 && d == 1 && aligned && W % 4 == 0 && W >= 32 && W <= 4000) {
+    if (s == 1 && d == 1 && aligned && W % 4 == 0 && W >= 32 && W <= 2040) {
         if (StreamFn f = stream_fn(k, p)) return f(x, out, NC, H, W, Ho, Wo, st);
     }
     const long long total = NC * Ho * Wo;
