@@ -194,6 +194,14 @@ fw_status fw_check_device_errors(void *stream);
  * devices, all calls).  Used to count launches inside a timed region. */
 unsigned long long fw_launch_count(void);
 
+/* Diagnostic with no counterpart on the pages: launches one small kernel whose
+ * mbarrier wait is never satisfied, so it gives up after limit_us microseconds
+ * (1 .. 2,000,000), records a timeout in the device error word and returns --
+ * the same bounded-wait path every kernel of the library takes if a stage never
+ * arrives.  The next fw_check_device_errors() on that stream then returns
+ * FW_ERR_TIMEOUT, and the CUDA context stays usable. */
+fw_status fw_selftest_bounded_wait(unsigned int limit_us, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

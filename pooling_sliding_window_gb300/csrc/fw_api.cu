@@ -23,6 +23,29 @@ size_t convt_workspace_bytes(int Cin, int Cout, int k, int s, int p);
 
 static std::atomic<unsigned long long> g_launches{0};
 
+__device__ unsigned g_err_api = 0;
+
+// Waits on an mbarrier that nothing ever completes; the bounded wait runs out
+// after limit_ns and records a timeout in the error word -- the path every
+// kernel's waits take when a producer never arrives.
+__global__ void selftest_wait_kernel(unsigned long long limit_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const bool ok = mbar_wait_bounded(smem_u32(&bar), 0, limit_ns);
+    if (__syncthreads_or(!ok) && threadIdx.x == 0) atomicOr(&g_err_api, DEVERR_TIMEOUT);
+}
+
+unsigned api_read_and_clear_error() {
+    unsigned v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_err_api, sizeof(v)) != cudaSuccess) return DEVERR_INTERNAL;
+    if (v) cudaMemcpyToSymbol(g_err_api, &zero, sizeof(zero));
+    return v;
+}
+
 void note_launch(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
 
 fw_status launch_status(cudaError_t e) { return e == cudaSuccess ? FW_OK : FW_ERR_LAUNCH; }
@@ -207,10 +230,17 @@ fw_status fw_convtranspose2d_softmax_bias_scale_sigmoid(const float *x, int N, i
                         (size_t)workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
+fw_status fw_selftest_bounded_wait(unsigned int limit_us, void *stream) {
+    if (limit_us == 0 || limit_us > 2000000u) return FW_ERR_PARAM;
+    selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(1000ull * limit_us);
+    note_launch();
+    return launch_status(cudaGetLastError());
+}
+
 fw_status fw_check_device_errors(void *stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FW_ERR_LAUNCH;
     const unsigned e = maxpool_read_and_clear_error() | convt_tc_read_and_clear_error() |
-                         convpool_tc_read_and_clear_error();
+                         convpool_tc_read_and_clear_error() | api_read_and_clear_error();
     if (e & DEVERR_TIMEOUT) return FW_ERR_TIMEOUT;
     if (e) return FW_ERR_INTERNAL;
     return FW_OK;

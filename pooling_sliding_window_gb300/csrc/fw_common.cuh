@@ -82,14 +82,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Wait for phase `parity` of an mbarrier, giving up after WAIT_LIMIT_NS.
-// Returns false on timeout.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+// Wait for phase `parity` of an mbarrier, giving up after `limit_ns` (default
+// WAIT_LIMIT_NS).  Returns false on timeout.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  unsigned long long limit_ns = WAIT_LIMIT_NS) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
     for (unsigned it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 255u) == 0 && globaltimer_ns() - t0 > WAIT_LIMIT_NS) return false;
+        if ((it & 255u) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
     }
 }
 

@@ -28,7 +28,7 @@ STATUS = {0: "FW_OK", 1: "FW_ERR_NULL", 2: "FW_ERR_SHAPE", 3: "FW_ERR_PARAM", 4:
 EXPORTS = ("fw_status_string", "fw_version", "fw_conv2d_pool_out_shape", "fw_maxpool2d_out_shape",
            "fw_convt_out_shape", "fw_conv2d_tanh_scale_bias_maxpool", "fw_maxpool2d",
            "fw_convtranspose2d_softmax_bias_scale_sigmoid", "fw_convt_workspace_size",
-           "fw_check_device_errors", "fw_launch_count",
+           "fw_check_device_errors", "fw_launch_count", "fw_selftest_bounded_wait",
            "fw_convtranspose2d_softmax_bias_scale_sigmoid_noalloc")
 
 
@@ -71,6 +71,8 @@ def lib():
         L.fw_convt_workspace_size.argtypes = [I, I, I, I, I]
         L.fw_check_device_errors.restype = I
         L.fw_check_device_errors.argtypes = [P]
+        L.fw_selftest_bounded_wait.restype = I
+        L.fw_selftest_bounded_wait.argtypes = [C.c_uint, P]
         L.fw_convtranspose2d_softmax_bias_scale_sigmoid_noalloc.restype = I
         L.fw_convtranspose2d_softmax_bias_scale_sigmoid_noalloc.argtypes = [
             P, I, I, I, I, P, P, I, I, I, I, I, P, F, P, P]
@@ -107,6 +109,12 @@ def fw_convt_workspace_size(Cin, Cout, k, s, p) -> int:
 
 def fw_launch_count() -> int:
     return int(lib().fw_launch_count())
+
+
+def fw_selftest_bounded_wait(limit_us, stream=None):
+    """Launch the bounded-wait self-test kernel (see include/fusedwin.h)."""
+    s = torch.cuda.current_stream() if stream is None else stream
+    _check(lib().fw_selftest_bounded_wait(int(limit_us), C.c_void_p(s.cuda_stream)), "fw_selftest_bounded_wait")
 
 
 def fw_check_device_errors(stream=None):

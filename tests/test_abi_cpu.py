@@ -110,6 +110,9 @@ def test_operator_argument_errors_without_launch():
     assert ct(op=2) == 3
     assert ct(Cout=2048) == 6
     assert ct(out=P(0x80000000 + 4096)) == 4  # out overlaps workspace
+    # the bounded-wait self-test checks its limit before launching
+    assert L.fw_selftest_bounded_wait(0, None) == 3
+    assert L.fw_selftest_bounded_wait(2_000_001, None) == 3
 
 
 def test_product_path_fails_loudly_without_gpu():
