@@ -326,8 +326,9 @@ def run_gpu(args):
                                                  src[("cp", "bias")], CP["scale"], 4, out=out)
         specs.append(dict(name="convpool", work=cp_flops(N=n), unit="TFLOP/s", scale=1e12, bound="tensor",
                           run=lambda: op_cp(d, out_cp), e2e=lambda: op_cp(pinned, h_cp), out=h_cp,
-                          kernel="convpool_tc_kernel<2,4,64> (tcgen05 kind::tf32, 3xTF32 split: "
-                                 "executed tensor FLOPs = 3 x algorithmic)", source="convpool_tc.cu"))
+                          kernel="convpool_tc_kernel<4,64> (tcgen05 kind::tf32, 3xTF32 split as two MMAs "
+                                 "per tap, N = 128 [w_hi|w_lo] and N = 64: executed tensor FLOPs = 3 x "
+                                 "algorithmic)", source="convpool_tc.cu"))
     if mp:
         n = mp["x"].shape[0]
         out_mp = torch.empty(n, MP["C"], 511, 511, device=dev)

@@ -11,23 +11,31 @@
 // dropped): three MMAs per K step, float32 accumulation in TMEM.
 //
 // Work item = one pooled output row of one image and a block of 128 conv columns:
-//   * the P conv rows of the pooled row are P GEMMs, M = 128 columns, N = Cout,
-//     K = 9 taps x 8 channels, each into its own TMEM accumulator;
+//   * the P conv rows of the pooled row are P GEMMs, M = 128 columns, K = 9 taps x
+//     8 channels, each into one slot of a 4-slot TMEM accumulator ring;
+//   * the weights are stacked along N as [w_hi | w_lo] (N = 2*Cout), so one MMA
+//     gives x_hi*w_hi and x_hi*w_lo side by side and a second, N = Cout, adds
+//     x_lo*w_hi onto the first half: two MMAs per tap instead of three;
 //   * the input the item reads -- P+2 rows x 130 columns x 8 channels -- is staged
-//     as hi and lo planes of 4 channels (16 bytes per position, row pitch 130
-//     positions), so tap (kh, kw) of conv row j is the start address of the MMA's
-//     A operand moved by (j+kh)*130 + kw positions;
+//     per input row in "column-interleaved" core matrices: core i (i < 18) holds
+//     columns i, i+16, ..., i+112 as its 8 rows, both 4-channel planes side by
+//     side (256 bytes).  MMA row m = 8*i + r is then conv column i + 16*r, and
+//     tap (kh, kw) of conv row j is the start address moved by input row j+kh and
+//     kw whole core matrices: every operand start stays 256-byte aligned and the
+//     operands keep the compact K-major layout (K-adjacent core matrices 128 B
+//     apart, M-adjacent ones 256 B apart) that the tensor cores read at full rate.
+//     Columns 16..17 + 16k appear twice (as rows 0/1 of core 16/17 too);
 //   * the weights, split into hi/lo in the CTA prologue, stay resident.
 // CTA roles (416 threads, one CTA per SM, persistent over items):
 //   warps 0-3   producers: load and split a slab (two stages);
-//   warp  12    allocates TMEM; one lane issues 3 x 9 x P MMAs per item into one of
-//               two accumulator sets;
-//   warps 4-11  epilogue, every warp on every item (warps 4-7 and 8-11 take
-//              alternate 16-channel chunks): a thread owns one conv column (TMEM
-//              lane) of one TMEM lane quarter; the max over
-//              the P rows is taken in registers, the max over the P columns of a
-//              window by a butterfly over lanes that halves the channels each lane
-//              keeps at every step, then out = bias + scale*tanh(m + conv_b).
+//   warp  12    allocates TMEM; one lane issues 2 x 9 MMAs per conv row;
+//   warps 4-11  epilogue, every warp on every conv row: warp w reads TMEM lane
+//               quarter w % 4 and half the channels; the max over the P rows of a
+//               window is kept in registers while the rows arrive, the max over
+//               its P columns (lanes 8 apart) by a butterfly that halves the
+//               channels each lane keeps at every step; out = bias +
+//               scale*tanh(m + conv_b) goes through shared memory so that the
+//               global stores are row-contiguous.
 // Scale < 0 takes the window minimum instead (the map is then decreasing).
 #include "fw_common.cuh"
 
@@ -37,35 +45,42 @@ __device__ unsigned g_err_convpool_tc = 0;
 
 namespace {
 
-constexpr int MT = 128;       // conv columns per item (MMA M)
-constexpr int SW = MT + 2;    // slab row pitch in positions
+constexpr int MT = 128;          // conv columns per item (MMA M)
+constexpr int NCORE = MT / 8 + 2;  // core matrices per staged input row
+constexpr int CORE = 256;        // bytes of one core index: 2 planes x 8 rows x 16 B
+constexpr int RB = NCORE * CORE;   // bytes of one staged input row (per split)
+constexpr int SLOTS_ROW = NCORE * 8;  // staged positions per input row
 constexpr int NSTAGE = 2;
 constexpr int EPI_WARP0 = 4;     // warps 4-11: epilogue
+constexpr int NEPI = 8;
 constexpr int MMA_WARP = 12;
 constexpr int NTHREADS = (MMA_WARP + 1) * 32;
+constexpr int NSLOT = 4;         // TMEM accumulator ring, one conv row per slot
+constexpr int SLOT_COLS = 128;
 constexpr float LOG2E = 1.4426950408889634f;
-constexpr int ACC_STRIDE = 256;  // TMEM columns between the two accumulator sets
 
 struct Bars {
     uint64_t slab_full[NSTAGE];
     uint64_t slab_empty[NSTAGE];
-    uint64_t acc_full[2];
-    uint64_t acc_empty[2];
+    uint64_t slot_full[NSLOT];
+    uint64_t slot_empty[NSLOT];
+    uint64_t stg_full[2];
     uint32_t tmem_base;
     int abort;
 };
 
-template <int G, int P, int N>
+template <int P, int N>
 struct Cfg {
-    static constexpr int CIN = 4 * G;
     static constexpr int ROWS = P + 2;
-    static constexpr int PLANE = ROWS * SW * 16;      // bytes per 4-channel plane
-    static constexpr int SPLIT = G * PLANE;           // hi (or lo) half of a slab
+    static constexpr int SPLIT = ROWS * RB;           // hi (or lo) half of a slab
     static constexpr int SLAB = 2 * SPLIT;
-    static constexpr int BPLANE = N * 16;             // bytes per (split, tap, plane) of B
-    static constexpr int B_BYTES = 2 * 9 * G * BPLANE;
-    static constexpr int NITER = (ROWS * SW + 127) / 128;
-    static constexpr size_t SMEM = (size_t)B_BYTES + NSTAGE * SLAB + 2 * N * 4 + sizeof(Bars);
+    static constexpr int BTAP = (2 * N / 8) * CORE;   // one tap of [w_hi | w_lo]
+    static constexpr int B_BYTES = 9 * BTAP;
+    static constexpr int PW = MT / P;                 // pooled columns per item
+    static constexpr int STG = N * PW;                // floats of one staging buffer
+    static constexpr int NH = N / 2;                  // channels per epilogue warp
+    static constexpr size_t SMEM =
+        (size_t)B_BYTES + NSTAGE * SLAB + 2 * STG * 4 + 2 * N * 4 + sizeof(Bars);
 };
 
 __device__ __forceinline__ float upd(float m, float v, bool use_min) {
@@ -81,16 +96,18 @@ __device__ __forceinline__ float tanh_fast(float z) {
     return 1.f - __fdividef(2.f, 1.f + e);
 }
 
-template <int G, int P, int N>
+template <int P, int N>
 __global__ void __launch_bounds__(NTHREADS, 1)
 convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, const float *__restrict__ cb,
                    const float *__restrict__ bias, float scale, float *__restrict__ out, int Nimg, int H, int W,
-                   int Ho, int Wo, int ncb) {
-    using C = Cfg<G, P, N>;
+                   int Ho, int Wo, int ncb, bool vec) {
+    using C = Cfg<P, N>;
+    constexpr int CIN = 8;
     extern __shared__ __align__(1024) unsigned char smem[];
     unsigned char *sB = smem;
     unsigned char *sSlab = smem + C::B_BYTES;
-    float *sCb = reinterpret_cast<float *>(sSlab + NSTAGE * C::SLAB);
+    float *sStg = reinterpret_cast<float *>(sSlab + NSTAGE * C::SLAB);  // 2 staging buffers
+    float *sCb = sStg + 2 * C::STG;
     float *sBias = sCb + N;
     Bars &bars = *reinterpret_cast<Bars *>(sBias + N);
 
@@ -102,28 +119,30 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
         sCb[i] = cb ? __ldg(cb + i) : 0.f;
         sBias[i] = __ldg(bias + i);
     }
-    // Weights split into TF32 hi/lo: B[split][tap][plane][co][c4].
-    for (int e = tid; e < 9 * C::CIN * N; e += NTHREADS) {
-        const int co = e % N, t = e / N, ci = t % C::CIN, tap = t / C::CIN;
-        const float v = __ldg(w + ((long long)co * C::CIN + ci) * 9 + tap);
+    // Weights split into TF32 hi/lo: B[tap][co' / 8][plane][co' % 8][c4] with
+    // co' = co for w_hi and N + co for w_lo.
+    for (int e = tid; e < 9 * CIN * N; e += NTHREADS) {
+        const int co = e % N, t = e / N, ci = t % CIN, tap = t / CIN;
+        const float v = __ldg(w + ((long long)co * CIN + ci) * 9 + tap);
         const float hi = tc::to_tf32(v), lo = tc::to_tf32(v - hi);
-        const int off = ((tap * G + ci / 4) * N + co) * 16 + (ci % 4) * 4;
-        *reinterpret_cast<float *>(sB + off) = hi;
-        *reinterpret_cast<float *>(sB + 9 * G * C::BPLANE + off) = lo;
+        const int base = tap * C::BTAP + (ci / 4) * 128 + (ci % 4) * 4;
+        *reinterpret_cast<float *>(sB + base + (co / 8) * CORE + (co % 8) * 16) = hi;
+        *reinterpret_cast<float *>(sB + base + ((N + co) / 8) * CORE + ((N + co) % 8) * 16) = lo;
     }
     if (tid == 0) {
         for (int s = 0; s < NSTAGE; ++s) {
             mbar_init(smem_u32(&bars.slab_full[s]), 4);
             mbar_init(smem_u32(&bars.slab_empty[s]), 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(smem_u32(&bars.acc_full[b]), 1);
-            mbar_init(smem_u32(&bars.acc_empty[b]), 8);  // the 8 epilogue warps
+        for (int b = 0; b < NSLOT; ++b) {
+            mbar_init(smem_u32(&bars.slot_full[b]), 1);
+            mbar_init(smem_u32(&bars.slot_empty[b]), NEPI);
         }
+        for (int b = 0; b < 2; ++b) mbar_init(smem_u32(&bars.stg_full[b]), NEPI);
         bars.abort = 0;
         fence_mbar_init();
     }
-    if (warp == MMA_WARP) tc::alloc(smem_u32(&bars.tmem_base), 512);
+    if (warp == MMA_WARP) tc::alloc(smem_u32(&bars.tmem_base), NSLOT * SLOT_COLS);
     fence_proxy_async_smem();
     tc::fence_before_sync();
     __syncthreads();
@@ -137,6 +156,14 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
 
     if (warp < 4) {
         // ------------------------------------------------------------ producers
+        // Main task (row rr, group a, r): the 4 input columns 4a + 16r .. +3 of the
+        // block, i.e. row r of cores 4a .. 4a+3.  Lane r + 8a of a warp, so a warp's
+        // loads cover 512 contiguous bytes (one float4 per channel when x rows are
+        // 16-byte aligned) and its shared-memory stores hit 8 distinct 16-byte bank
+        // groups per 8 lanes.  Tail task (row rr, r, t): row r of core 16 + t,
+        // input column 16 + t + 16r (a second copy of a main-task column, or
+        // column 128 / 129 for r = 7).
+        constexpr int MTASK = C::ROWS * 32, MITER = (MTASK + 127) / 128, TTASK = C::ROWS * 16;
         const long long plane_stride = (long long)H * W;
         int k = 0;
         for (long long item = blockIdx.x; item < n_items && !*abort_flag; item += gridDim.x, ++k) {
@@ -146,38 +173,70 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
             const int pr = (int)(t % Ho);
             const long long n = t / Ho;
             const int row0 = pr * P, col0 = cblk * MT;
-            const float *xn = x + n * C::CIN * plane_stride;
-            float r[C::NITER][C::CIN];
+            const float *xn = x + n * CIN * plane_stride;
+            float4 vm[MITER][CIN];
 #pragma unroll
-            for (int it = 0; it < C::NITER; ++it) {
-                const int pos = tid + it * 128;
-                const int rr = pos / SW, cc = pos - (pos / SW) * SW;
-                const int row = row0 + rr, col = col0 + cc;
-                const bool ok = pos < C::ROWS * SW && row < H && col < W;
+            for (int it = 0; it < MITER; ++it) {
+                const int mt = tid + 128 * it;
+                const int rr = mt >> 5, a = (mt >> 3) & 3, r = mt & 7;
+                const int row = row0 + rr, col = col0 + 4 * a + 16 * r;
+                const float *src = xn + (long long)row * W + col;
+                const bool ok = mt < MTASK && row < H;
+                if (vec) {
+                    const bool in = ok && col < W;  // W % 4 == 0: the 4 columns are all in or all out
+#pragma unroll
+                    for (int ci = 0; ci < CIN; ++ci)
+                        vm[it][ci] = in ? __ldg(reinterpret_cast<const float4 *>(src + ci * plane_stride))
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+                } else {
+#pragma unroll
+                    for (int ci = 0; ci < CIN; ++ci) {
+                        const float *sp = src + ci * plane_stride;
+                        vm[it][ci].x = ok && col < W ? __ldg(sp) : 0.f;
+                        vm[it][ci].y = ok && col + 1 < W ? __ldg(sp + 1) : 0.f;
+                        vm[it][ci].z = ok && col + 2 < W ? __ldg(sp + 2) : 0.f;
+                        vm[it][ci].w = ok && col + 3 < W ? __ldg(sp + 3) : 0.f;
+                    }
+                }
+            }
+            float vt[CIN];
+            const int tr = tid >> 4, tu = tid & 15;  // tail task of this thread (tid < TTASK)
+            {
+                const int row = row0 + tr, col = col0 + 16 + (tu >> 3) + 16 * (tu & 7);
+                const bool ok = tid < TTASK && row < H && col < W;
                 const float *src = xn + (long long)row * W + col;
 #pragma unroll
-                for (int ci = 0; ci < C::CIN; ++ci) r[it][ci] = ok ? __ldg(src + ci * plane_stride) : 0.f;
+                for (int ci = 0; ci < CIN; ++ci) vt[ci] = ok ? __ldg(src + ci * plane_stride) : 0.f;
             }
             if (use > 0 && !mbar_wait_bounded(smem_u32(&bars.slab_empty[stage]), (use - 1) & 1)) fail();
             unsigned char *slab = sSlab + stage * C::SLAB;
+            // hi/lo split of 4 channels of one position into the two halves of the slab
+            auto put = [&](unsigned char *dst, float c0, float c1, float c2, float c3) {
+                const float h0 = tc::to_tf32(c0), h1 = tc::to_tf32(c1), h2 = tc::to_tf32(c2), h3 = tc::to_tf32(c3);
+                *reinterpret_cast<float4 *>(dst) = make_float4(h0, h1, h2, h3);
+                *reinterpret_cast<float4 *>(dst + C::SPLIT) =
+                    make_float4(tc::to_tf32(c0 - h0), tc::to_tf32(c1 - h1), tc::to_tf32(c2 - h2), tc::to_tf32(c3 - h3));
+            };
 #pragma unroll
-            for (int it = 0; it < C::NITER; ++it) {
-                const int pos = tid + it * 128;
-                if (pos < C::ROWS * SW) {
+            for (int it = 0; it < MITER; ++it) {
+                const int mt = tid + 128 * it;
+                if (mt < MTASK) {
+                    const int rr = mt >> 5, a = (mt >> 3) & 3, r = mt & 7;
+                    unsigned char *dst = slab + rr * RB + 4 * a * CORE + r * 16;
 #pragma unroll
-                    for (int g = 0; g < G; ++g) {
-                        float hi[4], lo[4];
-#pragma unroll
-                        for (int c4 = 0; c4 < 4; ++c4) {
-                            hi[c4] = tc::to_tf32(r[it][4 * g + c4]);
-                            lo[c4] = tc::to_tf32(r[it][4 * g + c4] - hi[c4]);
-                        }
-                        *reinterpret_cast<float4 *>(slab + g * C::PLANE + pos * 16) =
-                            make_float4(hi[0], hi[1], hi[2], hi[3]);
-                        *reinterpret_cast<float4 *>(slab + C::SPLIT + g * C::PLANE + pos * 16) =
-                            make_float4(lo[0], lo[1], lo[2], lo[3]);
+                    for (int g = 0; g < 2; ++g) {
+                        const float4 *v = &vm[it][4 * g];
+                        put(dst + g * 128, v[0].x, v[1].x, v[2].x, v[3].x);
+                        put(dst + CORE + g * 128, v[0].y, v[1].y, v[2].y, v[3].y);
+                        put(dst + 2 * CORE + g * 128, v[0].z, v[1].z, v[2].z, v[3].z);
+                        put(dst + 3 * CORE + g * 128, v[0].w, v[1].w, v[2].w, v[3].w);
                     }
                 }
+            }
+            if (tid < TTASK) {
+                unsigned char *dst = slab + tr * RB + (16 + (tu >> 3)) * CORE + (tu & 7) * 16;
+                put(dst, vt[0], vt[1], vt[2], vt[3]);
+                put(dst + 128, vt[4], vt[5], vt[6], vt[7]);
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -186,125 +245,139 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
     } else if (warp == MMA_WARP) {
         // ------------------------------------------------------------ MMA issue
         if (lane == 0) {
-            constexpr uint32_t IDESC = tc::idesc_tf32(128, N);
+            constexpr uint32_t IDESC_HH_HL = tc::idesc_tf32(128, 2 * N);
+            constexpr uint32_t IDESC_LH = tc::idesc_tf32(128, N);
             const uint32_t sB_addr = smem_u32(sB), sSlab_addr = smem_u32(sSlab);
-            int k = 0;
-            for (long long item = blockIdx.x; item < n_items && !*abort_flag; item += gridDim.x, ++k) {
-                const int stage = k & 1, use = k >> 1, buf = k & 1;
-                if (use > 0 && !mbar_wait_bounded(smem_u32(&bars.acc_empty[buf]), (use - 1) & 1)) {
-                    fail();
-                    break;
-                }
+            int k = 0, rowc = 0;
+            bool ok = true;
+            for (long long item = blockIdx.x; ok && item < n_items && !*abort_flag; item += gridDim.x, ++k) {
+                const int stage = k & 1, use = k >> 1;
                 if (!mbar_wait_bounded(smem_u32(&bars.slab_full[stage]), use & 1)) {
                     fail();
                     break;
                 }
                 tc::fence_after_sync();
-                // Base descriptors; every tap / K step / split only moves the start
+                // Base descriptors; every row / tap / split only moves the start
                 // address, i.e. adds (bytes >> 4) to the low field (no carry: shared
                 // addresses stay below 2^18).
-                const uint64_t a0 = tc::smem_desc(sSlab_addr + stage * C::SLAB, C::PLANE, 128);
-                const uint64_t b0 = tc::smem_desc(sB_addr, C::BPLANE, 128);
+                const uint64_t a0 = tc::smem_desc(sSlab_addr + stage * C::SLAB, 128, CORE);
+                const uint64_t b0 = tc::smem_desc(sB_addr, 128, CORE);
 #pragma unroll
-                for (int j = 0; j < P; ++j) {
-                    const uint32_t d = tmem + (uint32_t)(buf * ACC_STRIDE + j * N);
-                    uint32_t acc = 0;
+                for (int j = 0; j < P; ++j, ++rowc) {
+                    const int slot = rowc % NSLOT, sus = rowc / NSLOT;
+                    if (sus > 0 && !mbar_wait_bounded(smem_u32(&bars.slot_empty[slot]), (sus - 1) & 1)) {
+                        fail();
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after_sync();
+                    const uint32_t d = tmem + (uint32_t)(slot * SLOT_COLS);
 #pragma unroll
                     for (int tap = 0; tap < 9; ++tap) {
-                        const int off = ((j + tap / 3) * SW + tap % 3) * 16;
-#pragma unroll
-                        for (int s = 0; s < G / 2; ++s) {
-                            const uint64_t ah = a0 + (uint64_t)((2 * s * C::PLANE + off) >> 4);
-                            const uint64_t al = ah + (uint64_t)(C::SPLIT >> 4);
-                            const uint64_t bh = b0 + (uint64_t)(((tap * G + 2 * s) * C::BPLANE) >> 4);
-                            const uint64_t bl = bh + (uint64_t)((9 * G * C::BPLANE) >> 4);
-                            tc::mma_tf32(d, al, bh, IDESC, acc);
-                            tc::mma_tf32(d, ah, bl, IDESC, 1);
-                            tc::mma_tf32(d, ah, bh, IDESC, 1);
-                            acc = 1;
-                        }
+                        const uint64_t ah = a0 + (uint64_t)((((j + tap / 3) * RB) + (tap % 3) * CORE) >> 4);
+                        const uint64_t al = ah + (uint64_t)(C::SPLIT >> 4);
+                        const uint64_t bd = b0 + (uint64_t)((tap * C::BTAP) >> 4);
+                        tc::mma_tf32(d, ah, bd, IDESC_HH_HL, tap > 0 ? 1u : 0u);
+                        tc::mma_tf32(d, al, bd, IDESC_LH, 1u);
                     }
+                    tc::commit(smem_u32(&bars.slot_full[slot]));
                 }
                 tc::commit(smem_u32(&bars.slab_empty[stage]));
-                tc::commit(smem_u32(&bars.acc_full[buf]));
             }
         }
         __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue
-        // All 8 epilogue warps serve every item: warp w reads TMEM lane quarter w % 4
-        // and the 16-channel chunks c with c % 2 == (w - 4) / 4.
+        // Warp w: TMEM lane quarter q = w % 4, channels [h*NH, (h+1)*NH).  Lane l of
+        // quarter q is MMA row m = 32q + l = 8*i + r with i = 4q + l/8, r = l % 8:
+        // conv column i + 16r.  The P columns of a pooling window are lanes l ^ 8
+        // (and l ^ 16 for P = 4) of the same warp.
+        constexpr int NH = C::NH;
         const int q = warp & 3;
-        const int half = (warp - EPI_WARP0) >> 2;
-        int k = 0;
-        for (long long item = blockIdx.x; item < n_items && !*abort_flag; item += gridDim.x, ++k) {
-            const int buf = k & 1;
-            if (!mbar_wait_bounded(smem_u32(&bars.acc_full[buf]), (k >> 1) & 1)) {
+        const int h = (warp - EPI_WARP0) >> 2;
+        const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(h * NH);
+        int k = 0, rowc = 0;
+        bool ok = true;
+        for (long long item = blockIdx.x; ok && item < n_items && !*abort_flag; item += gridDim.x, ++k) {
+            float m[NH];
+#pragma unroll
+            for (int c = 0; c < NH; ++c) m[c] = use_min ? INFINITY : -INFINITY;
+#pragma unroll 1
+            for (int j = 0; j < P; ++j, ++rowc) {
+                const int slot = rowc % NSLOT, sus = rowc / NSLOT;
+                if (!mbar_wait_bounded(smem_u32(&bars.slot_full[slot]), sus & 1)) {
+                    fail();
+                    ok = false;
+                    break;
+                }
+                tc::fence_after_sync();
+                float a[NH], b[NH];
+                const uint32_t ts = tq + (uint32_t)(slot * SLOT_COLS);
+#pragma unroll
+                for (int c = 0; c < NH; c += 8) {
+                    tc::ld8(ts + c, a + c);      // x_hi*w_hi + x_lo*w_hi
+                    tc::ld8(ts + N + c, b + c);  // x_hi*w_lo
+                }
+                tc::wait_ld();
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&bars.slot_empty[slot]));
+#pragma unroll
+                for (int c = 0; c < NH; ++c) m[c] = upd(m[c], a[c] + b[c], use_min);
+            }
+            if (!ok) break;
+            // butterfly over the P lanes of a window: keep half the channels per step
+            const int b3 = (lane >> 3) & 1;
+            float hbuf[NH / 2];
+#pragma unroll
+            for (int i = 0; i < NH / 2; ++i) {
+                const float give = b3 ? m[i] : m[NH / 2 + i];
+                const float keep = b3 ? m[NH / 2 + i] : m[i];
+                hbuf[i] = upd(keep, __shfl_xor_sync(0xffffffffu, give, 8), use_min);
+            }
+            int cbase = h * NH + b3 * (NH / 2);
+            constexpr int NRES = P == 4 ? NH / 4 : NH / 2;
+            float res[NRES];
+            int pwl;
+            if constexpr (P == 4) {
+                const int b4 = (lane >> 4) & 1;
+#pragma unroll
+                for (int i = 0; i < NH / 4; ++i) {
+                    const float give = b4 ? hbuf[i] : hbuf[NH / 4 + i];
+                    const float keep = b4 ? hbuf[NH / 4 + i] : hbuf[i];
+                    res[i] = upd(keep, __shfl_xor_sync(0xffffffffu, give, 16), use_min);
+                }
+                cbase += b4 * (NH / 4);
+                pwl = q + 4 * (lane & 7);  // window base column 4q + 16r
+            } else {
+#pragma unroll
+                for (int i = 0; i < NH / 2; ++i) res[i] = hbuf[i];
+                pwl = 2 * q + ((lane >> 4) & 1) + 8 * (lane & 7);  // base column 4q + 2*(l/16) + 16r
+            }
+            float *stg = sStg + (k & 1) * C::STG;
+#pragma unroll
+            for (int i = 0; i < NRES; ++i) {
+                const int co = cbase + i;
+                const float tv = tanh_fast(res[i] + sCb[co]);
+                stg[co * C::PW + pwl] = __fadd_rn(__fmul_rn(tv, scale), sBias[co]);
+            }
+            // all eight warps have staged this item (the other buffer is still
+            // being read only by warps that have not reached this point)
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bars.stg_full[k & 1]));
+            if (!mbar_wait_bounded(smem_u32(&bars.stg_full[k & 1]), (k >> 1) & 1)) {
                 fail();
                 break;
             }
-            tc::fence_after_sync();
             const int cblk = (int)(item % ncb);
             const long long t = item / ncb;
             const int pr = (int)(t % Ho);
             const long long n = t / Ho;
-            const int col = cblk * MT + 32 * q + lane;
-            const int pw = col / P;
-            const bool valid = pw < Wo;
-            const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * ACC_STRIDE);
-#pragma unroll
-            for (int c0 = 16 * half; c0 < N; c0 += 32) {
-                float v[P][16];
-#pragma unroll
-                for (int j = 0; j < P; ++j) tc::ld16(taddr + j * N + c0, v[j]);
-                tc::wait_ld();
-                float m[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    m[i] = v[0][i];
-#pragma unroll
-                    for (int j = 1; j < P; ++j) m[i] = upd(m[i], v[j][i], use_min);
-                }
-                // butterfly over the P lanes of a window: keep half the channels per step
-                const int b0 = lane & 1;
-                float h[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float give = b0 ? m[i] : m[8 + i];
-                    const float keep = b0 ? m[8 + i] : m[i];
-                    h[i] = upd(keep, __shfl_xor_sync(0xffffffffu, give, 1), use_min);
-                }
-                int cbase = c0 + 8 * b0;
-                float res[8];
-                int nres = 8;
-                if (P == 4) {
-                    const int b1 = (lane >> 1) & 1;
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const float give = b1 ? h[i] : h[4 + i];
-                        const float keep = b1 ? h[4 + i] : h[i];
-                        res[i] = upd(keep, __shfl_xor_sync(0xffffffffu, give, 2), use_min);
-                    }
-                    cbase += 4 * b1;
-                    nres = 4;
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) res[i] = h[i];
-                }
-                if (valid) {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        if (i < nres) {
-                            const int co = cbase + i;
-                            const float tv = tanh_fast(res[i] + sCb[co]);
-                            out[((n * N + co) * Ho + pr) * (long long)Wo + pw] = __fadd_rn(__fmul_rn(tv, scale), sBias[co]);
-                        }
-                    }
-                }
+            const int pw0 = cblk * C::PW;
+            for (int e = tid - EPI_WARP0 * 32; e < C::STG; e += NEPI * 32) {
+                const int co = e / C::PW, pw = e - co * C::PW;
+                if (pw0 + pw < Wo) out[((n * N + co) * Ho + pr) * (long long)Wo + pw0 + pw] = stg[e];
             }
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&bars.acc_empty[buf]));
         }
     }
 
@@ -312,16 +385,16 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
     __syncthreads();
     if (warp == MMA_WARP) {
         tc::fence_after_sync();
-        tc::dealloc(tmem, 512);
+        tc::dealloc(tmem, NSLOT * SLOT_COLS);
     }
 }
 
 template <int P, int N>
 fw_status launch_pn(const float *x, int Nimg, int H, int W, const float *w, const float *cb, const float *bias,
                     float scale, float *out, int Ho, int Wo, cudaStream_t st) {
-    using C = Cfg<2, P, N>;
+    using C = Cfg<P, N>;
     size_t smem = C::SMEM < 116 * 1024 ? 116 * 1024 : C::SMEM;  // one CTA per SM
-    cudaError_t e = cudaFuncSetAttribute(convpool_tc_kernel<2, P, N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(convpool_tc_kernel<P, N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return launch_status(e);
     int dev = 0, sms = 0;
@@ -331,7 +404,8 @@ fw_status launch_pn(const float *x, int Nimg, int H, int W, const float *w, cons
     const int ncb = (Wo * P + MT - 1) / MT;
     const long long items = (long long)Nimg * Ho * ncb;
     const int grid = (int)(items < sms ? items : sms);
-    convpool_tc_kernel<2, P, N><<<grid, NTHREADS, smem, st>>>(x, w, cb, bias, scale, out, Nimg, H, W, Ho, Wo, ncb);
+    const bool vec = W % 4 == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0;  // float4 input rows
+    convpool_tc_kernel<P, N><<<grid, NTHREADS, smem, st>>>(x, w, cb, bias, scale, out, Nimg, H, W, Ho, Wo, ncb, vec);
     note_launch();
     return launch_status(cudaGetLastError());
 }

@@ -109,6 +109,25 @@ def test_errors_raise():
         FW.fw_conv2d_tanh_scale_bias_maxpool(x[:, :, :4, :4].contiguous(), w, None, b, 2.0, 4)
 
 
+@pytest.mark.parametrize("N,H,W,Cout,pk", [(1, 36, 68, 32, 4), (2, 20, 132, 48, 2), (1, 30, 260, 48, 4)])
+def test_tensor_kernel_cout_32_48(N, H, W, Cout, pk):
+    """Cout 32 and 48 on the tensor-core kernel, W % 4 == 0 (float4 input rows), several column blocks."""
+    d = synth.convpool_inputs(N, 8, H, W, Cout, seed=W)
+    assert_close(run_gpu(d, 2.0, pk), run_oracle(d, 2.0, pk), TOL_FFMA, str((N, H, W, Cout, pk)))
+
+
+def test_input_rows_not_16_byte_aligned():
+    """x 4-byte aligned but not 16-byte aligned with W % 4 == 0: the tensor-core kernel
+    must take its scalar-load path and give the same result."""
+    d = synth.convpool_inputs(2, 8, 40, 64, 64, seed=11)
+    flat = torch.zeros(d["x"].size + 1, dtype=torch.float32, device="cuda")
+    x = flat[1:].view(d["x"].shape)
+    x.copy_(torch.from_numpy(d["x"]))
+    assert x.data_ptr() % 16 == 4
+    got = host(FW.fw_conv2d_tanh_scale_bias_maxpool(x, dev(d["w"]), dev(d["conv_b"]), dev(d["bias"]), -1.5, 4))
+    assert_close(got, run_oracle(d, -1.5, 4), TOL_FFMA, "unaligned rows")
+
+
 def test_ffma_kernel_when_forced():
     """The FP32-FMA tiled kernel (selected with FUSEDWIN_CONVPOOL_FFMA=1) on shapes the
     tensor-core kernel takes, in a fresh process."""
