@@ -26,9 +26,9 @@
 //     apart, M-adjacent ones 256 B apart) that the tensor cores read at full rate.
 //     Columns 16..17 + 16k appear twice (as rows 0/1 of core 16/17 too);
 //   * the weights, split into hi/lo in the CTA prologue, stay resident.
-// CTA roles (416 threads, one CTA per SM, persistent over items):
-//   warps 0-3   producers: load and split a slab (two stages);
-//   warp  12    allocates TMEM; one lane issues 2 x 9 MMAs per conv row;
+// CTA roles (512 threads, one CTA per SM, persistent over items):
+//   warps 1-3, 13-15  producers: load and split a slab (two stages);
+//   warp  0     allocates TMEM; one lane issues 2 x 9 MMAs per conv row;
 //   warps 4-11  epilogue, every warp on every conv row: warp w reads TMEM lane
 //               quarter w % 4 and half the channels; the max over the P rows of a
 //               window is kept in registers while the rows arrive, the max over
@@ -51,10 +51,19 @@ constexpr int CORE = 256;        // bytes of one core index: 2 planes x 8 rows x
 constexpr int RB = NCORE * CORE;   // bytes of one staged input row (per split)
 constexpr int SLOTS_ROW = NCORE * 8;  // staged positions per input row
 constexpr int NSTAGE = 2;
+// Warp roles.  A warp runs on SM sub-partition warp % 4 and reads TMEM lane quarter
+// warp % 4, so every sub-partition hosts epilogue warps; the MMA issuer (warp 0)
+// shares sub-partition 0 only with the two quarter-0 epilogue warps: busy warps on
+// the issuer's sub-partition slow MMA issue (measured: 2.3x with two FMA-bound
+// warps there, none with the same warps on the other three).
+constexpr int MMA_WARP = 0;
 constexpr int EPI_WARP0 = 4;     // warps 4-11: epilogue
 constexpr int NEPI = 8;
-constexpr int MMA_WARP = 12;
-constexpr int NTHREADS = (MMA_WARP + 1) * 32;
+constexpr int NPROD = 6;         // warps 1-3 and 13-15: producers (warp 12 idles)
+constexpr int NTHREADS = 16 * 32;
+__device__ __forceinline__ int producer_index(int warp) {  // 0..5, or -1
+    return (warp >= 1 && warp <= 3) ? warp - 1 : (warp >= 13 ? warp - 10 : -1);
+}
 constexpr int NSLOT = 4;         // TMEM accumulator ring, one conv row per slot
 constexpr int SLOT_COLS = 128;
 constexpr float LOG2E = 1.4426950408889634f;
@@ -131,7 +140,7 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
     }
     if (tid == 0) {
         for (int s = 0; s < NSTAGE; ++s) {
-            mbar_init(smem_u32(&bars.slab_full[s]), 4);
+            mbar_init(smem_u32(&bars.slab_full[s]), NPROD);
             mbar_init(smem_u32(&bars.slab_empty[s]), 1);
         }
         for (int b = 0; b < NSLOT; ++b) {
@@ -154,7 +163,7 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
         atomicOr(&g_err_convpool_tc, DEVERR_TIMEOUT);
     };
 
-    if (warp < 4) {
+    if (producer_index(warp) >= 0) {
         // ------------------------------------------------------------ producers
         // Main task (row rr, group a, r): the 4 input columns 4a + 16r .. +3 of the
         // block, i.e. row r of cores 4a .. 4a+3.  Lane r + 8a of a warp, so a warp's
@@ -163,7 +172,9 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
         // groups per 8 lanes.  Tail task (row rr, r, t): row r of core 16 + t,
         // input column 16 + t + 16r (a second copy of a main-task column, or
         // column 128 / 129 for r = 7).
-        constexpr int MTASK = C::ROWS * 32, MITER = (MTASK + 127) / 128, TTASK = C::ROWS * 16;
+        constexpr int NPT = NPROD * 32;  // producer threads
+        constexpr int MTASK = C::ROWS * 32, MITER = (MTASK + NPT - 1) / NPT, TTASK = C::ROWS * 16;
+        const int ptid = producer_index(warp) * 32 + lane;
         const long long plane_stride = (long long)H * W;
         int k = 0;
         for (long long item = blockIdx.x; item < n_items && !*abort_flag; item += gridDim.x, ++k) {
@@ -177,7 +188,7 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
             float4 vm[MITER][CIN];
 #pragma unroll
             for (int it = 0; it < MITER; ++it) {
-                const int mt = tid + 128 * it;
+                const int mt = ptid + NPT * it;
                 const int rr = mt >> 5, a = (mt >> 3) & 3, r = mt & 7;
                 const int row = row0 + rr, col = col0 + 4 * a + 16 * r;
                 const float *src = xn + (long long)row * W + col;
@@ -200,10 +211,10 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
                 }
             }
             float vt[CIN];
-            const int tr = tid >> 4, tu = tid & 15;  // tail task of this thread (tid < TTASK)
+            const int tr = ptid >> 4, tu = ptid & 15;  // tail task of this thread (ptid < TTASK)
             {
                 const int row = row0 + tr, col = col0 + 16 + (tu >> 3) + 16 * (tu & 7);
-                const bool ok = tid < TTASK && row < H && col < W;
+                const bool ok = ptid < TTASK && row < H && col < W;
                 const float *src = xn + (long long)row * W + col;
 #pragma unroll
                 for (int ci = 0; ci < CIN; ++ci) vt[ci] = ok ? __ldg(src + ci * plane_stride) : 0.f;
@@ -219,7 +230,7 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
             };
 #pragma unroll
             for (int it = 0; it < MITER; ++it) {
-                const int mt = tid + 128 * it;
+                const int mt = ptid + NPT * it;
                 if (mt < MTASK) {
                     const int rr = mt >> 5, a = (mt >> 3) & 3, r = mt & 7;
                     unsigned char *dst = slab + rr * RB + 4 * a * CORE + r * 16;
@@ -233,7 +244,7 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
                     }
                 }
             }
-            if (tid < TTASK) {
+            if (ptid < TTASK) {
                 unsigned char *dst = slab + tr * RB + (16 + (tu >> 3)) * CORE + (tu & 7) * 16;
                 put(dst, vt[0], vt[1], vt[2], vt[3]);
                 put(dst + 128, vt[4], vt[5], vt[6], vt[7]);
@@ -286,7 +297,7 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
             }
         }
         __syncwarp();
-    } else {
+    } else if (warp >= EPI_WARP0 && warp < EPI_WARP0 + NEPI) {
         // ------------------------------------------------------------ epilogue
         // Warp w: TMEM lane quarter q = w % 4, channels [h*NH, (h+1)*NH).  Lane l of
         // quarter q is MMA row m = 32q + l = 8*i + r with i = 4q + l/8, r = l % 8:
