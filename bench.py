@@ -404,6 +404,53 @@ def run_gpu(args):
             b.synchronize()
             ts.append(a.elapsed_time(b))
         e2e_local.append(statistics.mean(ts))
+    # What fusion saves: the same operators the pages' unfused way (conv output to memory,
+    # then a second kernel), built from this library's kernels; outside the timed step.
+    fusion = None
+    if not args.no_fusion_compare and (cp or ct):
+        fusion = {}
+
+        def med_ms(fn, reps=7):
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            ts = []
+            for _ in range(reps):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                b.record(stream)
+                b.synchronize()
+                ts.append(a.elapsed_time(b))
+            return statistics.median(ts)
+
+        if cp:
+            n = cp["x"].shape[0]
+            wsz = FW.fw_conv2d_pool_unfused_workspace_size(n, CP["H"], CP["W"], CP["Cout"], 3, 3, 4)
+            wsp_cp = torch.empty(wsz // 4, device=dev)
+            f_ms = med_ms(lambda: op_cp(d, out_cp))
+            u_ms = med_ms(lambda: FW.fw_conv2d_tanh_scale_bias_maxpool_unfused(
+                d[("cp", "x")], d[("cp", "w")], d[("cp", "conv_b")], d[("cp", "bias")], CP["scale"], 4,
+                out=out_cp, workspace=wsp_cp))
+            fusion["convpool"] = {"fused_ms": f_ms, "unfused_ms": u_ms, "unfused_over_fused": u_ms / f_ms,
+                                  "intermediate_bytes": wsz,
+                                  "unfused": "convpool_tc_kernel raw mode (conv + conv_b to memory) + "
+                                             "pool_tanh_scale_bias_kernel"}
+            del wsp_cp
+        if ct:
+            n = ct["x"].shape[0]
+            wsz = FW.fw_convt_unfused_workspace_size(n, CT["Cin"], CT["H"], CT["W"], CT["Cout"], 4, 2, 1, 1)
+            wsp_ct = torch.empty(wsz // 4, device=dev)
+            f_ms = med_ms(lambda: op_ct(d, out_ct))
+            u_ms = med_ms(lambda: FW.fw_convtranspose2d_softmax_bias_scale_sigmoid_unfused(
+                d[("ct", "x")], d[("ct", "w")], d[("ct", "conv_b")], d[("ct", "bias")], CT["scale"],
+                out=out_ct, workspace=wsp_ct))
+            fusion["convt"] = {"fused_ms": f_ms, "unfused_ms": u_ms, "unfused_over_fused": u_ms / f_ms,
+                               "intermediate_bytes": 4 * n * CT["Cout"] * 129 * 129,
+                               "unfused": "convt_k4s2_tc_kernel raw mode (conv-transpose + conv_b to memory) + "
+                                          "softmax_bias_scale_sigmoid_kernel (online max/sum pass, output pass)"}
+            del wsp_ct
+        FW.fw_check_device_errors()
     red = reduce_max(local_ms + e2e_local, ws, device=dev if args.backend == "nccl" else None)
     total_ms, op_ms, e2e_ms = red[0], red[1:1 + len(specs)], red[1 + len(specs):]
     h2d = sum(t.numel() * t.element_size() for t in pinned.values())
@@ -465,6 +512,8 @@ def run_gpu(args):
         "gpu_launches": launches, "launches_per_step": launches / args.steps,
         "clocks": clk.summary(), "device": props.name,
     })
+    if fusion:
+        line["fusion"] = fusion
     if args.only or args.batch:
         line["config"]["subset"] = {"only": args.only, "batch": args.batch}
     print(json.dumps(line), flush=True)
@@ -486,6 +535,8 @@ def main(argv=None):
     ap.add_argument("--only", default=None, choices=["convpool", "maxpool", "convt"],
                     help="time one operator only (profiling)")
     ap.add_argument("--batch", type=int, default=0, help="smaller batch for every workload (profiling)")
+    ap.add_argument("--no-fusion-compare", action="store_true",
+                    help="skip timing the unfused (conv output to memory) comparison path")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl != "reference":
         args.warmup = 3

@@ -181,6 +181,52 @@ fw_status fw_convtranspose2d_softmax_bias_scale_sigmoid_noalloc(const float *x, 
                                                                 const float *bias, float scale, float *out,
                                                                 void *stream);
 
+/* ------------------------------------------------------ unfused comparison */
+
+/*
+ * The pages' own design, unfused, built from this library's kernels so that what
+ * fusion saves can be measured (trace "Kimi-K2.6 l2_p82": a library convolution
+ * writes the whole conv output, then one kernel per pooled output takes the window
+ * max and applies tanh, scale and bias; trace "Kimi-K2.6 l2_p91": a library
+ * conv-transpose writes its output, then one thread per pixel makes an online
+ * pass over the channels for the softmax max and sum and a second pass for the
+ * output).  Same arguments, result and tolerance as the fused calls, plus a
+ * caller-owned workspace for the intermediate:
+ *
+ *   conv+pool: y [N, Cout, pool_k*Ho, pool_k*Wo] = conv(x) + conv_b (the conv
+ *              outputs the floor-mode pool reads), then out from y.  The result is
+ *              bit-identical to fw_conv2d_tanh_scale_bias_maxpool: rounding
+ *              y = a + conv_b is monotone in a, so the window maximum of y is the
+ *              rounded sum of the window maximum of a and conv_b.
+ *   convT:     [rewritten weights | y [N, Cout, Ho, Wo]], then out from y.
+ *
+ * workspace: at least fw_conv2d_pool_unfused_workspace_size(...) /
+ *            fw_convt_unfused_workspace_size(...) bytes, 16-byte aligned, not
+ *            overlapping any argument; contents undefined afterwards.
+ * Only the shapes the tensor-core kernels take are supported (conv+pool: Cin = 8,
+ * 3x3, pool_s = pool_k in {2, 4}, Cout in {16, 32, 48, 64}; convT: k = 4, s = 2,
+ * p = 1, Cout = 128, Cin in {8, 16, 32, 64}); other valid arguments return
+ * FW_ERR_UNSUPPORTED before any launch.  Two kernels per call (three for convT,
+ * counting the weight rewrite).
+ */
+fw_status fw_conv2d_tanh_scale_bias_maxpool_unfused(const float *x, int N, int Cin, int H, int W,
+                                                    const float *w, const float *conv_b, int Cout,
+                                                    int KH, int KW, float scale, const float *bias,
+                                                    int pool_k, int pool_s, float *out, void *workspace,
+                                                    unsigned long long workspace_bytes, void *stream);
+unsigned long long fw_conv2d_pool_unfused_workspace_size(int N, int H, int W, int Cout, int KH, int KW,
+                                                         int pool_k, int pool_s);
+
+fw_status fw_convtranspose2d_softmax_bias_scale_sigmoid_unfused(const float *x, int N, int Cin, int H, int W,
+                                                                const float *w, const float *conv_b,
+                                                                int Cout, int k, int s, int p, int op,
+                                                                const float *bias, float scale, float *out,
+                                                                void *workspace,
+                                                                unsigned long long workspace_bytes,
+                                                                void *stream);
+unsigned long long fw_convt_unfused_workspace_size(int N, int Cin, int H, int W, int Cout, int k, int s, int p,
+                                                   int op);
+
 /* ------------------------------------------------------------- diagnostics */
 
 /*

@@ -49,7 +49,6 @@ constexpr int MT = 128;          // conv columns per item (MMA M)
 constexpr int NCORE = MT / 8 + 2;  // core matrices per staged input row
 constexpr int CORE = 256;        // bytes of one core index: 2 planes x 8 rows x 16 B
 constexpr int RB = NCORE * CORE;   // bytes of one staged input row (per split)
-constexpr int SLOTS_ROW = NCORE * 8;  // staged positions per input row
 constexpr int NSTAGE = 2;
 // Warp roles.  A warp runs on SM sub-partition warp % 4 and reads TMEM lane quarter
 // warp % 4, so every sub-partition hosts epilogue warps; the MMA issuer (warp 0)
@@ -74,11 +73,12 @@ struct Bars {
     uint64_t slot_full[NSLOT];
     uint64_t slot_empty[NSLOT];
     uint64_t stg_full[2];
+    uint64_t raw_full[2];  // raw mode: a conv row staged by all epilogue warps
     uint32_t tmem_base;
     int abort;
 };
 
-template <int P, int N>
+template <int P, int N, bool RAW>
 struct Cfg {
     static constexpr int ROWS = P + 2;
     static constexpr int SPLIT = ROWS * RB;           // hi (or lo) half of a slab
@@ -86,7 +86,8 @@ struct Cfg {
     static constexpr int BTAP = (2 * N / 8) * CORE;   // one tap of [w_hi | w_lo]
     static constexpr int B_BYTES = 9 * BTAP;
     static constexpr int PW = MT / P;                 // pooled columns per item
-    static constexpr int STG = N * PW;                // floats of one staging buffer
+    // floats of one staging buffer: a pooled row, or (raw mode) one conv row of the block
+    static constexpr int STG = RAW ? N * MT : N * PW;
     static constexpr int NH = N / 2;                  // channels per epilogue warp
     static constexpr size_t SMEM =
         (size_t)B_BYTES + NSTAGE * SLAB + 2 * STG * 4 + 2 * N * 4 + sizeof(Bars);
@@ -105,12 +106,15 @@ __device__ __forceinline__ float tanh_fast(float z) {
     return 1.f - __fdividef(2.f, 1.f + e);
 }
 
-template <int P, int N>
+// RAW = false: the fused operator.  RAW = true: the first kernel of the unfused
+// comparison path -- `out` receives y = conv(x) + conv_b for the P*Ho x P*Wo conv
+// outputs the pool reads ([Nimg, N, P*Ho, P*Wo]); scale and bias are unused.
+template <int P, int N, bool RAW>
 __global__ void __launch_bounds__(NTHREADS, 1)
 convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, const float *__restrict__ cb,
                    const float *__restrict__ bias, float scale, float *__restrict__ out, int Nimg, int H, int W,
                    int Ho, int Wo, int ncb, bool vec) {
-    using C = Cfg<P, N>;
+    using C = Cfg<P, N, RAW>;
     constexpr int CIN = 8;
     extern __shared__ __align__(1024) unsigned char smem[];
     unsigned char *sB = smem;
@@ -126,7 +130,7 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
 
     for (int i = tid; i < N; i += NTHREADS) {
         sCb[i] = cb ? __ldg(cb + i) : 0.f;
-        sBias[i] = __ldg(bias + i);
+        sBias[i] = bias ? __ldg(bias + i) : 0.f;  // raw mode passes no bias
     }
     // Weights split into TF32 hi/lo: B[tap][co' / 8][plane][co' % 8][c4] with
     // co' = co for w_hi and N + co for w_lo.
@@ -147,7 +151,10 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
             mbar_init(smem_u32(&bars.slot_full[b]), 1);
             mbar_init(smem_u32(&bars.slot_empty[b]), NEPI);
         }
-        for (int b = 0; b < 2; ++b) mbar_init(smem_u32(&bars.stg_full[b]), NEPI);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&bars.stg_full[b]), NEPI);
+            mbar_init(smem_u32(&bars.raw_full[b]), NEPI);
+        }
         bars.abort = 0;
         fence_mbar_init();
     }
@@ -333,10 +340,39 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
                 tc::fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&bars.slot_empty[slot]));
+                if constexpr (RAW) {
+                    // Stage the row as [channel][position]; conv column i + 16r sits at
+                    // 8i + (r ^ 2(i/4)), so both the writes here and the column-order
+                    // reads below hit 32 distinct banks.
+                    float *rs = sStg + (rowc & 1) * C::STG;
+                    const int i = 4 * q + (lane >> 3), r = lane & 7;
+                    const int pos = 8 * i + (r ^ (2 * (i >> 2)));
 #pragma unroll
-                for (int c = 0; c < NH; ++c) m[c] = upd(m[c], a[c] + b[c], use_min);
+                    for (int c = 0; c < NH; ++c) rs[(h * NH + c) * MT + pos] = (a[c] + b[c]) + sCb[h * NH + c];
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&bars.raw_full[rowc & 1]));
+                    if (!mbar_wait_bounded(smem_u32(&bars.raw_full[rowc & 1]), (rowc >> 1) & 1)) {
+                        fail();
+                        ok = false;
+                        break;
+                    }
+                    const int cblk = (int)(item % ncb);
+                    const long long t = item / ncb;
+                    const int HI = P * Ho, WI = P * Wo;
+                    const int row = (int)(t % Ho) * P + j, col0 = cblk * MT;
+                    float *yrow = out + (t / Ho) * (long long)N * HI * WI + (long long)row * WI + col0;
+                    for (int e = tid - EPI_WARP0 * 32; e < N * MT; e += NEPI * 32) {
+                        const int co = e / MT, cc = e - co * MT;
+                        const int ci = cc & 15, cr = cc >> 4;
+                        if (col0 + cc < WI) yrow[(long long)co * HI * WI + cc] = rs[co * MT + 8 * ci + (cr ^ (2 * (ci >> 2)))];
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < NH; ++c) m[c] = upd(m[c], a[c] + b[c], use_min);
+                }
             }
             if (!ok) break;
+            if constexpr (RAW) continue;
             // butterfly over the P lanes of a window: keep half the channels per step
             const int b3 = (lane >> 3) & 1;
             float hbuf[NH / 2];
@@ -400,12 +436,12 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
     }
 }
 
-template <int P, int N>
+template <int P, int N, bool RAW>
 fw_status launch_pn(const float *x, int Nimg, int H, int W, const float *w, const float *cb, const float *bias,
                     float scale, float *out, int Ho, int Wo, cudaStream_t st) {
-    using C = Cfg<P, N>;
+    using C = Cfg<P, N, RAW>;
     size_t smem = C::SMEM < 116 * 1024 ? 116 * 1024 : C::SMEM;  // one CTA per SM
-    cudaError_t e = cudaFuncSetAttribute(convpool_tc_kernel<P, N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(convpool_tc_kernel<P, N, RAW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return launch_status(e);
     int dev = 0, sms = 0;
@@ -416,7 +452,8 @@ fw_status launch_pn(const float *x, int Nimg, int H, int W, const float *w, cons
     const long long items = (long long)Nimg * Ho * ncb;
     const int grid = (int)(items < sms ? items : sms);
     const bool vec = W % 4 == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0;  // float4 input rows
-    convpool_tc_kernel<P, N><<<grid, NTHREADS, smem, st>>>(x, w, cb, bias, scale, out, Nimg, H, W, Ho, Wo, ncb, vec);
+    convpool_tc_kernel<P, N, RAW><<<grid, NTHREADS, smem, st>>>(x, w, cb, bias, scale, out, Nimg, H, W, Ho, Wo, ncb,
+                                                                vec);
     note_launch();
     return launch_status(cudaGetLastError());
 }
@@ -431,11 +468,79 @@ bool convpool_tc_eligible(int Cin, int Cout, int KH, int KW, int pk, int ps) {
 fw_status convpool_tc_launch(const float *x, int N, int H, int W, const float *w, const float *cb, int Cout,
                              float scale, const float *bias, int pk, float *out, int Ho, int Wo, cudaStream_t st) {
 #define FW_CP_CASE(PP, NN) \
-    if (pk == PP && Cout == NN) return launch_pn<PP, NN>(x, N, H, W, w, cb, bias, scale, out, Ho, Wo, st);
+    if (pk == PP && Cout == NN) return launch_pn<PP, NN, false>(x, N, H, W, w, cb, bias, scale, out, Ho, Wo, st);
     FW_CP_CASE(4, 64) FW_CP_CASE(4, 48) FW_CP_CASE(4, 32) FW_CP_CASE(4, 16)
     FW_CP_CASE(2, 64) FW_CP_CASE(2, 48) FW_CP_CASE(2, 32) FW_CP_CASE(2, 16)
 #undef FW_CP_CASE
     return FW_ERR_UNSUPPORTED;
+}
+
+// ---------------------------------------------------------------- unfused path
+// The pages' own (unfused) design, built from this library's kernels for comparison:
+// the convolution writes its output to memory, then a second kernel pools it and
+// applies tanh, scale and bias.
+
+namespace {
+
+// One thread per pooled output: max (min for scale < 0) over the P x P window of
+// y = conv + conv_b, then bias + scale * tanh(m), rounded as in the fused kernel.
+template <int P>
+__global__ void __launch_bounds__(256) pool_tanh_scale_bias_kernel(const float *__restrict__ y,
+                                                                   const float *__restrict__ bias, float scale,
+                                                                   float *__restrict__ out, long long total, int C,
+                                                                   int Ho, int Wo) {
+    const bool use_min = scale < 0.f;
+    const int WI = P * Wo;
+    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const int pw = (int)(idx % Wo);
+        const long long t = idx / Wo;
+        const int pr = (int)(t % Ho);
+        const long long nc = t / Ho;
+        const float *base = y + (nc * (long long)(P * Ho) + (long long)pr * P) * WI + (long long)pw * P;
+        float m = use_min ? INFINITY : -INFINITY;
+#pragma unroll
+        for (int r = 0; r < P; ++r) {
+            if constexpr (P == 4) {
+                const float4 v = __ldg(reinterpret_cast<const float4 *>(base + (long long)r * WI));
+                m = upd(upd(upd(upd(m, v.x, use_min), v.y, use_min), v.z, use_min), v.w, use_min);
+            } else {
+                const float2 v = __ldg(reinterpret_cast<const float2 *>(base + (long long)r * WI));
+                m = upd(upd(m, v.x, use_min), v.y, use_min);
+            }
+        }
+        const int co = (int)(nc % C);
+        out[idx] = __fadd_rn(__fmul_rn(tanh_fast(m), scale), __ldg(bias + co));
+    }
+}
+
+}  // namespace
+
+// Stage 1 of the unfused path: y [N, Cout, pk*Ho, pk*Wo] = conv(x) + conv_b.
+fw_status convpool_tc_launch_raw(const float *x, int N, int H, int W, const float *w, const float *cb, int Cout,
+                                 int pk, float *y, int Ho, int Wo, cudaStream_t st) {
+#define FW_CP_CASE(PP, NN) \
+    if (pk == PP && Cout == NN) return launch_pn<PP, NN, true>(x, N, H, W, w, cb, nullptr, 0.f, y, Ho, Wo, st);
+    FW_CP_CASE(4, 64) FW_CP_CASE(4, 48) FW_CP_CASE(4, 32) FW_CP_CASE(4, 16)
+    FW_CP_CASE(2, 64) FW_CP_CASE(2, 48) FW_CP_CASE(2, 32) FW_CP_CASE(2, 16)
+#undef FW_CP_CASE
+    return FW_ERR_UNSUPPORTED;
+}
+
+// Stage 2 of the unfused path (y 16-byte aligned for pk = 4, 8-byte for pk = 2).
+fw_status pool_tanh_scale_bias_launch(const float *y, int N, int Cout, const float *bias, float scale, int pk,
+                                      float *out, int Ho, int Wo, cudaStream_t st) {
+    const long long total = (long long)N * Cout * Ho * Wo;
+    const long long want = (total + 255) / 256;
+    const unsigned blocks = (unsigned)(want < 152LL * 64 ? want : 152LL * 64);
+    if (pk == 4)
+        pool_tanh_scale_bias_kernel<4><<<blocks, 256, 0, st>>>(y, bias, scale, out, total, Cout, Ho, Wo);
+    else if (pk == 2)
+        pool_tanh_scale_bias_kernel<2><<<blocks, 256, 0, st>>>(y, bias, scale, out, total, Cout, Ho, Wo);
+    else
+        return FW_ERR_UNSUPPORTED;
+    note_launch();
+    return launch_status(cudaGetLastError());
 }
 
 unsigned convpool_tc_read_and_clear_error() {

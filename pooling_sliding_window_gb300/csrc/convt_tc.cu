@@ -59,6 +59,7 @@ constexpr int NACC = 3;            // TMEM accumulators (128 columns each), one 
 constexpr int MMA_WARP = EPI_WARP0 + 4 * NACC;
 constexpr int NTHREADS = (MMA_WARP + 1) * 32;
 constexpr float LOG2E = 1.4426950408889634f;
+constexpr float LN2 = 0.6931471805599453f;
 constexpr uint32_t IDESC = tc::idesc_tf32(128, COUT);
 constexpr size_t MIN_SMEM = 116 * 1024;  // > half an SM: one CTA per SM
 constexpr size_t SMEM_LIMIT = 232448;    // 227 KB of dynamic shared memory per CTA
@@ -112,7 +113,10 @@ __device__ __forceinline__ float ex2_approx(float x) {
 // A slab holds the positions one tile reads for the vertical taps it covers:
 // nslab == 1 -> both vertical taps (L = 129 + (W+1) positions), nslab == 2 ->
 // one vertical tap per slab (L = 129).
-template <int G>  // input channels / 4
+// RAW = false: the fused operator.  RAW = true: the first kernel of the unfused
+// comparison path -- `out` receives the conv-transpose output y (+ conv_b) for every
+// output pixel and channel; scale and bias are unused.
+template <int G, bool RAW>  // G = input channels / 4
 __global__ void __launch_bounds__(NTHREADS, 1)
 convt_k4s2_tc_kernel(const float *__restrict__ x, const float *__restrict__ wtc, const float *__restrict__ cb,
                      const float *__restrict__ bias, float scale, float *__restrict__ out, int N, int H, int W,
@@ -140,7 +144,7 @@ convt_k4s2_tc_kernel(const float *__restrict__ x, const float *__restrict__ wtc,
 
     for (int i = tid; i < COUT; i += NTHREADS) {
         sCb[i] = cb ? __ldg(cb + i) * LOG2E : 0.f;
-        sKb[i] = -__ldg(bias + i) * scale * LOG2E;
+        sKb[i] = bias ? -__ldg(bias + i) * scale * LOG2E : 0.f;
     }
     if (tid == 0) {
         mbar_init(smem_u32(&bars.b_full), 1);
@@ -315,6 +319,31 @@ convt_k4s2_tc_kernel(const float *__restrict__ x, const float *__restrict__ wtc,
                 break;
             }
             tc::fence_after_sync();
+            const long long a = (long long)tile * MT + 32 * q + lane;
+            const long long n = a / img_anchors;
+            const int rem = (int)(a - n * img_anchors);
+            const int m = rem / BW, nn = rem - m * BW;
+            const int oh = 2 * m + py, ow = 2 * nn + px;
+            const bool valid = a < n_anchor && oh < Ho && ow < Wo;
+            float *o = out + (n * COUT) * plane_out + (long long)oh * Wo + ow;
+            if constexpr (RAW) {
+                // y = z * ln(2): the accumulator holds (conv-transpose + conv_b) * log2(e)
+#pragma unroll 2
+                for (int c = 0; c < COUT / 32; ++c) {
+                    tc::ld32(taddr + 32 * c, v);
+                    tc::wait_ld();
+                    if (valid) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[(32 * c + i) * plane_out] = v[i] * LN2;
+                    }
+                    reset_chunk(c);
+                }
+                tc::wait_st();
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&bars.acc_empty[eg]));
+                continue;
+            }
             // The chunk loops are unrolled only twice: fully unrolled, the three
             // passes no longer fit the instruction caches next to the producer and
             // MMA code (measured 12 % slower).
@@ -343,13 +372,6 @@ convt_k4s2_tc_kernel(const float *__restrict__ x, const float *__restrict__ wtc,
             tc::wait_st();
             // softmax p = e / sum; out = 1 / (1 + 2^(-(p + bias) * scale * log2(e)))
             const float kp = ks / sum;
-            const long long a = (long long)tile * MT + 32 * q + lane;
-            const long long n = a / img_anchors;
-            const int rem = (int)(a - n * img_anchors);
-            const int m = rem / BW, nn = rem - m * BW;
-            const int oh = 2 * m + py, ow = 2 * nn + px;
-            const bool valid = a < n_anchor && oh < Ho && ow < Wo;
-            float *o = out + (n * COUT) * plane_out + (long long)oh * Wo + ow;
 #pragma unroll 2
             for (int c = 0; c < COUT / 32; ++c) {
                 tc::ld32(taddr + 32 * c, v);
@@ -382,7 +404,7 @@ convt_k4s2_tc_kernel(const float *__restrict__ x, const float *__restrict__ wtc,
     }
 }
 
-template <int G>
+template <int G, bool RAW>
 fw_status launch_g(const float *x, int N, int H, int W, const float *wtc, const float *cb, const float *bias,
                    float scale, float *out, int Ho, int Wo, cudaStream_t st) {
     int dev = 0, sms = 0, optin = 0;
@@ -400,13 +422,13 @@ fw_status launch_g(const float *x, int N, int H, int W, const float *wtc, const 
     }
     if (smem > limit) return FW_ERR_UNSUPPORTED;
     if (smem < MIN_SMEM) smem = MIN_SMEM;
-    cudaError_t e = cudaFuncSetAttribute(convt_k4s2_tc_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(convt_k4s2_tc_kernel<G, RAW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return launch_status(e);
     const long long tiles = ((long long)N * (H + 1) * (W + 1) + MT - 1) / MT;
     int per_phase = sms / 4 > 0 ? sms / 4 : 1;
     if (per_phase > tiles) per_phase = (int)tiles;
-    convt_k4s2_tc_kernel<G><<<4 * per_phase, NTHREADS, smem, st>>>(x, wtc, cb, bias, scale, out, N, H, W, Ho, Wo,
+    convt_k4s2_tc_kernel<G, RAW><<<4 * per_phase, NTHREADS, smem, st>>>(x, wtc, cb, bias, scale, out, N, H, W, Ho, Wo,
                                                                    nslab, L);
     note_launch();
     return launch_status(cudaGetLastError());
@@ -418,8 +440,11 @@ bool convt_tc_eligible(int Cin, int Cout, int k, int s, int p) {
     return k == 4 && s == 2 && p == 1 && Cout == COUT && (Cin == 8 || Cin == 16 || Cin == 32 || Cin == 64);
 }
 
-fw_status convt_tc_launch(const float *x, int N, int Cin, int H, int W, const float *w, const float *cb,
-                          const float *bias, float scale, float *out, int Ho, int Wo, void *ws, cudaStream_t st) {
+namespace {
+
+template <bool RAW>
+fw_status tc_launch(const float *x, int N, int Cin, int H, int W, const float *w, const float *cb,
+                    const float *bias, float scale, float *out, int Ho, int Wo, void *ws, cudaStream_t st) {
     float *wtc = static_cast<float *>(ws);
     const long long total = 16LL * Cin * COUT;
     convt_tc_prepack_kernel<<<(unsigned)min(1024LL, (total + 255) / 256), 256, 0, st>>>(w, wtc, Cin);
@@ -427,12 +452,65 @@ fw_status convt_tc_launch(const float *x, int N, int Cin, int H, int W, const fl
     fw_status rc = launch_status(cudaGetLastError());
     if (rc != FW_OK) return rc;
     switch (Cin) {
-        case 8: return launch_g<2>(x, N, H, W, wtc, cb, bias, scale, out, Ho, Wo, st);
-        case 16: return launch_g<4>(x, N, H, W, wtc, cb, bias, scale, out, Ho, Wo, st);
-        case 32: return launch_g<8>(x, N, H, W, wtc, cb, bias, scale, out, Ho, Wo, st);
-        case 64: return launch_g<16>(x, N, H, W, wtc, cb, bias, scale, out, Ho, Wo, st);
+        case 8: return launch_g<2, RAW>(x, N, H, W, wtc, cb, bias, scale, out, Ho, Wo, st);
+        case 16: return launch_g<4, RAW>(x, N, H, W, wtc, cb, bias, scale, out, Ho, Wo, st);
+        case 32: return launch_g<8, RAW>(x, N, H, W, wtc, cb, bias, scale, out, Ho, Wo, st);
+        case 64: return launch_g<16, RAW>(x, N, H, W, wtc, cb, bias, scale, out, Ho, Wo, st);
     }
     return FW_ERR_UNSUPPORTED;
+}
+
+// Stage 2 of the unfused path, one thread per output pixel: an online pass over the
+// channels for the softmax max and sum (the sum rescaled whenever the max grows),
+// then a second pass for sigmoid((p + bias) * scale).
+__global__ void __launch_bounds__(256) softmax_bias_scale_sigmoid_kernel(const float *__restrict__ y,
+                                                                         const float *__restrict__ bias,
+                                                                         float scale, float *__restrict__ out,
+                                                                         long long npix, int C, long long plane) {
+    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < npix;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const long long n = idx / plane, hw = idx - n * plane;
+        const float *yb = y + n * C * plane + hw;
+        float mx = -INFINITY, sum = 0.f;
+        for (int c = 0; c < C; ++c) {
+            const float z = __ldg(yb + c * plane) * LOG2E;
+            if (z > mx) {
+                sum *= ex2_approx(mx - z);
+                mx = z;
+            }
+            sum += ex2_approx(z - mx);
+        }
+        const float kp = -scale * LOG2E / sum;
+        float *ob = out + n * C * plane + hw;
+        for (int c = 0; c < C; ++c) {
+            const float e = ex2_approx(__ldg(yb + c * plane) * LOG2E - mx);
+            const float kb = -__ldg(bias + c) * scale * LOG2E;
+            ob[c * plane] = __fdividef(1.f, 1.f + ex2_approx(fmaf(e, kp, kb)));
+        }
+    }
+}
+
+}  // namespace
+
+fw_status convt_tc_launch(const float *x, int N, int Cin, int H, int W, const float *w, const float *cb,
+                          const float *bias, float scale, float *out, int Ho, int Wo, void *ws, cudaStream_t st) {
+    return tc_launch<false>(x, N, Cin, H, W, w, cb, bias, scale, out, Ho, Wo, ws, st);
+}
+
+// Stage 1 of the unfused path: y [N, 128, Ho, Wo] = conv-transpose(x) + conv_b.
+fw_status convt_tc_launch_raw(const float *x, int N, int Cin, int H, int W, const float *w, const float *cb,
+                              float *y, int Ho, int Wo, void *ws, cudaStream_t st) {
+    return tc_launch<true>(x, N, Cin, H, W, w, cb, nullptr, 0.f, y, Ho, Wo, ws, st);
+}
+
+fw_status softmax_bias_scale_sigmoid_launch(const float *y, int N, int C, int Ho, int Wo, const float *bias,
+                                            float scale, float *out, cudaStream_t st) {
+    const long long plane = (long long)Ho * Wo, npix = (long long)N * plane;
+    const long long want = (npix + 255) / 256;
+    const unsigned blocks = (unsigned)(want < 152LL * 64 ? want : 152LL * 64);
+    softmax_bias_scale_sigmoid_kernel<<<blocks, 256, 0, st>>>(y, bias, scale, out, npix, C, plane);
+    note_launch();
+    return launch_status(cudaGetLastError());
 }
 
 unsigned convt_tc_read_and_clear_error() {

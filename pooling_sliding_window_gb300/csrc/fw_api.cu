@@ -20,6 +20,16 @@ fw_status convt_launch(const float *x, int N, int Cin, int H, int W, const float
                        int Cout, int k, int s, int p, int op, const float *bias, float scale, float *out,
                        int Ho, int Wo, void *ws, size_t ws_bytes, cudaStream_t st);
 size_t convt_workspace_bytes(int Cin, int Cout, int k, int s, int p);
+bool convpool_tc_eligible(int Cin, int Cout, int KH, int KW, int pk, int ps);
+fw_status convpool_tc_launch_raw(const float *x, int N, int H, int W, const float *w, const float *cb, int Cout,
+                                 int pk, float *y, int Ho, int Wo, cudaStream_t st);
+fw_status pool_tanh_scale_bias_launch(const float *y, int N, int Cout, const float *bias, float scale, int pk,
+                                      float *out, int Ho, int Wo, cudaStream_t st);
+bool convt_tc_eligible(int Cin, int Cout, int k, int s, int p);
+fw_status convt_tc_launch_raw(const float *x, int N, int Cin, int H, int W, const float *w, const float *cb,
+                              float *y, int Ho, int Wo, void *ws, cudaStream_t st);
+fw_status softmax_bias_scale_sigmoid_launch(const float *y, int N, int C, int Ho, int Wo, const float *bias,
+                                            float scale, float *out, cudaStream_t st);
 
 static std::atomic<unsigned long long> g_launches{0};
 
@@ -228,6 +238,97 @@ fw_status fw_convtranspose2d_softmax_bias_scale_sigmoid(const float *x, int N, i
         return FW_ERR_ALIAS;
     return convt_launch(x, N, Cin, H, W, w, conv_b, Cout, k, s, p, op, bias, scale, out, Ho, Wo, workspace,
                         (size_t)workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+unsigned long long fw_conv2d_pool_unfused_workspace_size(int N, int H, int W, int Cout, int KH, int KW,
+                                                         int pool_k, int pool_s) {
+    int Ho = 0, Wo = 0;
+    if (N < 1 || Cout < 1 || conv_pool_shape(H, W, KH, KW, pool_k, pool_s, &Ho, &Wo) != FW_OK) return 0;
+    const long long n = prod({N, Cout, (long long)pool_k * Ho, (long long)pool_k * Wo});
+    return n < 0 ? 0 : 4ULL * (unsigned long long)n;
+}
+
+fw_status fw_conv2d_tanh_scale_bias_maxpool_unfused(const float *x, int N, int Cin, int H, int W, const float *w,
+                                                    const float *conv_b, int Cout, int KH, int KW, float scale,
+                                                    const float *bias, int pool_k, int pool_s, float *out,
+                                                    void *workspace, unsigned long long workspace_bytes,
+                                                    void *stream) {
+    if (!x || !w || !bias || !out || !workspace) return FW_ERR_NULL;
+    if (N < 1 || Cin < 1 || Cout < 1) return FW_ERR_SHAPE;
+    if (!std::isfinite(scale)) return FW_ERR_PARAM;
+    int Ho = 0, Wo = 0;
+    fw_status rc = conv_pool_shape(H, W, KH, KW, pool_k, pool_s, &Ho, &Wo);
+    if (rc != FW_OK) return rc;
+    if (pool_s <= 0) pool_s = pool_k;
+    if (misaligned(x) || misaligned(w) || misaligned(conv_b) || misaligned(bias) || misaligned(out) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 15u) != 0)
+        return FW_ERR_ALIGN;
+    const long long nx = prod({N, Cin, H, W}), nw = prod({Cout, Cin, KH, KW}), no = prod({N, Cout, Ho, Wo});
+    if (nx < 0 || nw < 0 || no < 0) return FW_ERR_SHAPE;
+    const unsigned long long need = fw_conv2d_pool_unfused_workspace_size(N, H, W, Cout, KH, KW, pool_k, pool_s);
+    if (need == 0) return FW_ERR_SHAPE;
+    if (workspace_bytes < need) return FW_ERR_NULL;
+    if (!convpool_tc_eligible(Cin, Cout, KH, KW, pool_k, pool_s)) return FW_ERR_UNSUPPORTED;
+    const long long ob = no * 4, wb = (long long)need;
+    const void *ins[] = {x, w, bias, conv_b};
+    const long long insz[] = {nx * 4, nw * 4, 4LL * Cout, 4LL * Cout};
+    for (int i = 0; i < 4; ++i)
+        if (overlaps(out, ob, ins[i], insz[i]) || overlaps(workspace, wb, ins[i], insz[i])) return FW_ERR_ALIAS;
+    if (overlaps(out, ob, workspace, wb)) return FW_ERR_ALIAS;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    float *y = static_cast<float *>(workspace);
+    rc = convpool_tc_launch_raw(x, N, H, W, w, conv_b, Cout, pool_k, y, Ho, Wo, st);
+    if (rc != FW_OK) return rc;
+    return pool_tanh_scale_bias_launch(y, N, Cout, bias, scale, pool_k, out, Ho, Wo, st);
+}
+
+// Workspace of the unfused conv-transpose: the weight rewrite, padded to 256 bytes,
+// then the intermediate.
+static unsigned long long convt_unfused_weights_bytes(int Cin, int Cout, int k, int s, int p) {
+    return ((unsigned long long)convt_workspace_bytes(Cin, Cout, k, s, p) + 255ULL) & ~255ULL;
+}
+
+unsigned long long fw_convt_unfused_workspace_size(int N, int Cin, int H, int W, int Cout, int k, int s, int p,
+                                                   int op) {
+    int Ho = 0, Wo = 0;
+    if (N < 1 || Cin < 1 || Cout < 1 || convt_shape(H, W, k, s, p, op, &Ho, &Wo) != FW_OK) return 0;
+    const long long n = prod({N, Cout, Ho, Wo});
+    return n < 0 ? 0 : convt_unfused_weights_bytes(Cin, Cout, k, s, p) + 4ULL * (unsigned long long)n;
+}
+
+fw_status fw_convtranspose2d_softmax_bias_scale_sigmoid_unfused(const float *x, int N, int Cin, int H, int W,
+                                                                const float *w, const float *conv_b, int Cout,
+                                                                int k, int s, int p, int op, const float *bias,
+                                                                float scale, float *out, void *workspace,
+                                                                unsigned long long workspace_bytes,
+                                                                void *stream) {
+    if (!x || !w || !bias || !out || !workspace) return FW_ERR_NULL;
+    if (N < 1 || Cin < 1 || Cout < 1) return FW_ERR_SHAPE;
+    if (!std::isfinite(scale)) return FW_ERR_PARAM;
+    int Ho = 0, Wo = 0;
+    fw_status rc = convt_shape(H, W, k, s, p, op, &Ho, &Wo);
+    if (rc != FW_OK) return rc;
+    if (misaligned(x) || misaligned(w) || misaligned(conv_b) || misaligned(bias) || misaligned(out) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 15u) != 0)
+        return FW_ERR_ALIGN;
+    const long long nx = prod({N, Cin, H, W}), nw = prod({Cin, Cout, k, k}), no = prod({N, Cout, Ho, Wo});
+    if (nx < 0 || nw < 0 || no < 0) return FW_ERR_SHAPE;
+    const unsigned long long need = fw_convt_unfused_workspace_size(N, Cin, H, W, Cout, k, s, p, op);
+    if (need == 0) return FW_ERR_SHAPE;
+    if (workspace_bytes < need) return FW_ERR_NULL;
+    if (!convt_tc_eligible(Cin, Cout, k, s, p)) return FW_ERR_UNSUPPORTED;
+    const long long ob = no * 4, wb = (long long)need;
+    const void *ins[] = {x, w, bias, conv_b};
+    const long long insz[] = {nx * 4, nw * 4, 4LL * Cout, 4LL * Cout};
+    for (int i = 0; i < 4; ++i)
+        if (overlaps(out, ob, ins[i], insz[i]) || overlaps(workspace, wb, ins[i], insz[i])) return FW_ERR_ALIAS;
+    if (overlaps(out, ob, workspace, wb)) return FW_ERR_ALIAS;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    float *y = reinterpret_cast<float *>(ws + convt_unfused_weights_bytes(Cin, Cout, k, s, p));
+    rc = convt_tc_launch_raw(x, N, Cin, H, W, w, conv_b, y, Ho, Wo, ws, st);
+    if (rc != FW_OK) return rc;
+    return softmax_bias_scale_sigmoid_launch(y, N, Cout, Ho, Wo, bias, scale, out, st);
 }
 
 fw_status fw_selftest_bounded_wait(unsigned int limit_us, void *stream) {

@@ -29,7 +29,9 @@ EXPORTS = ("fw_status_string", "fw_version", "fw_conv2d_pool_out_shape", "fw_max
            "fw_convt_out_shape", "fw_conv2d_tanh_scale_bias_maxpool", "fw_maxpool2d",
            "fw_convtranspose2d_softmax_bias_scale_sigmoid", "fw_convt_workspace_size",
            "fw_check_device_errors", "fw_launch_count", "fw_selftest_bounded_wait",
-           "fw_convtranspose2d_softmax_bias_scale_sigmoid_noalloc")
+           "fw_convtranspose2d_softmax_bias_scale_sigmoid_noalloc",
+           "fw_conv2d_tanh_scale_bias_maxpool_unfused", "fw_conv2d_pool_unfused_workspace_size",
+           "fw_convtranspose2d_softmax_bias_scale_sigmoid_unfused", "fw_convt_unfused_workspace_size")
 
 
 class FusedWinError(RuntimeError):
@@ -76,6 +78,16 @@ def lib():
         L.fw_convtranspose2d_softmax_bias_scale_sigmoid_noalloc.restype = I
         L.fw_convtranspose2d_softmax_bias_scale_sigmoid_noalloc.argtypes = [
             P, I, I, I, I, P, P, I, I, I, I, I, P, F, P, P]
+        L.fw_conv2d_tanh_scale_bias_maxpool_unfused.restype = I
+        L.fw_conv2d_tanh_scale_bias_maxpool_unfused.argtypes = [
+            P, I, I, I, I, P, P, I, I, I, F, P, I, I, P, P, U64, P]
+        L.fw_conv2d_pool_unfused_workspace_size.restype = U64
+        L.fw_conv2d_pool_unfused_workspace_size.argtypes = [I] * 8
+        L.fw_convtranspose2d_softmax_bias_scale_sigmoid_unfused.restype = I
+        L.fw_convtranspose2d_softmax_bias_scale_sigmoid_unfused.argtypes = [
+            P, I, I, I, I, P, P, I, I, I, I, I, P, F, P, P, U64, P]
+        L.fw_convt_unfused_workspace_size.restype = U64
+        L.fw_convt_unfused_workspace_size.argtypes = [I] * 9
         _lib = L
     return _lib
 
@@ -244,3 +256,63 @@ def fw_convtranspose2d_softmax_bias_scale_sigmoid_noalloc(x, w, conv_b, bias, sc
             _ptr(bias), float(scale), _ptr(out), C.c_void_p(stream)),
             "fw_convtranspose2d_softmax_bias_scale_sigmoid_noalloc")
     return out
+
+
+# ------------------------------------------------------ unfused comparison --
+
+def fw_conv2d_pool_unfused_workspace_size(N, H, W, Cout, KH, KW, pool_k, pool_s=0) -> int:
+    return int(lib().fw_conv2d_pool_unfused_workspace_size(N, H, W, Cout, KH, KW, pool_k, pool_s))
+
+
+def fw_convt_unfused_workspace_size(N, Cin, H, W, Cout, k, s, p, op) -> int:
+    return int(lib().fw_convt_unfused_workspace_size(N, Cin, H, W, Cout, k, s, p, op))
+
+
+def _workspace(need, workspace, dev):
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty((need + 15) // 16 * 4, device=dev, dtype=torch.float32)
+    return workspace, workspace.numel() * workspace.element_size()
+
+
+def fw_conv2d_tanh_scale_bias_maxpool_unfused(x, w, conv_b, bias, scale, pool_k, pool_s=0, out=None,
+                                              workspace=None):
+    """The conv+pool model the unfused way (conv output to memory, then pool + tanh
+    + scale + bias); bit-identical to fw_conv2d_tanh_scale_bias_maxpool."""
+    dev = _device_of(x)
+    xd, wd = _dev(x, "x", dev), _dev(w, "w", dev)
+    cbd, bd = _dev(conv_b, "conv_b", dev), _dev(bias.reshape(-1), "bias", dev)
+    N, Cin, H, W = xd.shape
+    Cout, _, KH, KW = wd.shape
+    Ho, Wo = fw_conv2d_pool_out_shape(H, W, KH, KW, pool_k, pool_s)
+    workspace, ws_bytes = _workspace(fw_conv2d_pool_unfused_workspace_size(N, H, W, Cout, KH, KW, pool_k, pool_s),
+                                     workspace, dev)
+    od = out if out is not None else torch.empty((N, Cout, Ho, Wo), device=dev, dtype=torch.float32)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    with torch.cuda.device(dev):
+        _check(lib().fw_conv2d_tanh_scale_bias_maxpool_unfused(
+            _ptr(xd), N, Cin, H, W, _ptr(wd), _ptr(cbd), Cout, KH, KW, float(scale), _ptr(bd),
+            pool_k, pool_s, _ptr(od), _ptr(workspace), ws_bytes, C.c_void_p(stream)),
+            "fw_conv2d_tanh_scale_bias_maxpool_unfused")
+    return od
+
+
+def fw_convtranspose2d_softmax_bias_scale_sigmoid_unfused(x, w, conv_b, bias, scale, stride=2, padding=1,
+                                                          output_padding=1, out=None, workspace=None):
+    """The conv-transpose model the unfused way (conv-transpose output to memory,
+    then an online-softmax pass and an output pass per pixel)."""
+    dev = _device_of(x)
+    xd, wd = _dev(x, "x", dev), _dev(w, "w", dev)
+    cbd, bd = _dev(conv_b, "conv_b", dev), _dev(bias.reshape(-1), "bias", dev)
+    N, Cin, H, W = xd.shape
+    _, Cout, K, _ = wd.shape
+    Ho, Wo = fw_convt_out_shape(H, W, K, stride, padding, output_padding)
+    workspace, ws_bytes = _workspace(
+        fw_convt_unfused_workspace_size(N, Cin, H, W, Cout, K, stride, padding, output_padding), workspace, dev)
+    od = out if out is not None else torch.empty((N, Cout, Ho, Wo), device=dev, dtype=torch.float32)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    with torch.cuda.device(dev):
+        _check(lib().fw_convtranspose2d_softmax_bias_scale_sigmoid_unfused(
+            _ptr(xd), N, Cin, H, W, _ptr(wd), _ptr(cbd), Cout, K, stride, padding, output_padding,
+            _ptr(bd), float(scale), _ptr(od), _ptr(workspace), ws_bytes, C.c_void_p(stream)),
+            "fw_convtranspose2d_softmax_bias_scale_sigmoid_unfused")
+    return od

@@ -110,6 +110,28 @@ def test_operator_argument_errors_without_launch():
     assert ct(op=2) == 3
     assert ct(Cout=2048) == 6
     assert ct(out=P(0x80000000 + 4096)) == 4  # out overlaps workspace
+    # unfused comparison path: workspace, alignment, support and aliasing checks
+    cpn = FW.fw_conv2d_pool_unfused_workspace_size(2, 64, 64, 64, 3, 3, 4)
+    assert cpn == 4 * 2 * 64 * 60 * 60
+    big = P(0x100000000)
+    cpu = lambda **kw: L.fw_conv2d_tanh_scale_bias_maxpool_unfused(
+        x, 2, kw.get("Cin", 8), 64, 64, w, None, 64, 3, 3, 2.0, b, 4, 0, kw.get("out", o), kw.get("ws", big),
+        kw.get("wsb", cpn), None)
+    assert cpu(ws=None) == 1
+    assert cpu(wsb=cpn - 1) == 1
+    assert cpu(ws=P(0x100000008)) == 5
+    assert cpu(Cin=4) == 6
+    assert cpu(out=P(0x100000000 + 64)) == 4
+    ctn = FW.fw_convt_unfused_workspace_size(1, 64, 8, 8, 128, 4, 2, 1, 1)
+    assert ctn == ((16 * 64 * 128 * 4 + 255) // 256) * 256 + 4 * 128 * 17 * 17
+    ctu = lambda **kw: L.fw_convtranspose2d_softmax_bias_scale_sigmoid_unfused(
+        x, 1, kw.get("Cin", 64), 8, 8, w, None, 128, 4, kw.get("s", 2), 1, 1, b, 2.0, o, kw.get("ws", big),
+        kw.get("wsb", ctn), None)
+    assert ctu(ws=None) == 1
+    assert ctu(wsb=ctn - 4) == 1
+    assert ctu(Cin=12) == 6
+    assert ctu(s=3) == 6
+    assert FW.fw_convt_unfused_workspace_size(1, 64, 8, 8, 128, 4, 2, 1, 2) == 0  # op >= s
     # the bounded-wait self-test checks its limit before launching
     assert L.fw_selftest_bounded_wait(0, None) == 3
     assert L.fw_selftest_bounded_wait(2_000_001, None) == 3
