@@ -32,6 +32,12 @@
  *   - The fused conv+pool applies tanh/scale/bias to EVERY conv output before
  *     pooling, literally in the model's order; no reordering is done here.
  *   - Pool windows use floor mode (ragged rows/cols are dropped), no padding.
+ *   - Extensions beyond the pages (the generic MaxPool2d options the l1_p42 trace
+ *     names only as PyTorch's non-default behaviour): ceil mode and argmax
+ *     indices, following PyTorch's documented MaxPool2d definition -- in ceil
+ *     mode the size rounds up, and a window that would start in the right
+ *     padding is dropped; an index is the flat ih*W + iw of the tap the value
+ *     came from (same tie and NaN rules; -1 when a window has no input tap).
  *
  * Parity pins for every function here live in the CPU test-suite (brute force,
  * library special cases, closed forms, invariants, the adjoint identity).
@@ -65,6 +71,17 @@ long oracle_conv2d_out_size(long H, long k, long s, long p) {
 long oracle_pool_out_size(long H, long k, long s, long p, long d) {
     if (k < 1 || s < 1 || p < 0 || d < 1) return -1;
     return floordiv(H + 2 * p - d * (k - 1) - 1, s) + 1;
+}
+
+/* MaxPool2d output size in ceil mode (extension, see the readings above):
+ * ceil((H + 2p - d(k-1) - 1) / s) + 1, minus one when that last window would
+ * start at or past H + p (inside the right padding). */
+long oracle_pool_out_size_ceil(long H, long k, long s, long p, long d) {
+    if (k < 1 || s < 1 || p < 0 || d < 1) return -1;
+    const long span = H + 2 * p - d * (k - 1) - 1;
+    long o = -floordiv(-span, s) + 1;  /* ceil(span / s) + 1 */
+    if (o >= 1 && (o - 1) * s >= H + p) o -= 1;
+    return o;
 }
 
 /* ConvTranspose2d output size, dilation 1 ([P3] output-size formula: 64 -> 129). */
@@ -135,6 +152,50 @@ float oracle_maxpool2d_one(const float *plane, long H, long W, long k, long s,
             m = max_update(m, v);
         }
     return m;
+}
+
+/* One MaxPool2d output and its argmax (extension): the value as in
+ * oracle_maxpool2d_one; *idx = ih*W + iw of the input tap that value came from --
+ * the first in-bounds tap initialises the running (value, index), later taps
+ * replace it by the running-max rule -- or -1 when no tap is in bounds. */
+float oracle_maxpool2d_one_idx(const float *plane, long H, long W, long k, long s,
+                               long p, long d, long oh, long ow, long *idx) {
+    float m = -INFINITY;
+    long at = -1;
+    for (long kh = 0; kh < k; ++kh)
+        for (long kw = 0; kw < k; ++kw) {
+            const long ih = oh * s - p + kh * d;
+            const long iw = ow * s - p + kw * d;
+            if (ih < 0 || ih >= H || iw < 0 || iw >= W) continue;  /* -inf: never the first max */
+            float v = plane[ih * W + iw];
+            /* the running-max rule of max_update, keeping the tap's index with the value */
+            if (at < 0 || (!isnan(m) && (isnan(v) || v > m))) {
+                m = v;
+                at = ih * W + iw;
+            }
+        }
+    *idx = at;
+    return m;
+}
+
+/* MaxPool2d with ceil mode and indices (extension): out and idx [N,C,Ho,Wo]
+ * (idx may be NULL), Ho/Wo from oracle_pool_out_size(_ceil). */
+int oracle_maxpool2d_ex(const float *x, long N, long C, long H, long W, long k, long s, long p,
+                        long d, int ceil_mode, float *out, long *idx) {
+    long Ho = ceil_mode ? oracle_pool_out_size_ceil(H, k, s, p, d) : oracle_pool_out_size(H, k, s, p, d);
+    long Wo = ceil_mode ? oracle_pool_out_size_ceil(W, k, s, p, d) : oracle_pool_out_size(W, k, s, p, d);
+    if (Ho < 1 || Wo < 1) return ORACLE_EINVAL;
+    for (long nc = 0; nc < N * C; ++nc) {
+        const float *plane = x + nc * H * W;
+        for (long oh = 0; oh < Ho; ++oh)
+            for (long ow = 0; ow < Wo; ++ow) {
+                long at;
+                const long o = (nc * Ho + oh) * Wo + ow;
+                out[o] = oracle_maxpool2d_one_idx(plane, H, W, k, s, p, d, oh, ow, &at);
+                if (idx) idx[o] = at;
+            }
+    }
+    return ORACLE_OK;
 }
 
 /* Full MaxPool2d: x [N,C,H,W] -> out [N,C,Ho,Wo]. */

@@ -62,6 +62,12 @@ def load(path: str):
     L.oracle_maxpool2d.argtypes = [_f32p, _L, _L, _L, _L, _L, _L, _L, _L, _f32p]
     L.oracle_maxpool2d_one.restype = C.c_float
     L.oracle_maxpool2d_one.argtypes = [fp, _L, _L, _L, _L, _L, _L, _L, _L]
+    L.oracle_pool_out_size_ceil.restype = _L
+    L.oracle_pool_out_size_ceil.argtypes = [_L] * 5
+    L.oracle_maxpool2d_one_idx.restype = C.c_float
+    L.oracle_maxpool2d_one_idx.argtypes = [fp, _L, _L, _L, _L, _L, _L, _L, _L, C.POINTER(_L)]
+    L.oracle_maxpool2d_ex.restype = C.c_int
+    L.oracle_maxpool2d_ex.argtypes = [_f32p, _L, _L, _L, _L, _L, _L, _L, _L, C.c_int, _f32p, C.c_void_p]
     L.oracle_conv2d_tanh_scale_bias_maxpool.restype = C.c_int
     L.oracle_conv2d_tanh_scale_bias_maxpool.argtypes = [
         _f32p, _L, _L, _L, _L, _f32p, fp, _L, _L, _L, C.c_float, _f32p, _L, _L, _f32p]
@@ -165,6 +171,26 @@ def maxpool2d(x, k, s=None, p=0, d=1):
     out = np.empty((N, Cc, max(Ho, 0), max(Wo, 0)), dtype=np.float32)
     _check(lib().oracle_maxpool2d(x, N, Cc, H, W, k, s, p, d, out))
     return out
+
+
+def pool_out_size_ceil(H, k, s, p=0, d=1):
+    """MaxPool2d output size in ceil mode (extension beyond the pages)."""
+    return int(lib().oracle_pool_out_size_ceil(H, k, s, p, d))
+
+
+def maxpool2d_ex(x, k, s=None, p=0, d=1, ceil_mode=False):
+    """MaxPool2d with ceil mode and argmax indices (extension): (out float32,
+    idx int64 = flat ih*W + iw of the chosen tap, -1 for a window with no input tap)."""
+    x = _f32(x)
+    s = k if s is None else s
+    N, Cc, H, W = x.shape
+    size = pool_out_size_ceil if ceil_mode else pool_out_size
+    Ho, Wo = size(H, k, s, p, d), size(W, k, s, p, d)
+    out = np.empty((N, Cc, max(Ho, 0), max(Wo, 0)), dtype=np.float32)
+    idx = np.empty(out.shape, dtype=np.int64)
+    _check(lib().oracle_maxpool2d_ex(x, N, Cc, H, W, k, s, p, d, int(bool(ceil_mode)), out,
+                                     idx.ctypes.data_as(C.c_void_p)))
+    return out, idx
 
 
 def maxpool2d_at(x, k, s, p, d, n, c, oh, ow):

@@ -27,6 +27,9 @@ MUTANTS = {
                               "long ih = oh * s - p + kh, iw = ow * s - p + kw * d;"),
     "pool_tie_keeps_last": ("if (isnan(v) || v > m) return v;", "if (isnan(v) || v >= m) return v;"),
     "pool_size_formula": ("return floordiv(H + 2 * p - d * (k - 1) - 1, s) + 1;", "return floordiv(H + 2 * p - d * (k - 1), s) + 1;"),
+    "ceil_keeps_window_in_right_padding": ("if (o >= 1 && (o - 1) * s >= H + p) o -= 1;", "if (o >= 1 && (o - 1) * s > H + p) o -= 1;"),
+    "index_tie_keeps_last": ("if (at < 0 || (!isnan(m) && (isnan(v) || v > m))) {", "if (at < 0 || (!isnan(m) && (isnan(v) || v >= m))) {"),
+    "index_transposed": ("                at = ih * W + iw;\n            }", "                at = iw * H + ih;\n            }"),
     "epilogue_bias_sign": ("return (float)((double)u + (double)b);", "return (float)((double)u - (double)b);"),
     "epilogue_no_tanh": ("float t = (float)tanh((double)y);", "float t = y;"),
     "convpool_window_stride": ("long oh = i * ps + a, ow = j * ps + b;", "long oh = i * pk + a, ow = j * ps + b;"),

@@ -244,6 +244,75 @@ def test_maxpool_tie_and_nan_reading():
     assert np.isnan(ref[0, 0, 0, 0])
 
 
+# ---------------------------------------------- maxpool extensions (ceil mode, indices) --
+# Not on the pages: PyTorch's documented MaxPool2d options, pinned against its CPU
+# implementation on NaN-free inputs (torch keeps the last NaN, the reading here is
+# the first) and by invariants.
+
+CEIL_GRID = [(k, s, p, d) for k in (1, 2, 3, 4) for s in (1, 2, 3) for p in range(0, k // 2 + 1) for d in (1, 2)]
+
+
+def test_ceil_sizes_match_torch():
+    seen_drop = False
+    for H in (1, 2, 3, 4, 5, 6, 7, 10, 13):
+        for k, s, p, d in CEIL_GRID:
+            if H + 2 * p - d * (k - 1) - 1 < 0:
+                continue
+            ref = F.max_pool2d(torch.zeros(1, 1, H, H), k, s, p, d, ceil_mode=True).shape[-1]
+            assert O.pool_out_size_ceil(H, k, s, p, d) == ref, (H, k, s, p, d)
+            span = H + 2 * p - d * (k - 1) - 1
+            if -(-span // s) * s >= H + p:  # the last ceil window would start in the right padding
+                seen_drop = True
+    assert seen_drop  # the sweep exercises the dropped-window rule
+
+
+@pytest.mark.parametrize("ceil_mode", [False, True])
+def test_maxpool_indices_match_torch(ceil_mode):
+    # small integers: many ties, so the first-max rule is exercised
+    x = RNG.integers(-3, 4, size=(2, 2, 11, 9)).astype(np.float32)
+    for k, s, p, d in CEIL_GRID:
+        if 9 + 2 * p - d * (k - 1) - 1 < 0:
+            continue
+        out, idx = O.maxpool2d_ex(x, k, s, p, d, ceil_mode)
+        ro, ri = F.max_pool2d(torch.from_numpy(x), k, s, p, d, ceil_mode=ceil_mode, return_indices=True)
+        np.testing.assert_array_equal(out, ro.numpy(), err_msg=str((k, s, p, d)))
+        np.testing.assert_array_equal(idx, ri.numpy(), err_msg=str((k, s, p, d)))
+        if not ceil_mode:
+            np.testing.assert_array_equal(out, O.maxpool2d(x, k, s, p, d))
+
+
+def test_maxpool_indices_invariants_with_nan():
+    x = RNG.standard_normal((1, 2, 12, 10)).astype(np.float32)
+    x[0, 0, 3, 4] = x[0, 1, 7, 2] = x[0, 1, 7, 5] = np.nan
+    x[0, 0, 5, 5] = x[0, 0, 5, 6] = 9.0  # a tie at the maximum
+    k, s, p, d = 3, 2, 1, 1
+    out, idx = O.maxpool2d_ex(x, k, s, p, d, True)
+    for c in range(2):
+        plane = x[0, c]
+        for oh in range(out.shape[2]):
+            for ow in range(out.shape[3]):
+                taps = [(oh * s - p + i * d, ow * s - p + j * d) for i in range(k) for j in range(k)]
+                taps = [(h, w) for h, w in taps if 0 <= h < 12 and 0 <= w < 10]
+                v, at = out[0, c, oh, ow], idx[0, c, oh, ow]
+                assert (at // 10, at % 10) in taps
+                vals = [plane[h, w] for h, w in taps]
+                pos = taps.index((at // 10, at % 10))
+                if np.isnan(v):  # the first NaN of the window in row-major order
+                    assert np.isnan(plane[at // 10, at % 10]) and not any(np.isnan(vals[:pos]))
+                else:  # the first maximum; no NaN in the window
+                    assert plane[at // 10, at % 10] == v and not any(np.isnan(vals))
+                    assert all(u < v for u in vals[:pos]) and all(u <= v for u in vals)
+    assert idx[0, 0, 3, 3] == 5 * 10 + 5  # window rows/cols 5-7: the tie keeps the first tap
+    assert idx[0, 0, 2, 2] == 3 * 10 + 4  # window rows/cols 3-5 holds the NaN at (3, 4)
+
+
+def test_maxpool_index_of_window_without_input_tap():
+    x = rnd(1, 1, 3, 3)
+    out, idx = O.maxpool2d_ex(x, 1, 1, 1, 1, False)  # k = 1, p = 1: the border windows see only padding
+    assert idx[0, 0, 0, 0] == -1 and np.isneginf(out[0, 0, 0, 0])
+    assert idx[0, 0, 1, 1] == 0 and out[0, 0, 1, 1] == x[0, 0, 0, 0]
+
+
 # ------------------------------------------------------ fused conv+pool ----
 
 def torch_model_p82(x, w, cb, scale, bias, pk, ps):
