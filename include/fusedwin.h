@@ -120,6 +120,24 @@ fw_status fw_maxpool2d(const float *x, int N, int C, int H, int W, int k, int s,
                        float *out, void *stream);
 
 /*
+ * MaxPool2d with PyTorch's optional extensions (not on the pages: the l1_p42 trace
+ * names ceil mode only as the non-default behaviour it does not use; indices are
+ * not mentioned).  Same definition, tie and NaN rules as fw_maxpool2d, plus:
+ *   ceil_mode != 0: each output size is ceil((H + 2p - d(k-1) - 1)/s) + 1, minus
+ *     one when that last window would start at or past H + p (in the right
+ *     padding); see fw_maxpool2d_out_shape_ex.  With s = 1 it equals floor mode.
+ *   indices (optional, int64 [N, C, Ho, Wo], 8-byte aligned, or NULL): for each
+ *     output, the flat index ih*W + iw within its input plane of the tap the value
+ *     came from (first maximum in row-major tap order; first NaN if any), or -1
+ *     when the window holds no input tap (the value is then -inf).
+ * Without indices and with the floor-mode size, the call takes fw_maxpool2d's
+ * kernels; otherwise a direct kernel (one thread per output).
+ */
+fw_status fw_maxpool2d_ex(const float *x, int N, int C, int H, int W, int k, int s, int p, int d,
+                          int ceil_mode, float *out, long long *indices, void *stream);
+fw_status fw_maxpool2d_out_shape_ex(int H, int W, int k, int s, int p, int d, int ceil_mode, int *Ho, int *Wo);
+
+/*
  * ConvTranspose2d -> softmax over channels -> +bias -> *scale -> sigmoid
  * (trace "Kimi-K2.6 l2_p91", the model and the index map oh = ih*s + kh - p):
  *

@@ -10,6 +10,8 @@ namespace fw {
 
 fw_status maxpool2d_launch(const float *x, long long NC, int H, int W, int k, int s, int p, int d, int Ho,
                            int Wo, float *out, cudaStream_t st);
+fw_status maxpool2d_ex_launch(const float *x, long long NC, int H, int W, int k, int s, int p, int d, int Ho,
+                              int Wo, float *out, long long *idx, cudaStream_t st);
 unsigned maxpool_read_and_clear_error();
 unsigned convt_tc_read_and_clear_error();
 unsigned convpool_tc_read_and_clear_error();
@@ -113,6 +115,26 @@ fw_status maxpool_shape(int H, int W, int k, int s, int p, int d, int *Ho, int *
     return FW_OK;
 }
 
+// One dimension in ceil mode (PyTorch's MaxPool2d option, not on the pages): the
+// size rounds up, and a last window that would start in the right padding is dropped.
+long long pool_dim_ceil(long long H, int k, int s, int p, int d) {
+    const long long span = H + 2LL * p - (long long)d * (k - 1) - 1;
+    long long o = -floordiv(-span, s) + 1;
+    if (o >= 1 && (o - 1) * s >= H + p) --o;
+    return o;
+}
+
+fw_status maxpool_shape_ex(int H, int W, int k, int s, int p, int d, int ceil_mode, int *Ho, int *Wo) {
+    if (!ceil_mode) return maxpool_shape(H, W, k, s, p, d, Ho, Wo);
+    if (H < 1 || W < 1) return FW_ERR_SHAPE;
+    if (k < 1 || s < 1 || p < 0 || d < 1) return FW_ERR_PARAM;
+    const long long ho = pool_dim_ceil(H, k, s, p, d), wo = pool_dim_ceil(W, k, s, p, d);
+    if (ho < 1 || wo < 1 || ho > 0x7fffffffLL || wo > 0x7fffffffLL) return FW_ERR_SHAPE;
+    *Ho = (int)ho;
+    *Wo = (int)wo;
+    return FW_OK;
+}
+
 fw_status convt_shape(int H, int W, int k, int s, int p, int op, int *Ho, int *Wo) {
     if (H < 1 || W < 1) return FW_ERR_SHAPE;
     if (k < 1 || s < 1 || p < 0 || op < 0 || op >= s) return FW_ERR_PARAM;
@@ -161,6 +183,11 @@ fw_status fw_maxpool2d_out_shape(int H, int W, int k, int s, int p, int d, int *
     return maxpool_shape(H, W, k, s, p, d, Ho, Wo);
 }
 
+fw_status fw_maxpool2d_out_shape_ex(int H, int W, int k, int s, int p, int d, int ceil_mode, int *Ho, int *Wo) {
+    if (!Ho || !Wo) return FW_ERR_NULL;
+    return maxpool_shape_ex(H, W, k, s, p, d, ceil_mode, Ho, Wo);
+}
+
 fw_status fw_convt_out_shape(int H, int W, int k, int s, int p, int op, int *Ho, int *Wo) {
     if (!Ho || !Wo) return FW_ERR_NULL;
     return convt_shape(H, W, k, s, p, op, Ho, Wo);
@@ -207,6 +234,26 @@ fw_status fw_maxpool2d(const float *x, int N, int C, int H, int W, int k, int s,
     if (overlaps(out, no * 4, x, nx * 4)) return FW_ERR_ALIAS;
     return maxpool2d_launch(x, (long long)N * C, H, W, k, s, p, d, Ho, Wo, out,
                             static_cast<cudaStream_t>(stream));
+}
+
+fw_status fw_maxpool2d_ex(const float *x, int N, int C, int H, int W, int k, int s, int p, int d, int ceil_mode,
+                          float *out, long long *indices, void *stream) {
+    if (!x || !out) return FW_ERR_NULL;
+    if (N < 1 || C < 1) return FW_ERR_SHAPE;
+    int Ho = 0, Wo = 0;
+    fw_status rc = maxpool_shape_ex(H, W, k, s, p, d, ceil_mode, &Ho, &Wo);
+    if (rc != FW_OK) return rc;
+    if (misaligned(x) || misaligned(out) || (reinterpret_cast<uintptr_t>(indices) & 7u) != 0) return FW_ERR_ALIGN;
+    const long long nx = prod({N, C, H, W}), no = prod({N, C, Ho, Wo});
+    if (nx < 0 || no < 0) return FW_ERR_SHAPE;
+    if (overlaps(out, no * 4, x, nx * 4) || overlaps(indices, no * 8, x, nx * 4) ||
+        overlaps(indices, no * 8, out, no * 4))
+        return FW_ERR_ALIAS;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int fHo = 0, fWo = 0;
+    if (!indices && maxpool_shape(H, W, k, s, p, d, &fHo, &fWo) == FW_OK && fHo == Ho && fWo == Wo)
+        return maxpool2d_launch(x, (long long)N * C, H, W, k, s, p, d, Ho, Wo, out, st);  // same as floor mode
+    return maxpool2d_ex_launch(x, (long long)N * C, H, W, k, s, p, d, Ho, Wo, out, indices, st);
 }
 
 fw_status fw_convtranspose2d_softmax_bias_scale_sigmoid(const float *x, int N, int Cin, int H, int W,

@@ -240,6 +240,44 @@ __global__ void maxpool_direct_kernel(const float *__restrict__ x, float *__rest
     }
 }
 
+// Generic MaxPool2d with the optional PyTorch extensions (not on the pages): any
+// (k, s, p, d), an output size from floor or ceil mode (given), and optional argmax
+// indices.  One thread per output; the first in-bounds tap initialises the
+// running (value, index), later taps replace it by the running-max rule (a larger
+// value, or a NaN when the current value is not NaN), so values equal the other
+// kernels' and an index is the flat ih*W + iw of the tap the value came from (-1
+// when the window has no input tap; the value is then -inf).
+__global__ void __launch_bounds__(256) maxpool_direct_ex_kernel(const float *__restrict__ x, float *__restrict__ out,
+                                                                long long *__restrict__ idx, long long NC, int H,
+                                                                int W, int Ho, int Wo, int k, int s, int p, int d) {
+    const long long total = NC * Ho * Wo;
+    for (long long o = blockIdx.x * (long long)blockDim.x + threadIdx.x; o < total;
+         o += (long long)gridDim.x * blockDim.x) {
+        const int ow = (int)(o % Wo);
+        const long long t = o / Wo;
+        const int oh = (int)(t % Ho);
+        const long long nc = t / Ho;
+        const float *plane = x + nc * (long long)H * W;
+        float m = -INFINITY;
+        long long at = -1;
+        for (int i = 0; i < k; ++i) {
+            const int ih = oh * s - p + i * d;
+            if (ih < 0 || ih >= H) continue;
+            for (int j = 0; j < k; ++j) {
+                const int iw = ow * s - p + j * d;
+                if (iw < 0 || iw >= W) continue;
+                const float v = __ldg(plane + (long long)ih * W + iw);
+                if (at < 0 || (m == m && (v != v || v > m))) {
+                    m = v;
+                    at = (long long)ih * W + iw;
+                }
+            }
+        }
+        out[o] = m;
+        if (idx) idx[o] = at;
+    }
+}
+
 template <int K, int P>
 fw_status launch_stream(const float *x, float *out, long long NC, int H, int W, int Ho, int Wo,
                         cudaStream_t st) {
@@ -301,6 +339,17 @@ unsigned maxpool_read_and_clear_error() {
     if (cudaMemcpyFromSymbol(&v, g_err_maxpool, sizeof(v)) != cudaSuccess) return DEVERR_INTERNAL;
     if (v) cudaMemcpyToSymbol(g_err_maxpool, &zero, sizeof(zero));
     return v;
+}
+
+fw_status maxpool2d_ex_launch(const float *x, long long NC, int H, int W, int k, int s, int p, int d, int Ho,
+                              int Wo, float *out, long long *idx, cudaStream_t st) {
+    const long long total = NC * Ho * Wo;
+    const int threads = 256;
+    long long blocks = (total + threads - 1) / threads;
+    if (blocks > 152LL * 64) blocks = 152LL * 64;
+    maxpool_direct_ex_kernel<<<(unsigned)blocks, threads, 0, st>>>(x, out, idx, NC, H, W, Ho, Wo, k, s, p, d);
+    note_launch();
+    return launch_status(cudaGetLastError());
 }
 
 }  // namespace fw

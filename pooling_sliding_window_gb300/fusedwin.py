@@ -31,7 +31,8 @@ EXPORTS = ("fw_status_string", "fw_version", "fw_conv2d_pool_out_shape", "fw_max
            "fw_check_device_errors", "fw_launch_count", "fw_selftest_bounded_wait",
            "fw_convtranspose2d_softmax_bias_scale_sigmoid_noalloc",
            "fw_conv2d_tanh_scale_bias_maxpool_unfused", "fw_conv2d_pool_unfused_workspace_size",
-           "fw_convtranspose2d_softmax_bias_scale_sigmoid_unfused", "fw_convt_unfused_workspace_size")
+           "fw_convtranspose2d_softmax_bias_scale_sigmoid_unfused", "fw_convt_unfused_workspace_size",
+           "fw_maxpool2d_ex", "fw_maxpool2d_out_shape_ex")
 
 
 class FusedWinError(RuntimeError):
@@ -88,6 +89,10 @@ def lib():
             P, I, I, I, I, P, P, I, I, I, I, I, P, F, P, P, U64, P]
         L.fw_convt_unfused_workspace_size.restype = U64
         L.fw_convt_unfused_workspace_size.argtypes = [I] * 9
+        L.fw_maxpool2d_ex.restype = I
+        L.fw_maxpool2d_ex.argtypes = [P, I, I, I, I, I, I, I, I, I, P, P, P]
+        L.fw_maxpool2d_out_shape_ex.restype = I
+        L.fw_maxpool2d_out_shape_ex.argtypes = [I] * 7 + [IP, IP]
         _lib = L
     return _lib
 
@@ -316,3 +321,26 @@ def fw_convtranspose2d_softmax_bias_scale_sigmoid_unfused(x, w, conv_b, bias, sc
             _ptr(bd), float(scale), _ptr(od), _ptr(workspace), ws_bytes, C.c_void_p(stream)),
             "fw_convtranspose2d_softmax_bias_scale_sigmoid_unfused")
     return od
+
+
+# ------------------------------------------------- maxpool extensions --
+
+def fw_maxpool2d_out_shape_ex(H, W, k, s, p, d, ceil_mode=False):
+    return _shape2("fw_maxpool2d_out_shape_ex", H, W, k, s, p, d, int(bool(ceil_mode)))
+
+
+def fw_maxpool2d_ex(x, k, s=None, p=0, d=1, ceil_mode=False, return_indices=False, out=None):
+    """MaxPool2d with ceil mode and argmax indices (PyTorch's options; not on the
+    pages).  Returns out, or (out, indices int64) with return_indices."""
+    s = k if s is None else s
+    dev = _device_of(x)
+    xd = _dev(x, "x", dev)
+    N, Cc, H, W = xd.shape
+    Ho, Wo = fw_maxpool2d_out_shape_ex(H, W, k, s, p, d, ceil_mode)
+    od = out if out is not None else torch.empty((N, Cc, Ho, Wo), device=dev, dtype=torch.float32)
+    idx = torch.empty((N, Cc, Ho, Wo), device=dev, dtype=torch.int64) if return_indices else None
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    with torch.cuda.device(dev):
+        _check(lib().fw_maxpool2d_ex(_ptr(xd), N, Cc, H, W, k, s, p, d, int(bool(ceil_mode)), _ptr(od), _ptr(idx),
+                                     C.c_void_p(stream)), "fw_maxpool2d_ex")
+    return (od, idx) if return_indices else od

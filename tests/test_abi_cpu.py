@@ -59,6 +59,15 @@ def test_convt_shape_matches_oracle(H, k, s, p, op):
     assert FW.fw_convt_out_shape(H, H, k, s, p, op) == (want, want)
 
 
+@pytest.mark.parametrize("H,k,s,p,d", [(5, 2, 2, 0, 1), (4, 2, 3, 1, 1), (13, 3, 2, 1, 2), (6, 3, 2, 1, 1),
+                                       (1, 2, 2, 0, 1), (512, 4, 1, 1, 1), (7, 4, 3, 2, 1)])
+def test_maxpool_ceil_shape_matches_oracle(H, k, s, p, d):
+    assert FW.fw_maxpool2d_out_shape_ex(H, H + 2, k, s, p, d, True) == (O.pool_out_size_ceil(H, k, s, p, d),
+                                                                         O.pool_out_size_ceil(H + 2, k, s, p, d))
+    if H + 2 * p - d * (k - 1) - 1 >= 0:  # floor mode has a window
+        assert FW.fw_maxpool2d_out_shape_ex(H, H, k, s, p, d, False) == FW.fw_maxpool2d_out_shape(H, H, k, s, p, d)
+
+
 def test_shape_errors():
     L = FW.lib()
     a, b = C.c_int(), C.c_int()
@@ -132,6 +141,12 @@ def test_operator_argument_errors_without_launch():
     assert ctu(Cin=12) == 6
     assert ctu(s=3) == 6
     assert FW.fw_convt_unfused_workspace_size(1, 64, 8, 8, 128, 4, 2, 1, 2) == 0  # op >= s
+    # maxpool with ceil mode / indices
+    assert L.fw_maxpool2d_ex(x, 1, 1, 8, 8, 2, 2, 0, 1, 1, o, P(0x50000004), None) == 5  # indices not 8-aligned
+    assert L.fw_maxpool2d_ex(x, 1, 1, 8, 8, 2, 2, 0, 1, 1, o, P(0x40000000 + 8), None) == 4  # indices overlap out
+    assert L.fw_maxpool2d_ex(x, 1, 1, 8, 8, 2, 2, 0, 1, 1, o, P(0x10000 + 8), None) == 4  # indices overlap x
+    assert L.fw_maxpool2d_ex(x, 1, 1, 2, 2, 4, 2, 0, 1, 1, o, None, None) == 2  # output size < 1
+    assert L.fw_maxpool2d_ex(None, 1, 1, 8, 8, 2, 2, 0, 1, 0, o, None, None) == 1
     # the bounded-wait self-test checks its limit before launching
     assert L.fw_selftest_bounded_wait(0, None) == 3
     assert L.fw_selftest_bounded_wait(2_000_001, None) == 3
