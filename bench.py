@@ -324,8 +324,15 @@ def run_gpu(args):
         def op_cp(src, out):
             FW.fw_conv2d_tanh_scale_bias_maxpool(src[("cp", "x")], src[("cp", "w")], src[("cp", "conv_b")],
                                                  src[("cp", "bias")], CP["scale"], 4, out=out)
+        hws_cp = torch.empty(FW.lib().fw_conv2d_tanh_scale_bias_maxpool_host_workspace_size(
+            n, CP["Cin"], CP["H"], CP["W"], CP["Cout"], 3, 3, 4, 4) // 4 + 64, device=dev)
+
+        def host_cp():  # C-ABI host-buffer call: pipelined H2D copies, kernels, D2H copies
+            FW.fw_conv2d_tanh_scale_bias_maxpool_host(pinned[("cp", "x")], pinned[("cp", "w")],
+                                                      pinned[("cp", "conv_b")], pinned[("cp", "bias")], CP["scale"],
+                                                      4, out=h_cp, workspace=hws_cp)
         specs.append(dict(name="convpool", work=cp_flops(N=n), unit="TFLOP/s", scale=1e12, bound="tensor",
-                          run=lambda: op_cp(d, out_cp), e2e=lambda: op_cp(pinned, h_cp), out=h_cp,
+                          run=lambda: op_cp(d, out_cp), e2e=lambda: host_cp(), out=h_cp,
                           kernel="convpool_tc_kernel<4,64> (tcgen05 kind::tf32, 3xTF32 split as two MMAs "
                                  "per tap, N = 128 [w_hi|w_lo] and N = 64: executed tensor FLOPs = 3 x "
                                  "algorithmic)", source="convpool_tc.cu"))
@@ -336,8 +343,13 @@ def run_gpu(args):
 
         def op_mp(src, out):
             FW.fw_maxpool2d(src[("mp", "x")], 4, 1, 1, 1, out=out)
+        hws_mp = torch.empty(FW.lib().fw_maxpool2d_host_workspace_size(n, MP["C"], MP["H"], MP["W"], 4, 1, 1, 1)
+                             // 4 + 64, device=dev)
+
+        def host_mp():
+            FW.fw_maxpool2d_host(pinned[("mp", "x")], 4, 1, 1, 1, out=h_mp, workspace=hws_mp)
         specs.append(dict(name="maxpool", work=mp_bytes(N=n), unit="GB/s", scale=1e9, bound="hbm",
-                          run=lambda: op_mp(d, out_mp), e2e=lambda: op_mp(pinned, h_mp), out=h_mp,
+                          run=lambda: op_mp(d, out_mp), e2e=lambda: host_mp(), out=h_mp,
                           kernel="maxpool_s1_stream_kernel<4,1>", source="maxpool.cu"))
     if ct:
         n = ct["x"].shape[0]
@@ -350,8 +362,15 @@ def run_gpu(args):
             FW.fw_convtranspose2d_softmax_bias_scale_sigmoid(src[("ct", "x")], src[("ct", "w")],
                                                              src[("ct", "conv_b")], src[("ct", "bias")],
                                                              CT["scale"], out=out, workspace=wsp)
+        hws_ct = torch.empty(FW.lib().fw_convtranspose2d_softmax_bias_scale_sigmoid_host_workspace_size(
+            n, CT["Cin"], CT["H"], CT["W"], CT["Cout"], 4, 2, 1, 1) // 4 + 64, device=dev)
+
+        def host_ct():
+            FW.fw_convtranspose2d_softmax_bias_scale_sigmoid_host(
+                pinned[("ct", "x")], pinned[("ct", "w")], pinned[("ct", "conv_b")], pinned[("ct", "bias")],
+                CT["scale"], out=h_ct, workspace=hws_ct)
         specs.append(dict(name="convt", work=ct_flops(N=n), unit="TFLOP/s", scale=1e12, bound="tensor",
-                          run=lambda: op_ct(d, out_ct), e2e=lambda: op_ct(pinned, h_ct), out=h_ct,
+                          run=lambda: op_ct(d, out_ct), e2e=lambda: host_ct(), out=h_ct,
                           kernel="convt_k4s2_tc_kernel<16> (tcgen05 kind::tf32) + weight prepack",
                           source="convt_tc.cu"))
 
@@ -508,7 +527,8 @@ def run_gpu(args):
         "e2e": {"value": weak_value(hs["work"], ws, hems) / hs["scale"], "unit": hs["unit"],
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ops_ms": {sp["name"]: e for sp, e in zip(specs, e2e_ms)},
-                "note": "public API with pinned host tensors: H2D copy, kernels, D2H copy of each op's result"},
+                "note": "C-ABI host-buffer calls (fw_*_host) on pinned host tensors: per op, chunked H2D copies, "
+                        "kernels and D2H copies pipelined on copy streams; timed until the result is in host memory"},
         "gpu_launches": launches, "launches_per_step": launches / args.steps,
         "clocks": clk.summary(), "device": props.name,
     })

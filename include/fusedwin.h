@@ -199,6 +199,42 @@ fw_status fw_convtranspose2d_softmax_bias_scale_sigmoid_noalloc(const float *x, 
                                                                 const float *bias, float scale, float *out,
                                                                 void *stream);
 
+/* ------------------------------------------------------- host-buffer calls */
+
+/*
+ * The three operators on tensors in host memory (page-locked for the copies to
+ * overlap; pageable memory works, more slowly).  x, w, conv_b, bias and out are
+ * HOST pointers with the layouts of the device calls above; `workspace` is
+ * caller-owned DEVICE memory of at least the matching *_host_workspace_size
+ * bytes, 256-byte aligned, holding the device copies of the inputs and output
+ * (and the conv-transpose weight rewrite).  The batch is split into up to 8
+ * chunks of images; each chunk's host->device copy, operator launch (on
+ * `stream`, through the device entry point above, so the same checks and kernels
+ * apply) and device->host copy are pipelined on two copy streams the library
+ * creates once per device, so copies overlap the kernels of neighbouring chunks.
+ * The call is ordered after earlier work on `stream`, and later work on `stream`
+ * (e.g. a synchronisation) runs after the last output copy: out is complete once
+ * `stream` is synchronised.  Calls serialise on a host lock while they enqueue;
+ * two calls in flight at once must not share a workspace or host buffers.
+ */
+fw_status fw_conv2d_tanh_scale_bias_maxpool_host(const float *x, int N, int Cin, int H, int W, const float *w,
+                                                 const float *conv_b, int Cout, int KH, int KW, float scale,
+                                                 const float *bias, int pool_k, int pool_s, float *out,
+                                                 void *workspace, unsigned long long workspace_bytes, void *stream);
+unsigned long long fw_conv2d_tanh_scale_bias_maxpool_host_workspace_size(int N, int Cin, int H, int W, int Cout,
+                                                                         int KH, int KW, int pool_k, int pool_s);
+fw_status fw_maxpool2d_host(const float *x, int N, int C, int H, int W, int k, int s, int p, int d, float *out,
+                            void *workspace, unsigned long long workspace_bytes, void *stream);
+unsigned long long fw_maxpool2d_host_workspace_size(int N, int C, int H, int W, int k, int s, int p, int d);
+fw_status fw_convtranspose2d_softmax_bias_scale_sigmoid_host(const float *x, int N, int Cin, int H, int W,
+                                                             const float *w, const float *conv_b, int Cout, int k,
+                                                             int s, int p, int op, const float *bias, float scale,
+                                                             float *out, void *workspace,
+                                                             unsigned long long workspace_bytes, void *stream);
+unsigned long long fw_convtranspose2d_softmax_bias_scale_sigmoid_host_workspace_size(int N, int Cin, int H, int W,
+                                                                                     int Cout, int k, int s, int p,
+                                                                                     int op);
+
 /* ------------------------------------------------------ unfused comparison */
 
 /*

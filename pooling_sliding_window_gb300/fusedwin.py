@@ -32,7 +32,11 @@ EXPORTS = ("fw_status_string", "fw_version", "fw_conv2d_pool_out_shape", "fw_max
            "fw_convtranspose2d_softmax_bias_scale_sigmoid_noalloc",
            "fw_conv2d_tanh_scale_bias_maxpool_unfused", "fw_conv2d_pool_unfused_workspace_size",
            "fw_convtranspose2d_softmax_bias_scale_sigmoid_unfused", "fw_convt_unfused_workspace_size",
-           "fw_maxpool2d_ex", "fw_maxpool2d_out_shape_ex")
+           "fw_maxpool2d_ex", "fw_maxpool2d_out_shape_ex",
+           "fw_conv2d_tanh_scale_bias_maxpool_host", "fw_conv2d_tanh_scale_bias_maxpool_host_workspace_size",
+           "fw_maxpool2d_host", "fw_maxpool2d_host_workspace_size",
+           "fw_convtranspose2d_softmax_bias_scale_sigmoid_host",
+           "fw_convtranspose2d_softmax_bias_scale_sigmoid_host_workspace_size")
 
 
 class FusedWinError(RuntimeError):
@@ -93,6 +97,19 @@ def lib():
         L.fw_maxpool2d_ex.argtypes = [P, I, I, I, I, I, I, I, I, I, P, P, P]
         L.fw_maxpool2d_out_shape_ex.restype = I
         L.fw_maxpool2d_out_shape_ex.argtypes = [I] * 7 + [IP, IP]
+        L.fw_conv2d_tanh_scale_bias_maxpool_host.restype = I
+        L.fw_conv2d_tanh_scale_bias_maxpool_host.argtypes = [P, I, I, I, I, P, P, I, I, I, F, P, I, I, P, P, U64, P]
+        L.fw_conv2d_tanh_scale_bias_maxpool_host_workspace_size.restype = U64
+        L.fw_conv2d_tanh_scale_bias_maxpool_host_workspace_size.argtypes = [I] * 9
+        L.fw_maxpool2d_host.restype = I
+        L.fw_maxpool2d_host.argtypes = [P, I, I, I, I, I, I, I, I, P, P, U64, P]
+        L.fw_maxpool2d_host_workspace_size.restype = U64
+        L.fw_maxpool2d_host_workspace_size.argtypes = [I] * 8
+        L.fw_convtranspose2d_softmax_bias_scale_sigmoid_host.restype = I
+        L.fw_convtranspose2d_softmax_bias_scale_sigmoid_host.argtypes = [
+            P, I, I, I, I, P, P, I, I, I, I, I, P, F, P, P, U64, P]
+        L.fw_convtranspose2d_softmax_bias_scale_sigmoid_host_workspace_size.restype = U64
+        L.fw_convtranspose2d_softmax_bias_scale_sigmoid_host_workspace_size.argtypes = [I] * 9
         _lib = L
     return _lib
 
@@ -344,3 +361,78 @@ def fw_maxpool2d_ex(x, k, s=None, p=0, d=1, ceil_mode=False, return_indices=Fals
         _check(lib().fw_maxpool2d_ex(_ptr(xd), N, Cc, H, W, k, s, p, d, int(bool(ceil_mode)), _ptr(od), _ptr(idx),
                                      C.c_void_p(stream)), "fw_maxpool2d_ex")
     return (od, idx) if return_indices else od
+
+
+# ------------------------------------------------------ host-buffer calls --
+# Host (CPU) tensors in and out, pinned for the copies to overlap; the C call
+# pipelines chunked copies and kernels.  `workspace` is a device tensor (made here
+# when None) of at least the *_host_workspace_size bytes.
+
+def _host(t, name):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or t.device.type != "cpu":
+        raise TypeError(f"{name} must be a float32 CPU tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous (dense NCHW)")
+    return t
+
+
+def _dev_workspace(need, workspace):
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        if not torch.cuda.is_available():
+            raise RuntimeError("libfusedwin needs a CUDA device; none is available")
+        workspace = torch.empty((need + 15) // 16 * 4, device="cuda", dtype=torch.float32)
+    return workspace, workspace.numel() * workspace.element_size()
+
+
+def fw_conv2d_tanh_scale_bias_maxpool_host(x, w, conv_b, bias, scale, pool_k, pool_s=0, out=None, workspace=None,
+                                           stream=None):
+    x, w, conv_b, bias = _host(x, "x"), _host(w, "w"), _host(conv_b, "conv_b"), _host(bias.reshape(-1), "bias")
+    N, Cin, H, W = x.shape
+    Cout, _, KH, KW = w.shape
+    Ho, Wo = fw_conv2d_pool_out_shape(H, W, KH, KW, pool_k, pool_s)
+    out = torch.empty((N, Cout, Ho, Wo), pin_memory=True) if out is None else _host(out, "out")
+    workspace, wsb = _dev_workspace(int(lib().fw_conv2d_tanh_scale_bias_maxpool_host_workspace_size(
+        N, Cin, H, W, Cout, KH, KW, pool_k, pool_s)), workspace)
+    s = torch.cuda.current_stream(workspace.device) if stream is None else stream
+    with torch.cuda.device(workspace.device):
+        _check(lib().fw_conv2d_tanh_scale_bias_maxpool_host(
+            _ptr(x), N, Cin, H, W, _ptr(w), _ptr(conv_b), Cout, KH, KW, float(scale), _ptr(bias), pool_k, pool_s,
+            _ptr(out), _ptr(workspace), wsb, C.c_void_p(s.cuda_stream)), "fw_conv2d_tanh_scale_bias_maxpool_host")
+    s.synchronize()
+    return out
+
+
+def fw_maxpool2d_host(x, k, s=None, p=0, d=1, out=None, workspace=None, stream=None):
+    s = k if s is None else s
+    x = _host(x, "x")
+    N, Cc, H, W = x.shape
+    Ho, Wo = fw_maxpool2d_out_shape(H, W, k, s, p, d)
+    out = torch.empty((N, Cc, Ho, Wo), pin_memory=True) if out is None else _host(out, "out")
+    workspace, wsb = _dev_workspace(int(lib().fw_maxpool2d_host_workspace_size(N, Cc, H, W, k, s, p, d)), workspace)
+    st = torch.cuda.current_stream(workspace.device) if stream is None else stream
+    with torch.cuda.device(workspace.device):
+        _check(lib().fw_maxpool2d_host(_ptr(x), N, Cc, H, W, k, s, p, d, _ptr(out), _ptr(workspace), wsb,
+                                       C.c_void_p(st.cuda_stream)), "fw_maxpool2d_host")
+    st.synchronize()
+    return out
+
+
+def fw_convtranspose2d_softmax_bias_scale_sigmoid_host(x, w, conv_b, bias, scale, stride=2, padding=1,
+                                                       output_padding=1, out=None, workspace=None, stream=None):
+    x, w, conv_b, bias = _host(x, "x"), _host(w, "w"), _host(conv_b, "conv_b"), _host(bias.reshape(-1), "bias")
+    N, Cin, H, W = x.shape
+    _, Cout, K, _ = w.shape
+    Ho, Wo = fw_convt_out_shape(H, W, K, stride, padding, output_padding)
+    out = torch.empty((N, Cout, Ho, Wo), pin_memory=True) if out is None else _host(out, "out")
+    workspace, wsb = _dev_workspace(int(lib().fw_convtranspose2d_softmax_bias_scale_sigmoid_host_workspace_size(
+        N, Cin, H, W, Cout, K, stride, padding, output_padding)), workspace)
+    st = torch.cuda.current_stream(workspace.device) if stream is None else stream
+    with torch.cuda.device(workspace.device):
+        _check(lib().fw_convtranspose2d_softmax_bias_scale_sigmoid_host(
+            _ptr(x), N, Cin, H, W, _ptr(w), _ptr(conv_b), Cout, K, stride, padding, output_padding, _ptr(bias),
+            float(scale), _ptr(out), _ptr(workspace), wsb, C.c_void_p(st.cuda_stream)),
+            "fw_convtranspose2d_softmax_bias_scale_sigmoid_host")
+    st.synchronize()
+    return out

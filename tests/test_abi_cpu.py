@@ -147,6 +147,15 @@ def test_operator_argument_errors_without_launch():
     assert L.fw_maxpool2d_ex(x, 1, 1, 8, 8, 2, 2, 0, 1, 1, o, P(0x10000 + 8), None) == 4  # indices overlap x
     assert L.fw_maxpool2d_ex(x, 1, 1, 2, 2, 4, 2, 0, 1, 1, o, None, None) == 2  # output size < 1
     assert L.fw_maxpool2d_ex(None, 1, 1, 8, 8, 2, 2, 0, 1, 0, o, None, None) == 1
+    # host-buffer calls: workspace checks before anything is enqueued
+    hn = L.fw_maxpool2d_host_workspace_size(2, 3, 16, 16, 2, 2, 0, 1)
+    assert hn == 2 * 3 * 16 * 16 * 4 + 2 * 3 * 8 * 8 * 4  # both parts already 256-byte multiples
+    assert L.fw_maxpool2d_host(x, 2, 3, 16, 16, 2, 2, 0, 1, o, None, hn, None) == 1
+    assert L.fw_maxpool2d_host(x, 2, 3, 16, 16, 2, 2, 0, 1, o, big, hn - 1, None) == 1
+    assert L.fw_maxpool2d_host(x, 2, 3, 16, 16, 2, 2, 0, 1, o, P(0x100000010), hn, None) == 5
+    assert L.fw_maxpool2d_host(x, 2, 3, 1, 1, 2, 2, 0, 1, o, big, hn, None) == 2
+    assert L.fw_conv2d_tanh_scale_bias_maxpool_host_workspace_size(1, 8, 2, 2, 4, 3, 3, 4, 4) == 0
+    assert L.fw_convtranspose2d_softmax_bias_scale_sigmoid_host_workspace_size(1, 4, 4, 4, 8, 4, 2, 1, 2) == 0
     # the bounded-wait self-test checks its limit before launching
     assert L.fw_selftest_bounded_wait(0, None) == 3
     assert L.fw_selftest_bounded_wait(2_000_001, None) == 3
