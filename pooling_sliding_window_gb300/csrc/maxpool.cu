@@ -278,6 +278,192 @@ __global__ void __launch_bounds__(256) maxpool_direct_ex_kernel(const float *__r
     }
 }
 
+// The definition's window maximum for one output with any stride and dilation.
+__device__ __noinline__ float window_max_exact_sd(const float *__restrict__ plane, int H, int W, int k, int s, int p,
+                                                  int d, int oh, int ow) {
+    float m = -INFINITY;
+    for (int i = 0; i < k; ++i) {
+        const int ih = oh * s - p + i * d;
+        for (int j = 0; j < k; ++j) {
+            const int iw = ow * s - p + j * d;
+            const float v = (ih >= 0 && ih < H && iw >= 0 && iw < W) ? __ldg(plane + (long long)ih * W + iw) : -INFINITY;
+            m = max_update(m, v);
+        }
+    }
+    return m;
+}
+
+// Streaming kernel for stride S and dilation D (S > 1 or D > 1): the same bulk-copy
+// row ring and -inf guards as the stride-1 kernel.  Thread t owns output columns
+// [4t, 4t+4), whose taps span the SPAN input columns from 4tS - P; it reads them
+// with aligned float4 loads and takes the horizontal maxima (taps D apart, outputs
+// S apart).  The last R = (K-1)D + 1 row maxima stay in a register ring; input row
+// ir completes output row oh when ir = oh*S - P + (K-1)D.
+template <int K, int S, int D, int P>
+__global__ void __launch_bounds__(512) maxpool_stream_sd_kernel(const float *__restrict__ x, float *__restrict__ out,
+                                                                int H, int W, int Ho, int Wo, int band, int nbands,
+                                                                int rps, int pitch) {
+    constexpr int SPAN = 3 * S + (K - 1) * D + 1;    // input columns of 4 outputs
+    constexpr int R = (K - 1) * D + 1;               // rows a window spans
+    constexpr int OFF = (4 - P % 4) % 4;             // span start - aligned load start
+    constexpr int NQ = (OFF + SPAN + 3) / 4;         // float4 loads per row
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem_raw);
+    float *ring = reinterpret_cast<float *>(smem_raw + 64);  // NSTAGE * rps rows
+    float *ostage = ring + (size_t)NSTAGE * rps * pitch;    // 128 floats per warp
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const long long plane = blockIdx.x / nbands;
+    const int b = blockIdx.x - (int)(plane * nbands);
+    const int r0 = b * band, r1 = min(Ho, r0 + band);                    // output rows [r0, r1)
+    const int ir_begin = r0 * S - P, ir_end = (r1 - 1) * S - P + (K - 1) * D;  // input rows [.., ir_end]
+    const int la = max(0, ir_begin), lb = min(H, ir_end + 1);            // of them, inside the plane
+    const int nrows = max(0, lb - la);
+    const int nst = (nrows + rps - 1) / rps;
+    const float *src = x + plane * (long long)H * W;
+    float *dst = out + plane * (long long)Ho * Wo;
+
+    const int nguard = pitch - W;
+    for (int i = tid; i < NSTAGE * rps * nguard; i += blockDim.x) {
+        const int row = i / nguard, g = i % nguard;
+        ring[(size_t)row * pitch + (g < GUARD ? g : W + g)] = -INFINITY;
+    }
+    if (tid == 0) {
+        for (int st = 0; st < NSTAGE; ++st) mbar_init(smem_u32(&bars[st]), 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    auto issue = [&](int st) {  // thread 0 only: copy stage `st` into its slot
+        const int slot = st % NSTAGE;
+        const int row0 = la + st * rps, cnt = min(rps, lb - row0);
+        const uint32_t bar = smem_u32(&bars[slot]);
+        const uint32_t row_bytes = (uint32_t)W * 4u;
+        mbar_arrive_expect_tx(bar, row_bytes * cnt);
+        for (int r = 0; r < cnt; ++r)
+            bulk_g2s(smem_u32(ring + ((size_t)slot * rps + r) * pitch + GUARD), src + (long long)(row0 + r) * W,
+                     row_bytes, bar);
+    };
+    if (tid == 0) {
+        fence_proxy_async_smem();
+        for (int st = 0; st < min(NSTAGE, nst); ++st) issue(st);
+    }
+
+    float4 hist[R];
+#pragma unroll
+    for (int i = 0; i < R; ++i) hist[i] = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    const int a0 = GUARD + 4 * tid * S - P - OFF;  // aligned first column this thread loads
+    bool err = false, any_err = false;
+    int st = 0, r_in_st = 0, st_rows = min(rps, lb - la);
+    for (int base = ir_begin; base <= ir_end && !any_err; base += R) {
+#pragma unroll
+        for (int u = 0; u < R; ++u) {
+            const int ir = base + u;
+            if (ir > ir_end) break;
+            float4 h = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            if (ir >= la && ir < lb) {
+                const int slot = st % NSTAGE;
+                if (r_in_st == 0 && !mbar_wait_bounded(smem_u32(&bars[slot]), (uint32_t)(st / NSTAGE) & 1u))
+                    err = true;
+                const float *row = ring + ((size_t)slot * rps + r_in_st) * pitch + a0;
+                float v[4 * NQ];
+#pragma unroll
+                for (int q = 0; q < NQ; ++q) {
+                    const float4 f = *reinterpret_cast<const float4 *>(row + 4 * q);
+                    v[4 * q] = f.x;
+                    v[4 * q + 1] = f.y;
+                    v[4 * q + 2] = f.z;
+                    v[4 * q + 3] = f.w;
+                }
+                float hv[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    float m = v[OFF + j * S];
+#pragma unroll
+                    for (int i = 1; i < K; ++i) m = max_nan(m, v[OFF + j * S + i * D]);
+                    hv[j] = m;
+                }
+                h = make_float4(hv[0], hv[1], hv[2], hv[3]);
+                if (++r_in_st == st_rows) {  // stage consumed: release the slot, refill it
+                    if (__syncthreads_or(err)) {
+                        if (tid == 0) atomicOr(&g_err_maxpool, DEVERR_TIMEOUT);
+                        any_err = true;
+                        break;
+                    }
+                    if (tid == 0 && st + NSTAGE < nst) {
+                        fence_proxy_async_smem();
+                        issue(st + NSTAGE);
+                    }
+                    ++st;
+                    r_in_st = 0;
+                    st_rows = min(rps, lb - (la + st * rps));
+                }
+            }
+            hist[u] = h;
+            const int t = ir - ir_begin - (K - 1) * D;  // = (oh - r0) * S when this row completes output row oh
+            if (t >= 0 && t % S == 0) {
+                const int oh = r0 + t / S;
+                if (oh < r1) {
+                    float4 m = hist[((u - (K - 1) * D) % R + R) % R];
+#pragma unroll
+                    for (int i = 1; i < K; ++i) {
+                        const float4 g = hist[((u - (K - 1 - i) * D) % R + R) % R];
+                        m.x = max_nan(m.x, g.x);
+                        m.y = max_nan(m.y, g.y);
+                        m.z = max_nan(m.z, g.z);
+                        m.w = max_nan(m.w, g.w);
+                    }
+                    // a zero maximum: the sign is the first zero's by the definition
+                    if (m.x == 0.f || m.y == 0.f || m.z == 0.f || m.w == 0.f) {
+                        float r[4] = {m.x, m.y, m.z, m.w};
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            if (r[j] == 0.f) r[j] = window_max_exact_sd(src, H, W, K, S, P, D, oh, 4 * tid + j);
+                        m = make_float4(r[0], r[1], r[2], r[3]);
+                    }
+                    float *os = ostage + warp * 128;
+                    __syncwarp();
+                    *reinterpret_cast<float4 *>(os + lane * 4) = m;
+                    __syncwarp();
+                    float *orow = dst + (long long)oh * Wo + warp * 128;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int c = q * 32 + lane;
+                        if (warp * 128 + c < Wo) orow[c] = os[c];
+                    }
+                }
+            }
+        }
+    }
+    if (any_err && tid == 0) {
+        for (int s2 = st; s2 < min(nst, st + NSTAGE); ++s2)
+            mbar_wait_bounded(smem_u32(&bars[s2 % NSTAGE]), (uint32_t)(s2 / NSTAGE) & 1u);
+    }
+}
+
+template <int K, int S, int D, int P>
+fw_status launch_stream_sd(const float *x, float *out, long long NC, int H, int W, int Ho, int Wo, cudaStream_t st) {
+    const int threads = ((Wo + 3) / 4 + 31) / 32 * 32;
+    if (threads > 512) return FW_ERR_UNSUPPORTED;
+    // every column a thread may load: up to 4*threads*S + SPAN past the guard
+    const int pitch = (GUARD + 4 * threads * S + 3 * S + (K - 1) * D + 1 + 8 + 3) / 4 * 4;
+    if (pitch - W < GUARD) return FW_ERR_UNSUPPORTED;
+    const int row_bytes = W * 4;
+    const int rps = max(1, min(8, 12288 / row_bytes));
+    const size_t smem = 64 + (size_t)NSTAGE * rps * pitch * 4 + (size_t)(threads / 32) * 128 * 4;
+    const int band = Ho <= 64 ? Ho : 64;
+    const int nbands = (Ho + band - 1) / band;
+    const long long blocks = NC * nbands;
+    if (blocks > 0x7fffffffLL) return FW_ERR_SHAPE;
+    cudaError_t e = cudaFuncSetAttribute(maxpool_stream_sd_kernel<K, S, D, P>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return launch_status(e);
+    maxpool_stream_sd_kernel<K, S, D, P><<<(unsigned)blocks, threads, smem, st>>>(x, out, H, W, Ho, Wo, band, nbands,
+                                                                                 rps, pitch);
+    note_launch();
+    return launch_status(cudaGetLastError());
+}
+
 template <int K, int P>
 fw_status launch_stream(const float *x, float *out, long long NC, int H, int W, int Ho, int Wo,
                         cudaStream_t st) {
@@ -317,6 +503,16 @@ StreamFn stream_fn(int k, int p) {
     return nullptr;
 }
 
+StreamFn stream_sd_fn(int k, int s, int d, int p) {
+#define FW_MP_SD(KK, SS, DD, PP) \
+    if (k == KK && s == SS && d == DD && p == PP) return launch_stream_sd<KK, SS, DD, PP>;
+    FW_MP_SD(2, 2, 1, 0) FW_MP_SD(2, 2, 1, 1) FW_MP_SD(3, 2, 1, 0) FW_MP_SD(3, 2, 1, 1) FW_MP_SD(4, 2, 1, 1)
+    FW_MP_SD(5, 2, 1, 2) FW_MP_SD(3, 3, 1, 0) FW_MP_SD(3, 3, 1, 1) FW_MP_SD(4, 4, 1, 0) FW_MP_SD(3, 1, 2, 1)
+    FW_MP_SD(3, 1, 2, 2) FW_MP_SD(2, 1, 2, 1)
+#undef FW_MP_SD
+    return nullptr;
+}
+
 }  // namespace
 
 fw_status maxpool2d_launch(const float *x, long long NC, int H, int W, int k, int s, int p, int d,
@@ -324,6 +520,12 @@ fw_status maxpool2d_launch(const float *x, long long NC, int H, int W, int k, in
     const bool aligned = ((reinterpret_cast<uintptr_t>(x) & 15u) == 0);
     if (s == 1 && d == 1 && aligned && W % 4 == 0 && W >= 32 && W <= 2040) {
         if (StreamFn f = stream_fn(k, p)) return f(x, out, NC, H, W, Ho, Wo, st);
+    }
+    if ((s > 1 || d > 1) && aligned && W % 4 == 0 && W >= 32 && W <= 2040) {
+        if (StreamFn f = stream_sd_fn(k, s, d, p)) {
+            const fw_status rc = f(x, out, NC, H, W, Ho, Wo, st);
+            if (rc != FW_ERR_UNSUPPORTED) return rc;
+        }
     }
     const long long total = NC * Ho * Wo;
     const int threads = 256;

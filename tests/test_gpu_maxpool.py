@@ -37,6 +37,23 @@ def test_maxpool_small_bit_exact(case):
     assert_bits_equal(got, want, str(case))
 
 
+# (k, s, d, p) with a strided / dilated streaming kernel
+SD = [(2, 2, 1, 0), (2, 2, 1, 1), (3, 2, 1, 0), (3, 2, 1, 1), (4, 2, 1, 1), (5, 2, 1, 2), (3, 3, 1, 0), (3, 3, 1, 1),
+      (4, 4, 1, 0), (3, 1, 2, 1), (3, 1, 2, 2), (2, 1, 2, 1)]
+
+
+@pytest.mark.parametrize("k,s,d,p", SD)
+def test_strided_dilated_stream_bit_exact(k, s, d, p):
+    for N, C, H, W in ((1, 2, 301, 512), (2, 1, 37, 64), (1, 1, 23, 132)):
+        x = synth.maxpool_inputs(N, C, H, W, seed=k + 10 * s + 100 * d + p + W)["x"]
+        assert_bits_equal(host(FW.fw_maxpool2d(dev(x), k, s, p, d)), O.maxpool2d(x, k, s, p, d),
+                          str((N, C, H, W, k, s, p, d)))
+    rng = np.random.default_rng(k + s + d + p)
+    x = rng.choice(np.array([0.0, -0.0, 1.0, -1.0, np.inf, -np.inf, np.nan, 0.5], np.float32),
+                   size=(1, 2, 29, 64), p=[.3, .3, .1, .1, .04, .04, .02, .1]).astype(np.float32)
+    assert_bits_equal(host(FW.fw_maxpool2d(dev(x), k, s, p, d)), O.maxpool2d(x, k, s, p, d), "special values")
+
+
 def test_maxpool_special_values():
     """Signed zeros, NaN, +-inf: ties keep the first tap, NaN propagates."""
     rng = np.random.default_rng(7)
