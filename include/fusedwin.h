@@ -167,6 +167,22 @@ fw_status fw_convtranspose2d_softmax_bias_scale_sigmoid(const float *x, int N, i
                                                         void *workspace, unsigned long long workspace_bytes,
                                                         void *stream);
 
+/*
+ * Channels-last variant (the l2_p91 trace considers the channels_last memory
+ * format for this model): x [N, H, W, Cin] and out [N, Ho, Wo, Cout], same
+ * weights, workspace (fw_convt_workspace_size), definition and tolerance.  Only
+ * the tensor-core shapes (k = 4, s = 2, p = 1, Cout = 128, Cin in {8, 16, 32, 64});
+ * other valid arguments return FW_ERR_UNSUPPORTED.  x must be 16-byte and out
+ * 32-byte aligned (FW_ERR_ALIGN otherwise).  A pixel's 128 channels are contiguous
+ * in both tensors, so the gather reads 16 bytes per lane and every output store
+ * writes whole 32-byte sectors.
+ */
+fw_status fw_convtranspose2d_softmax_bias_scale_sigmoid_nhwc(const float *x, int N, int Cin, int H, int W,
+                                                             const float *w, const float *conv_b, int Cout, int k,
+                                                             int s, int p, int op, const float *bias, float scale,
+                                                             float *out, void *workspace,
+                                                             unsigned long long workspace_bytes, void *stream);
+
 /* Bytes of device workspace fw_convtranspose2d_softmax_bias_scale_sigmoid
  * needs for these arguments (0 when it needs none). */
 unsigned long long fw_convt_workspace_size(int Cin, int Cout, int k, int s, int p);

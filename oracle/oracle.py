@@ -270,3 +270,12 @@ def convt_fused_pixel(x, w, cb, bias, scale, stride, pad, n, oh, ow):
     _check(lib().oracle_convt_fused_pixel(x, Cin, H, W, w, _ptr_or_null(cb), Cout, K, stride, pad,
                                           bias, scale, n, oh, ow, out))
     return out
+
+
+def convtranspose2d_softmax_bias_scale_sigmoid_nhwc(x_nhwc, w, cb, bias, scale, stride=2, pad=1, output_padding=1):
+    """Channels-last layout of the same model: x [N, H, W, Cin] -> out [N, Ho, Wo, Cout].
+    A layout change only -- the definition is the NCHW function above, with the
+    activations transposed in and out."""
+    x = np.ascontiguousarray(np.transpose(np.asarray(x_nhwc, dtype=np.float32), (0, 3, 1, 2)))
+    out = convtranspose2d_softmax_bias_scale_sigmoid(x, w, cb, bias, scale, stride, pad, output_padding)
+    return np.ascontiguousarray(np.transpose(out, (0, 2, 3, 1)))

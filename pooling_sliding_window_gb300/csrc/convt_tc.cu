@@ -104,6 +104,13 @@ __host__ __device__ inline size_t tc_smem_bytes(int G, int L) {
     return (size_t)4 * G * COUT * 16 + (size_t)NSTAGE * G * L * 16 + 2 * COUT * 4 + sizeof(Bars);
 }
 
+// One 256-bit store (8 floats, 32-byte aligned address): a whole L2 sector.
+__device__ __forceinline__ void st_global_v8(float *p, const float *v) {
+    asm volatile("st.global.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "f"(v[0]), "f"(v[1]), "f"(v[2]),
+                 "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7])
+                 : "memory");
+}
+
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -116,7 +123,10 @@ __device__ __forceinline__ float ex2_approx(float x) {
 // RAW = false: the fused operator.  RAW = true: the first kernel of the unfused
 // comparison path -- `out` receives the conv-transpose output y (+ conv_b) for every
 // output pixel and channel; scale and bias are unused.
-template <int G, bool RAW>  // G = input channels / 4
+// NHWC = true: x is [N, H, W, Cin] and out [N, Ho, Wo, Cout] (channels last); the
+// gather then loads 4 channels per lane with one 16-byte load, and each epilogue
+// thread writes its pixel's 128 channels as 256-bit stores (whole 32-byte sectors).
+template <int G, bool RAW, bool NHWC = false>  // G = input channels / 4
 __global__ void __launch_bounds__(NTHREADS, 1)
 convt_k4s2_tc_kernel(const float *__restrict__ x, const float *__restrict__ wtc, const float *__restrict__ cb,
                      const float *__restrict__ bias, float scale, float *__restrict__ out, int N, int H, int W,
@@ -186,7 +196,58 @@ convt_k4s2_tc_kernel(const float *__restrict__ x, const float *__restrict__ wtc,
                 const long long pbase = (long long)tile * MT + BW + (long long)dy_lo * BW + dx0;
                 unsigned char *slab = sSlab + stage * slab_bytes;
                 bool waited = use == 0;
-                for (int pos = tid; pos < L; pos += PROD_WARPS * 32) {
+                if constexpr (NHWC) {
+                    // G lanes per position, lane g loading channels 4g..4g+3 (16 bytes);
+                    // PPP positions per pass, NB passes in flight per batch.
+                    constexpr int PPP = PROD_WARPS * 32 / G, NB = 14;
+                    const int g = tid % G, pslot = tid / G;
+                    for (int b0 = 0; b0 < L; b0 += PPP * NB) {
+                        float4 r[NB];
+                        // decode the batch's first position once, then step PPP positions
+                        // at a time (row / image carries instead of divisions)
+                        long long q = pbase + b0 + pslot;
+                        int R, c;
+                        if (n_pos < 0x7fffffffLL) {
+                            R = (int)q / BW;
+                            c = (int)q - R * BW;
+                        } else {
+                            R = (int)(q / BW);
+                            c = (int)(q - (long long)R * BW);
+                        }
+                        int n = R > 0 ? (R - 1) / BH : 0;
+                        int row = R > 0 ? R - 1 - n * BH : -1;  // -1: the zero row above image 0
+#pragma unroll
+                        for (int j = 0; j < NB; ++j) {
+                            const int pos = b0 + pslot + PPP * j;
+                            r[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                            if (pos < L && q >= 0 && q < n_pos && c >= 0 && c < W && row >= 0 && row < H)
+                                r[j] = __ldg(reinterpret_cast<const float4 *>(
+                                    x + (((long long)n * H + row) * W + c) * CIN + 4 * g));
+                            q += PPP;
+                            c += PPP;
+                            while (c >= BW) {
+                                c -= BW;
+                                if (++row == BH) {
+                                    row = 0;
+                                    ++n;
+                                }
+                            }
+                        }
+                        if (!waited) {
+                            if (!mbar_wait_bounded(smem_u32(&bars.slab_empty[stage]), (use - 1) & 1)) fail();
+                            waited = true;
+                        }
+#pragma unroll
+                        for (int j = 0; j < NB; ++j) {
+                            const int pos = b0 + pslot + PPP * j;
+                            if (pos < L)
+                                *reinterpret_cast<float4 *>(slab + g * slab_plane + pos * 16) =
+                                    make_float4(tc::to_tf32(r[j].x), tc::to_tf32(r[j].y), tc::to_tf32(r[j].z),
+                                                tc::to_tf32(r[j].w));
+                        }
+                    }
+                }
+                for (int pos = NHWC ? L : tid; pos < L; pos += PROD_WARPS * 32) {
                     const long long q = pbase + pos;
                     const float *src = nullptr;
                     if (q >= 0 && q < n_pos) {
@@ -325,7 +386,8 @@ convt_k4s2_tc_kernel(const float *__restrict__ x, const float *__restrict__ wtc,
             const int m = rem / BW, nn = rem - m * BW;
             const int oh = 2 * m + py, ow = 2 * nn + px;
             const bool valid = a < n_anchor && oh < Ho && ow < Wo;
-            float *o = out + (n * COUT) * plane_out + (long long)oh * Wo + ow;
+            float *o = NHWC ? out + ((n * Ho + oh) * (long long)Wo + ow) * COUT
+                            : out + (n * COUT) * plane_out + (long long)oh * Wo + ow;
             if constexpr (RAW) {
                 // y = z * ln(2): the accumulator holds (conv-transpose + conv_b) * log2(e)
 #pragma unroll 2
@@ -377,14 +439,27 @@ convt_k4s2_tc_kernel(const float *__restrict__ x, const float *__restrict__ wtc,
                 tc::ld32(taddr + 32 * c, v);
                 tc::wait_ld();
                 if (valid) {
+                    if constexpr (NHWC) {
 #pragma unroll
-                    for (int i = 0; i < 32; i += 4) {
-                        const float4 kb = kb4[8 * c + i / 4];
-                        float *oc = o + (32 * c + i) * plane_out;
-                        oc[0] = __fdividef(1.f, 1.f + ex2_approx(fmaf(v[i], kp, kb.x)));
-                        oc[plane_out] = __fdividef(1.f, 1.f + ex2_approx(fmaf(v[i + 1], kp, kb.y)));
-                        oc[2 * plane_out] = __fdividef(1.f, 1.f + ex2_approx(fmaf(v[i + 2], kp, kb.z)));
-                        oc[3 * plane_out] = __fdividef(1.f, 1.f + ex2_approx(fmaf(v[i + 3], kp, kb.w)));
+                        for (int i = 0; i < 32; i += 4) {
+                            const float4 kb = kb4[8 * c + i / 4];
+                            v[i] = __fdividef(1.f, 1.f + ex2_approx(fmaf(v[i], kp, kb.x)));
+                            v[i + 1] = __fdividef(1.f, 1.f + ex2_approx(fmaf(v[i + 1], kp, kb.y)));
+                            v[i + 2] = __fdividef(1.f, 1.f + ex2_approx(fmaf(v[i + 2], kp, kb.z)));
+                            v[i + 3] = __fdividef(1.f, 1.f + ex2_approx(fmaf(v[i + 3], kp, kb.w)));
+                        }
+#pragma unroll
+                        for (int i = 0; i < 32; i += 8) st_global_v8(o + 32 * c + i, v + i);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4) {
+                            const float4 kb = kb4[8 * c + i / 4];
+                            float *oc = o + (32 * c + i) * plane_out;
+                            oc[0] = __fdividef(1.f, 1.f + ex2_approx(fmaf(v[i], kp, kb.x)));
+                            oc[plane_out] = __fdividef(1.f, 1.f + ex2_approx(fmaf(v[i + 1], kp, kb.y)));
+                            oc[2 * plane_out] = __fdividef(1.f, 1.f + ex2_approx(fmaf(v[i + 2], kp, kb.z)));
+                            oc[3 * plane_out] = __fdividef(1.f, 1.f + ex2_approx(fmaf(v[i + 3], kp, kb.w)));
+                        }
                     }
                 }
                 reset_chunk(c);
@@ -404,7 +479,7 @@ convt_k4s2_tc_kernel(const float *__restrict__ x, const float *__restrict__ wtc,
     }
 }
 
-template <int G, bool RAW>
+template <int G, bool RAW, bool NHWC>
 fw_status launch_g(const float *x, int N, int H, int W, const float *wtc, const float *cb, const float *bias,
                    float scale, float *out, int Ho, int Wo, cudaStream_t st) {
     int dev = 0, sms = 0, optin = 0;
@@ -414,6 +489,7 @@ fw_status launch_g(const float *x, int N, int H, int W, const float *wtc, const 
         return FW_ERR_LAUNCH;
     const size_t limit = (size_t)optin < SMEM_LIMIT ? (size_t)optin : SMEM_LIMIT;
     int nslab = 1, L = MT + 1 + (W + 1);
+    if (NHWC) L |= 1;  // an odd plane stride (in 16-byte units) spreads the gather's stores over the banks
     size_t smem = tc_smem_bytes(G, L);
     if (smem > limit) {
         nslab = 2;
@@ -422,13 +498,13 @@ fw_status launch_g(const float *x, int N, int H, int W, const float *wtc, const 
     }
     if (smem > limit) return FW_ERR_UNSUPPORTED;
     if (smem < MIN_SMEM) smem = MIN_SMEM;
-    cudaError_t e = cudaFuncSetAttribute(convt_k4s2_tc_kernel<G, RAW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(convt_k4s2_tc_kernel<G, RAW, NHWC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return launch_status(e);
     const long long tiles = ((long long)N * (H + 1) * (W + 1) + MT - 1) / MT;
     int per_phase = sms / 4 > 0 ? sms / 4 : 1;
     if (per_phase > tiles) per_phase = (int)tiles;
-    convt_k4s2_tc_kernel<G, RAW><<<4 * per_phase, NTHREADS, smem, st>>>(x, wtc, cb, bias, scale, out, N, H, W, Ho, Wo,
+    convt_k4s2_tc_kernel<G, RAW, NHWC><<<4 * per_phase, NTHREADS, smem, st>>>(x, wtc, cb, bias, scale, out, N, H, W, Ho, Wo,
                                                                    nslab, L);
     note_launch();
     return launch_status(cudaGetLastError());
@@ -442,7 +518,7 @@ bool convt_tc_eligible(int Cin, int Cout, int k, int s, int p) {
 
 namespace {
 
-template <bool RAW>
+template <bool RAW, bool NHWC = false>
 fw_status tc_launch(const float *x, int N, int Cin, int H, int W, const float *w, const float *cb,
                     const float *bias, float scale, float *out, int Ho, int Wo, void *ws, cudaStream_t st) {
     float *wtc = static_cast<float *>(ws);
@@ -452,10 +528,10 @@ fw_status tc_launch(const float *x, int N, int Cin, int H, int W, const float *w
     fw_status rc = launch_status(cudaGetLastError());
     if (rc != FW_OK) return rc;
     switch (Cin) {
-        case 8: return launch_g<2, RAW>(x, N, H, W, wtc, cb, bias, scale, out, Ho, Wo, st);
-        case 16: return launch_g<4, RAW>(x, N, H, W, wtc, cb, bias, scale, out, Ho, Wo, st);
-        case 32: return launch_g<8, RAW>(x, N, H, W, wtc, cb, bias, scale, out, Ho, Wo, st);
-        case 64: return launch_g<16, RAW>(x, N, H, W, wtc, cb, bias, scale, out, Ho, Wo, st);
+        case 8: return launch_g<2, RAW, NHWC>(x, N, H, W, wtc, cb, bias, scale, out, Ho, Wo, st);
+        case 16: return launch_g<4, RAW, NHWC>(x, N, H, W, wtc, cb, bias, scale, out, Ho, Wo, st);
+        case 32: return launch_g<8, RAW, NHWC>(x, N, H, W, wtc, cb, bias, scale, out, Ho, Wo, st);
+        case 64: return launch_g<16, RAW, NHWC>(x, N, H, W, wtc, cb, bias, scale, out, Ho, Wo, st);
     }
     return FW_ERR_UNSUPPORTED;
 }
@@ -495,6 +571,12 @@ __global__ void __launch_bounds__(256) softmax_bias_scale_sigmoid_kernel(const f
 fw_status convt_tc_launch(const float *x, int N, int Cin, int H, int W, const float *w, const float *cb,
                           const float *bias, float scale, float *out, int Ho, int Wo, void *ws, cudaStream_t st) {
     return tc_launch<false>(x, N, Cin, H, W, w, cb, bias, scale, out, Ho, Wo, ws, st);
+}
+
+// Channels-last: x [N, H, W, Cin], out [N, Ho, Wo, 128] (out 32-byte aligned).
+fw_status convt_tc_launch_nhwc(const float *x, int N, int Cin, int H, int W, const float *w, const float *cb,
+                               const float *bias, float scale, float *out, int Ho, int Wo, void *ws, cudaStream_t st) {
+    return tc_launch<false, true>(x, N, Cin, H, W, w, cb, bias, scale, out, Ho, Wo, ws, st);
 }
 
 // Stage 1 of the unfused path: y [N, 128, Ho, Wo] = conv-transpose(x) + conv_b.

@@ -32,6 +32,8 @@ fw_status convt_tc_launch_raw(const float *x, int N, int Cin, int H, int W, cons
                               float *y, int Ho, int Wo, void *ws, cudaStream_t st);
 fw_status softmax_bias_scale_sigmoid_launch(const float *y, int N, int C, int Ho, int Wo, const float *bias,
                                             float scale, float *out, cudaStream_t st);
+fw_status convt_tc_launch_nhwc(const float *x, int N, int Cin, int H, int W, const float *w, const float *cb,
+                               const float *bias, float scale, float *out, int Ho, int Wo, void *ws, cudaStream_t st);
 
 static std::atomic<unsigned long long> g_launches{0};
 
@@ -376,6 +378,36 @@ fw_status fw_convtranspose2d_softmax_bias_scale_sigmoid_unfused(const float *x, 
     rc = convt_tc_launch_raw(x, N, Cin, H, W, w, conv_b, y, Ho, Wo, ws, st);
     if (rc != FW_OK) return rc;
     return softmax_bias_scale_sigmoid_launch(y, N, Cout, Ho, Wo, bias, scale, out, st);
+}
+
+fw_status fw_convtranspose2d_softmax_bias_scale_sigmoid_nhwc(const float *x, int N, int Cin, int H, int W,
+                                                             const float *w, const float *conv_b, int Cout, int k,
+                                                             int s, int p, int op, const float *bias, float scale,
+                                                             float *out, void *workspace,
+                                                             unsigned long long workspace_bytes, void *stream) {
+    if (!x || !w || !bias || !out) return FW_ERR_NULL;
+    if (N < 1 || Cin < 1 || Cout < 1) return FW_ERR_SHAPE;
+    if (!std::isfinite(scale)) return FW_ERR_PARAM;
+    int Ho = 0, Wo = 0;
+    fw_status rc = convt_shape(H, W, k, s, p, op, &Ho, &Wo);
+    if (rc != FW_OK) return rc;
+    if (misaligned(w) || misaligned(conv_b) || misaligned(bias) || (reinterpret_cast<uintptr_t>(x) & 15u) != 0 ||
+        (reinterpret_cast<uintptr_t>(out) & 31u) != 0)
+        return FW_ERR_ALIGN;
+    if (!convt_tc_eligible(Cin, Cout, k, s, p)) return FW_ERR_UNSUPPORTED;
+    const long long nx = prod({N, H, W, Cin}), nw = prod({Cin, Cout, k, k}), no = prod({N, Ho, Wo, Cout});
+    if (nx < 0 || nw < 0 || no < 0) return FW_ERR_SHAPE;
+    const unsigned long long need = convt_workspace_bytes(Cin, Cout, k, s, p);
+    if (!workspace || workspace_bytes < need) return FW_ERR_NULL;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 15u) != 0) return FW_ERR_ALIGN;
+    const long long ob = no * 4, wb = (long long)need;
+    const void *ins[] = {x, w, bias, conv_b};
+    const long long insz[] = {nx * 4, nw * 4, 4LL * Cout, 4LL * Cout};
+    for (int i = 0; i < 4; ++i)
+        if (overlaps(out, ob, ins[i], insz[i]) || overlaps(workspace, wb, ins[i], insz[i])) return FW_ERR_ALIAS;
+    if (overlaps(out, ob, workspace, wb)) return FW_ERR_ALIAS;
+    return convt_tc_launch_nhwc(x, N, Cin, H, W, w, conv_b, bias, scale, out, Ho, Wo, workspace,
+                                static_cast<cudaStream_t>(stream));
 }
 
 fw_status fw_selftest_bounded_wait(unsigned int limit_us, void *stream) {

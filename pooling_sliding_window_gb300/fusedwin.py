@@ -36,7 +36,8 @@ EXPORTS = ("fw_status_string", "fw_version", "fw_conv2d_pool_out_shape", "fw_max
            "fw_conv2d_tanh_scale_bias_maxpool_host", "fw_conv2d_tanh_scale_bias_maxpool_host_workspace_size",
            "fw_maxpool2d_host", "fw_maxpool2d_host_workspace_size",
            "fw_convtranspose2d_softmax_bias_scale_sigmoid_host",
-           "fw_convtranspose2d_softmax_bias_scale_sigmoid_host_workspace_size")
+           "fw_convtranspose2d_softmax_bias_scale_sigmoid_host_workspace_size",
+           "fw_convtranspose2d_softmax_bias_scale_sigmoid_nhwc")
 
 
 class FusedWinError(RuntimeError):
@@ -110,6 +111,9 @@ def lib():
             P, I, I, I, I, P, P, I, I, I, I, I, P, F, P, P, U64, P]
         L.fw_convtranspose2d_softmax_bias_scale_sigmoid_host_workspace_size.restype = U64
         L.fw_convtranspose2d_softmax_bias_scale_sigmoid_host_workspace_size.argtypes = [I] * 9
+        L.fw_convtranspose2d_softmax_bias_scale_sigmoid_nhwc.restype = I
+        L.fw_convtranspose2d_softmax_bias_scale_sigmoid_nhwc.argtypes = [
+            P, I, I, I, I, P, P, I, I, I, I, I, P, F, P, P, U64, P]
         _lib = L
     return _lib
 
@@ -436,3 +440,28 @@ def fw_convtranspose2d_softmax_bias_scale_sigmoid_host(x, w, conv_b, bias, scale
             "fw_convtranspose2d_softmax_bias_scale_sigmoid_host")
     st.synchronize()
     return out
+
+
+# -------------------------------------------------------- channels last --
+
+def fw_convtranspose2d_softmax_bias_scale_sigmoid_nhwc(x, w, conv_b, bias, scale, stride=2, padding=1,
+                                                       output_padding=1, out=None, workspace=None):
+    """The conv-transpose model on channels-last tensors: x [N, H, W, Cin] ->
+    out [N, Ho, Wo, Cout] (device tensors; w keeps the [Cin, Cout, k, k] layout)."""
+    dev = _device_of(x)
+    xd, wd = _dev(x, "x", dev), _dev(w, "w", dev)
+    cbd, bd = _dev(conv_b, "conv_b", dev), _dev(bias.reshape(-1), "bias", dev)
+    N, H, W, Cin = xd.shape
+    _, Cout, K, _ = wd.shape
+    Ho, Wo = fw_convt_out_shape(H, W, K, stride, padding, output_padding)
+    need = fw_convt_workspace_size(Cin, Cout, K, stride, padding)
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(max(1, (need + 3) // 4), device=dev, dtype=torch.float32)
+    od = out if out is not None else torch.empty((N, Ho, Wo, Cout), device=dev, dtype=torch.float32)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    with torch.cuda.device(dev):
+        _check(lib().fw_convtranspose2d_softmax_bias_scale_sigmoid_nhwc(
+            _ptr(xd), N, Cin, H, W, _ptr(wd), _ptr(cbd), Cout, K, stride, padding, output_padding, _ptr(bd),
+            float(scale), _ptr(od), _ptr(workspace), workspace.numel() * workspace.element_size(),
+            C.c_void_p(stream)), "fw_convtranspose2d_softmax_bias_scale_sigmoid_nhwc")
+    return od
