@@ -469,6 +469,15 @@ def run_gpu(args):
                                "unfused": "convt_k4s2_tc_kernel raw mode (conv-transpose + conv_b to memory) + "
                                           "softmax_bias_scale_sigmoid_kernel (online max/sum pass, output pass)"}
             del wsp_ct
+            # channels-last variant of the same model (x [N,H,W,Cin] -> out [N,Ho,Wo,Cout])
+            xn = d[("ct", "x")].permute(0, 2, 3, 1).contiguous()
+            on = torch.empty(n, 129, 129, CT["Cout"], device=dev)
+            nhwc_ms = med_ms(lambda: FW.fw_convtranspose2d_softmax_bias_scale_sigmoid_nhwc(
+                xn, d[("ct", "w")], d[("ct", "conv_b")], d[("ct", "bias")], CT["scale"], out=on, workspace=wsp))
+            fusion["convt_channels_last"] = {"nchw_ms": f_ms, "nhwc_ms": nhwc_ms,
+                                             "kernel": "convt_k4s2_tc_kernel<16,false,true>: 16-byte channel "
+                                                       "gathers, 256-bit output stores"}
+            del xn, on
         FW.fw_check_device_errors()
     red = reduce_max(local_ms + e2e_local, ws, device=dev if args.backend == "nccl" else None)
     total_ms, op_ms, e2e_ms = red[0], red[1:1 + len(specs)], red[1 + len(specs):]
