@@ -358,7 +358,16 @@ def run_gpu(args):
         wsz = FW.fw_convt_workspace_size(CT["Cin"], CT["Cout"], 4, 2, 1)
         wsp = torch.empty(max(1, wsz // 4), device=dev)
 
+        if args.convt_layout == "nhwc":  # profiling the channels-last variant through the same step
+            x_nhwc = d[("ct", "x")].permute(0, 2, 3, 1).contiguous()
+            out_nhwc = torch.empty(n, 129, 129, CT["Cout"], device=dev)
+
         def op_ct(src, out):
+            if args.convt_layout == "nhwc" and src is d:
+                FW.fw_convtranspose2d_softmax_bias_scale_sigmoid_nhwc(x_nhwc, src[("ct", "w")], src[("ct", "conv_b")],
+                                                                      src[("ct", "bias")], CT["scale"], out=out_nhwc,
+                                                                      workspace=wsp)
+                return
             FW.fw_convtranspose2d_softmax_bias_scale_sigmoid(src[("ct", "x")], src[("ct", "w")],
                                                              src[("ct", "conv_b")], src[("ct", "bias")],
                                                              CT["scale"], out=out, workspace=wsp)
@@ -543,8 +552,8 @@ def run_gpu(args):
     })
     if fusion:
         line["fusion"] = fusion
-    if args.only or args.batch:
-        line["config"]["subset"] = {"only": args.only, "batch": args.batch}
+    if args.only or args.batch or args.convt_layout != "nchw":
+        line["config"]["subset"] = {"only": args.only, "batch": args.batch, "convt_layout": args.convt_layout}
     print(json.dumps(line), flush=True)
     if ws > 1:
         dist.barrier()
@@ -564,6 +573,8 @@ def main(argv=None):
     ap.add_argument("--only", default=None, choices=["convpool", "maxpool", "convt"],
                     help="time one operator only (profiling)")
     ap.add_argument("--batch", type=int, default=0, help="smaller batch for every workload (profiling)")
+    ap.add_argument("--convt-layout", default="nchw", choices=["nchw", "nhwc"],
+                    help="layout of the conv-transpose in the timed step (nhwc: channels-last variant, profiling)")
     ap.add_argument("--no-fusion-compare", action="store_true",
                     help="skip timing the unfused (conv output to memory) comparison path")
     args = ap.parse_args(argv)
