@@ -321,9 +321,12 @@ def run_gpu(args):
         out_cp = torch.empty(n, CP["Cout"], 63, 63, device=dev)
         h_cp = torch.empty(tuple(out_cp.shape), pin_memory=True)
 
+        cp_fn = (FW.fw_conv2d_tanh_scale_bias_maxpool_tf32 if args.convpool_precision == "tf32"
+                 else FW.fw_conv2d_tanh_scale_bias_maxpool)  # tf32: profiling the plain-TF32 variant
+
         def op_cp(src, out):
-            FW.fw_conv2d_tanh_scale_bias_maxpool(src[("cp", "x")], src[("cp", "w")], src[("cp", "conv_b")],
-                                                 src[("cp", "bias")], CP["scale"], 4, out=out)
+            cp_fn(src[("cp", "x")], src[("cp", "w")], src[("cp", "conv_b")], src[("cp", "bias")], CP["scale"], 4,
+                  out=out)
         hws_cp = torch.empty(FW.lib().fw_conv2d_tanh_scale_bias_maxpool_host_workspace_size(
             n, CP["Cin"], CP["H"], CP["W"], CP["Cout"], 3, 3, 4, 4) // 4 + 64, device=dev)
 
@@ -465,6 +468,15 @@ def run_gpu(args):
                                   "unfused": "convpool_tc_kernel raw mode (conv + conv_b to memory) + "
                                              "pool_tanh_scale_bias_kernel"}
             del wsp_cp
+            # plain-TF32 variant of the fused operator (one TF32 product per multiply-add, 5e-3 bound)
+            out_tf = torch.empty_like(out_cp)
+            tf_ms = med_ms(lambda: FW.fw_conv2d_tanh_scale_bias_maxpool_tf32(
+                d[("cp", "x")], d[("cp", "w")], d[("cp", "conv_b")], d[("cp", "bias")], CP["scale"], 4, out=out_tf))
+            fusion["convpool_tf32"] = {"ms": tf_ms, "x3_ms": f_ms, "work_per_launch": cp_flops(N=n),
+                                       "kernel": "convpool_tc_kernel<4,64,false,false>: one kind::tf32 MMA "
+                                                 "(N = 64) per tap",
+                                       "max_abs_diff_vs_x3": float((out_tf - out_cp).abs().max())}
+            del out_tf
         if ct:
             n = ct["x"].shape[0]
             wsz = FW.fw_convt_unfused_workspace_size(n, CT["Cin"], CT["H"], CT["W"], CT["Cout"], 4, 2, 1, 1)
@@ -551,9 +563,14 @@ def run_gpu(args):
         "clocks": clk.summary(), "device": props.name,
     })
     if fusion:
+        if "convpool_tf32" in fusion:
+            v = fusion["convpool_tf32"]
+            v["tflops"] = v["work_per_launch"] / (v["ms"] * 1e-3) / 1e12
+            v["frac_of_tf32_peak"] = v["tflops"] / pk["tf32_tflops"]
         line["fusion"] = fusion
-    if args.only or args.batch or args.convt_layout != "nchw":
-        line["config"]["subset"] = {"only": args.only, "batch": args.batch, "convt_layout": args.convt_layout}
+    if args.only or args.batch or args.convt_layout != "nchw" or args.convpool_precision != "x3":
+        line["config"]["subset"] = {"only": args.only, "batch": args.batch, "convt_layout": args.convt_layout,
+                                    "convpool_precision": args.convpool_precision}
     print(json.dumps(line), flush=True)
     if ws > 1:
         dist.barrier()
@@ -575,6 +592,8 @@ def main(argv=None):
     ap.add_argument("--batch", type=int, default=0, help="smaller batch for every workload (profiling)")
     ap.add_argument("--convt-layout", default="nchw", choices=["nchw", "nhwc"],
                     help="layout of the conv-transpose in the timed step (nhwc: channels-last variant, profiling)")
+    ap.add_argument("--convpool-precision", default="x3", choices=["x3", "tf32"],
+                    help="conv+pool in the timed step: 3xTF32 split (x3) or plain TF32 (profiling)")
     ap.add_argument("--no-fusion-compare", action="store_true",
                     help="skip timing the unfused (conv output to memory) comparison path")
     args = ap.parse_args(argv)

@@ -100,6 +100,24 @@ fw_status fw_conv2d_tanh_scale_bias_maxpool(const float *x, int N, int Cin, int 
                                             int pool_k, int pool_s, float *out, void *stream);
 
 /*
+ * The same operator as fw_conv2d_tanh_scale_bias_maxpool (trace "Kimi-K2.6
+ * l2_p82", model) with the convolution in plain TF32, the mode the trace
+ * "Kimi-K2.6 l2_p91" describes for float32 convolutions on tensor cores (inputs
+ * rounded, float32 accumulation); its bound is 5e-3 absolute.  On the tiled
+ * tensor-core shapes (Cin = 8, KH = KW = 3, pool_s = pool_k in {2, 4},
+ * Cout in {16, 32, 48, 64}) every product of the convolution is taken once in
+ * TF32 (both operands rounded to 10 mantissa bits, float32 accumulation) instead
+ * of the 3xTF32 split, about 3x less tensor work; measured error against a
+ * float64 evaluation is a few 1e-4 on unit-variance inputs.  Other shapes run
+ * the float32 FMA kernels of fw_conv2d_tanh_scale_bias_maxpool.  Arguments,
+ * statuses, layout and ownership are those of fw_conv2d_tanh_scale_bias_maxpool.
+ */
+fw_status fw_conv2d_tanh_scale_bias_maxpool_tf32(const float *x, int N, int Cin, int H, int W,
+                                                 const float *w, const float *conv_b, int Cout,
+                                                 int KH, int KW, float scale, const float *bias,
+                                                 int pool_k, int pool_s, float *out, void *stream);
+
+/*
  * MaxPool2d (trace "Kimi-K2.6 l1_p42", problem statement and the -inf padding
  * semantics it quotes):
  *

@@ -196,7 +196,8 @@ fw_status launch_tiled(const float *x, int N, int Cin, int H, int W, const float
 
 bool convpool_tc_eligible(int Cin, int Cout, int KH, int KW, int pk, int ps);
 fw_status convpool_tc_launch(const float *x, int N, int H, int W, const float *w, const float *cb, int Cout,
-                             float scale, const float *bias, int pk, float *out, int Ho, int Wo, cudaStream_t st);
+                             float scale, const float *bias, int pk, float *out, int Ho, int Wo, bool x3,
+                             cudaStream_t st);
 
 // FUSEDWIN_CONVPOOL_FFMA=1 in the environment selects the FP32-FMA tiled kernel
 // instead of the tensor-core one (used to cross-check the two).
@@ -208,11 +209,13 @@ static bool convpool_force_ffma() {
     return v;
 }
 
+// tf32 = true: the tensor-core kernel runs one TF32 product per K step (the other
+// kernels are float32 FMA either way).
 fw_status convpool_launch(const float *x, int N, int Cin, int H, int W, const float *w,
                           const float *cb, int Cout, int KH, int KW, float scale, const float *bias,
-                          int pk, int ps, float *out, int Ho, int Wo, cudaStream_t st) {
+                          int pk, int ps, float *out, int Ho, int Wo, bool tf32, cudaStream_t st) {
     if (convpool_tc_eligible(Cin, Cout, KH, KW, pk, ps) && !convpool_force_ffma())
-        return convpool_tc_launch(x, N, H, W, w, cb, Cout, scale, bias, pk, out, Ho, Wo, st);
+        return convpool_tc_launch(x, N, H, W, w, cb, Cout, scale, bias, pk, out, Ho, Wo, !tf32, st);
     if (KH == 3 && KW == 3 && pk == ps && Cin <= MAX_CIN && N <= 65535 && (pk == 4 || pk == 2)) {
         if (pk == 4) return launch_tiled<4>(x, N, Cin, H, W, w, cb, Cout, scale, bias, out, Ho, Wo, st);
         return launch_tiled<2>(x, N, Cin, H, W, w, cb, Cout, scale, bias, out, Ho, Wo, st);

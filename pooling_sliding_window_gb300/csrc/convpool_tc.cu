@@ -8,7 +8,9 @@
 // error after tanh -- too coarse for a 1e-5 bound.  Each operand is split as
 // v = hi + lo with hi = tf32(v) and lo = tf32(v - hi), and the product is
 // accumulated as hi*hi + lo*hi + hi*lo (the lo*lo term, ~2^-22 relative, is
-// dropped): three MMAs per K step, float32 accumulation in TMEM.
+// dropped): three MMAs per K step, float32 accumulation in TMEM.  X3 = false
+// is the plain TF32 variant (one product, hi*hi, per K step; the 5e-3 bound the
+// pages set for a TF32 path): no lo planes are staged and one MMA runs per tap.
 //
 // Work item = one pooled output row of one image and a block of 128 conv columns:
 //   * the P conv rows of the pooled row are P GEMMs, M = 128 columns, K = 9 taps x
@@ -49,7 +51,7 @@ constexpr int MT = 128;          // conv columns per item (MMA M)
 constexpr int NCORE = MT / 8 + 2;  // core matrices per staged input row
 constexpr int CORE = 256;        // bytes of one core index: 2 planes x 8 rows x 16 B
 constexpr int RB = NCORE * CORE;   // bytes of one staged input row (per split)
-constexpr int NSTAGE = 2;
+constexpr int MAX_STAGE = 4;  // slab ring depth bound (Cfg::NST stages are used)
 // Warp roles.  A warp runs on SM sub-partition warp % 4 and reads TMEM lane quarter
 // warp % 4, so every sub-partition hosts epilogue warps; the MMA issuer (warp 0)
 // shares sub-partition 0 only with the two quarter-0 epilogue warps: busy warps on
@@ -68,8 +70,8 @@ constexpr int SLOT_COLS = 128;
 constexpr float LOG2E = 1.4426950408889634f;
 
 struct Bars {
-    uint64_t slab_full[NSTAGE];
-    uint64_t slab_empty[NSTAGE];
+    uint64_t slab_full[MAX_STAGE];
+    uint64_t slab_empty[MAX_STAGE];
     uint64_t slot_full[NSLOT];
     uint64_t slot_empty[NSLOT];
     uint64_t stg_full[2];
@@ -78,23 +80,64 @@ struct Bars {
     int abort;
 };
 
-template <int P, int N, bool RAW>
+template <int P, int N, bool RAW, bool X3>
 struct Cfg {
     static constexpr int ROWS = P + 2;
     static constexpr int SPLIT = ROWS * RB;           // hi (or lo) half of a slab
-    static constexpr int SLAB = 2 * SPLIT;
-    static constexpr int BTAP = (2 * N / 8) * CORE;   // one tap of [w_hi | w_lo]
+    static constexpr int SLAB = (X3 ? 2 : 1) * SPLIT;
+    static constexpr int NST = 2;                     // slab ring stages
+    static constexpr int BTAP = ((X3 ? 2 : 1) * N / 8) * CORE;  // one tap of [w_hi | w_lo] (or w_hi)
     static constexpr int B_BYTES = 9 * BTAP;
     static constexpr int PW = MT / P;                 // pooled columns per item
     // floats of one staging buffer: a pooled row, or (raw mode) one conv row of the block
     static constexpr int STG = RAW ? N * MT : N * PW;
     static constexpr int NH = N / 2;                  // channels per epilogue warp
     static constexpr size_t SMEM =
-        (size_t)B_BYTES + NSTAGE * SLAB + 2 * STG * 4 + 2 * N * 4 + sizeof(Bars);
+        (size_t)B_BYTES + NST * SLAB + 2 * STG * 4 + 2 * N * 4 + sizeof(Bars);
+    static_assert(NST <= MAX_STAGE, "slab ring");
+};
+
+// Window extreme of conv values: max.NaN / min.NaN, one instruction, a NaN
+// propagates.  The sign of a zero extreme is left to the hardware, which the
+// absolute-error bound of this operator cannot see (+0 and -0 differ by 0).
+__device__ __forceinline__ float max_nan(float a, float b) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ float min_nan(float a, float b) {
+    float r;
+    asm("min.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+// Item index -> (image n, pooled row pr, column block cblk), item = (n*Ho + pr)*ncb + cblk,
+// advanced by the grid stride without a division per item (one at the start).
+struct ItemCursor {
+    long long n, dn;
+    int pr, cblk, dp, dc;
+    __device__ ItemCursor(long long item, long long stride, int Ho, int ncb) {
+        cblk = (int)(item % ncb);
+        const long long t = item / ncb;
+        pr = (int)(t % Ho);
+        n = t / Ho;
+        dc = (int)(stride % ncb);
+        const long long ts = stride / ncb;
+        dp = (int)(ts % Ho);
+        dn = ts / Ho;
+    }
+    __device__ __forceinline__ void advance(int Ho, int ncb) {
+        cblk += dc;
+        int carry = cblk >= ncb;
+        cblk -= carry ? ncb : 0;
+        pr += dp + carry;
+        carry = pr >= Ho;
+        pr -= carry ? Ho : 0;
+        n += dn + carry;
+    }
 };
 
 __device__ __forceinline__ float upd(float m, float v, bool use_min) {
-    return use_min ? min_update(m, v) : max_update(m, v);
+    return use_min ? min_nan(m, v) : max_nan(m, v);
 }
 
 // tanh(z) = 1 - 2 / (1 + e^(2z)) with a base-2 exponential and a fast reciprocal:
@@ -109,17 +152,18 @@ __device__ __forceinline__ float tanh_fast(float z) {
 // RAW = false: the fused operator.  RAW = true: the first kernel of the unfused
 // comparison path -- `out` receives y = conv(x) + conv_b for the P*Ho x P*Wo conv
 // outputs the pool reads ([Nimg, N, P*Ho, P*Wo]); scale and bias are unused.
-template <int P, int N, bool RAW>
+// X3 selects the 3xTF32 split (true) or a single TF32 product (false).
+template <int P, int N, bool RAW, bool X3>
 __global__ void __launch_bounds__(NTHREADS, 1)
 convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, const float *__restrict__ cb,
                    const float *__restrict__ bias, float scale, float *__restrict__ out, int Nimg, int H, int W,
                    int Ho, int Wo, int ncb, bool vec) {
-    using C = Cfg<P, N, RAW>;
+    using C = Cfg<P, N, RAW, X3>;
     constexpr int CIN = 8;
     extern __shared__ __align__(1024) unsigned char smem[];
     unsigned char *sB = smem;
     unsigned char *sSlab = smem + C::B_BYTES;
-    float *sStg = reinterpret_cast<float *>(sSlab + NSTAGE * C::SLAB);  // 2 staging buffers
+    float *sStg = reinterpret_cast<float *>(sSlab + C::NST * C::SLAB);  // 2 staging buffers
     float *sCb = sStg + 2 * C::STG;
     float *sBias = sCb + N;
     Bars &bars = *reinterpret_cast<Bars *>(sBias + N);
@@ -140,10 +184,10 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
         const float hi = tc::to_tf32(v), lo = tc::to_tf32(v - hi);
         const int base = tap * C::BTAP + (ci / 4) * 128 + (ci % 4) * 4;
         *reinterpret_cast<float *>(sB + base + (co / 8) * CORE + (co % 8) * 16) = hi;
-        *reinterpret_cast<float *>(sB + base + ((N + co) / 8) * CORE + ((N + co) % 8) * 16) = lo;
+        if constexpr (X3) *reinterpret_cast<float *>(sB + base + ((N + co) / 8) * CORE + ((N + co) % 8) * 16) = lo;
     }
     if (tid == 0) {
-        for (int s = 0; s < NSTAGE; ++s) {
+        for (int s = 0; s < C::NST; ++s) {
             mbar_init(smem_u32(&bars.slab_full[s]), NPROD);
             mbar_init(smem_u32(&bars.slab_empty[s]), 1);
         }
@@ -184,13 +228,12 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
         const int ptid = producer_index(warp) * 32 + lane;
         const long long plane_stride = (long long)H * W;
         int k = 0;
-        for (long long item = blockIdx.x; item < n_items && !*abort_flag; item += gridDim.x, ++k) {
-            const int stage = k & 1, use = k >> 1;
-            const int cblk = (int)(item % ncb);
-            const long long t = item / ncb;
-            const int pr = (int)(t % Ho);
-            const long long n = t / Ho;
-            const int row0 = pr * P, col0 = cblk * MT;
+        ItemCursor cur(blockIdx.x, gridDim.x, Ho, ncb);
+        for (long long item = blockIdx.x; item < n_items && !*abort_flag;
+             item += gridDim.x, ++k, cur.advance(Ho, ncb)) {
+            const int stage = k % C::NST, use = k / C::NST;
+            const int row0 = cur.pr * P, col0 = cur.cblk * MT;
+            const long long n = cur.n;
             const float *xn = x + n * CIN * plane_stride;
             float4 vm[MITER][CIN];
 #pragma unroll
@@ -232,8 +275,9 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
             auto put = [&](unsigned char *dst, float c0, float c1, float c2, float c3) {
                 const float h0 = tc::to_tf32(c0), h1 = tc::to_tf32(c1), h2 = tc::to_tf32(c2), h3 = tc::to_tf32(c3);
                 *reinterpret_cast<float4 *>(dst) = make_float4(h0, h1, h2, h3);
-                *reinterpret_cast<float4 *>(dst + C::SPLIT) =
-                    make_float4(tc::to_tf32(c0 - h0), tc::to_tf32(c1 - h1), tc::to_tf32(c2 - h2), tc::to_tf32(c3 - h3));
+                if constexpr (X3)
+                    *reinterpret_cast<float4 *>(dst + C::SPLIT) = make_float4(
+                        tc::to_tf32(c0 - h0), tc::to_tf32(c1 - h1), tc::to_tf32(c2 - h2), tc::to_tf32(c3 - h3));
             };
 #pragma unroll
             for (int it = 0; it < MITER; ++it) {
@@ -263,13 +307,13 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
     } else if (warp == MMA_WARP) {
         // ------------------------------------------------------------ MMA issue
         if (lane == 0) {
-            constexpr uint32_t IDESC_HH_HL = tc::idesc_tf32(128, 2 * N);
+            constexpr uint32_t IDESC_HH_HL = tc::idesc_tf32(128, (X3 ? 2 : 1) * N);
             constexpr uint32_t IDESC_LH = tc::idesc_tf32(128, N);
             const uint32_t sB_addr = smem_u32(sB), sSlab_addr = smem_u32(sSlab);
             int k = 0, rowc = 0;
             bool ok = true;
             for (long long item = blockIdx.x; ok && item < n_items && !*abort_flag; item += gridDim.x, ++k) {
-                const int stage = k & 1, use = k >> 1;
+                const int stage = k % C::NST, use = k / C::NST;
                 if (!mbar_wait_bounded(smem_u32(&bars.slab_full[stage]), use & 1)) {
                     fail();
                     break;
@@ -296,7 +340,7 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
                         const uint64_t al = ah + (uint64_t)(C::SPLIT >> 4);
                         const uint64_t bd = b0 + (uint64_t)((tap * C::BTAP) >> 4);
                         tc::mma_tf32(d, ah, bd, IDESC_HH_HL, tap > 0 ? 1u : 0u);
-                        tc::mma_tf32(d, al, bd, IDESC_LH, 1u);
+                        if constexpr (X3) tc::mma_tf32(d, al, bd, IDESC_LH, 1u);
                     }
                     tc::commit(smem_u32(&bars.slot_full[slot]));
                 }
@@ -316,7 +360,9 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
         const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(h * NH);
         int k = 0, rowc = 0;
         bool ok = true;
-        for (long long item = blockIdx.x; ok && item < n_items && !*abort_flag; item += gridDim.x, ++k) {
+        ItemCursor cur(blockIdx.x, gridDim.x, Ho, ncb);
+        for (long long item = blockIdx.x; ok && item < n_items && !*abort_flag;
+             item += gridDim.x, ++k, cur.advance(Ho, ncb)) {
             float m[NH];
 #pragma unroll
             for (int c = 0; c < NH; ++c) m[c] = use_min ? INFINITY : -INFINITY;
@@ -334,7 +380,7 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
 #pragma unroll
                 for (int c = 0; c < NH; c += 8) {
                     tc::ld8(ts + c, a + c);      // x_hi*w_hi + x_lo*w_hi
-                    tc::ld8(ts + N + c, b + c);  // x_hi*w_lo
+                    if constexpr (X3) tc::ld8(ts + N + c, b + c);  // x_hi*w_lo
                 }
                 tc::wait_ld();
                 tc::fence_before_sync();
@@ -356,19 +402,20 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
                         ok = false;
                         break;
                     }
-                    const int cblk = (int)(item % ncb);
-                    const long long t = item / ncb;
                     const int HI = P * Ho, WI = P * Wo;
-                    const int row = (int)(t % Ho) * P + j, col0 = cblk * MT;
-                    float *yrow = out + (t / Ho) * (long long)N * HI * WI + (long long)row * WI + col0;
+                    const int row = cur.pr * P + j, col0 = cur.cblk * MT;
+                    float *yrow = out + cur.n * (long long)N * HI * WI + (long long)row * WI + col0;
                     for (int e = tid - EPI_WARP0 * 32; e < N * MT; e += NEPI * 32) {
                         const int co = e / MT, cc = e - co * MT;
                         const int ci = cc & 15, cr = cc >> 4;
                         if (col0 + cc < WI) yrow[(long long)co * HI * WI + cc] = rs[co * MT + 8 * ci + (cr ^ (2 * (ci >> 2)))];
                     }
+                } else if (use_min) {  // warp-uniform: one instruction per conv value
+#pragma unroll
+                    for (int c = 0; c < NH; ++c) m[c] = min_nan(m[c], X3 ? a[c] + b[c] : a[c]);
                 } else {
 #pragma unroll
-                    for (int c = 0; c < NH; ++c) m[c] = upd(m[c], a[c] + b[c], use_min);
+                    for (int c = 0; c < NH; ++c) m[c] = max_nan(m[c], X3 ? a[c] + b[c] : a[c]);
                 }
             }
             if (!ok) break;
@@ -416,14 +463,18 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
                 fail();
                 break;
             }
-            const int cblk = (int)(item % ncb);
-            const long long t = item / ncb;
-            const int pr = (int)(t % Ho);
-            const long long n = t / Ho;
-            const int pw0 = cblk * C::PW;
-            for (int e = tid - EPI_WARP0 * 32; e < C::STG; e += NEPI * 32) {
-                const int co = e / C::PW, pw = e - co * C::PW;
-                if (pw0 + pw < Wo) out[((n * N + co) * Ho + pr) * (long long)Wo + pw0 + pw] = stg[e];
+            // thread et stores column pw of channels co0, co0 + CSTEP, ...: row-contiguous
+            // warps, a pointer stride per store
+            constexpr int CSTEP = NEPI * 32 / C::PW;
+            const int et = tid - EPI_WARP0 * 32, pw = et % C::PW, co0 = et / C::PW;
+            const int pw0 = cur.cblk * C::PW;
+            if (pw0 + pw < Wo) {
+                const long long cstride = (long long)Ho * Wo;
+                float *op = out + ((cur.n * N + co0) * Ho + cur.pr) * (long long)Wo + pw0 + pw;
+                const float *sp = stg + co0 * C::PW + pw;
+                static_assert(N % CSTEP == 0, "store passes");
+#pragma unroll
+                for (int i = 0; i < N / CSTEP; ++i, op += CSTEP * cstride, sp += CSTEP * C::PW) *op = *sp;
             }
         }
     }
@@ -436,13 +487,13 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
     }
 }
 
-template <int P, int N, bool RAW>
+template <int P, int N, bool RAW, bool X3>
 fw_status launch_pn(const float *x, int Nimg, int H, int W, const float *w, const float *cb, const float *bias,
                     float scale, float *out, int Ho, int Wo, cudaStream_t st) {
-    using C = Cfg<P, N, RAW>;
+    using C = Cfg<P, N, RAW, X3>;
     size_t smem = C::SMEM < 116 * 1024 ? 116 * 1024 : C::SMEM;  // one CTA per SM
-    cudaError_t e = cudaFuncSetAttribute(convpool_tc_kernel<P, N, RAW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(convpool_tc_kernel<P, N, RAW, X3>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return launch_status(e);
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -452,8 +503,8 @@ fw_status launch_pn(const float *x, int Nimg, int H, int W, const float *w, cons
     const long long items = (long long)Nimg * Ho * ncb;
     const int grid = (int)(items < sms ? items : sms);
     const bool vec = W % 4 == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0;  // float4 input rows
-    convpool_tc_kernel<P, N, RAW><<<grid, NTHREADS, smem, st>>>(x, w, cb, bias, scale, out, Nimg, H, W, Ho, Wo, ncb,
-                                                                vec);
+    convpool_tc_kernel<P, N, RAW, X3><<<grid, NTHREADS, smem, st>>>(x, w, cb, bias, scale, out, Nimg, H, W, Ho, Wo,
+                                                                    ncb, vec);
     note_launch();
     return launch_status(cudaGetLastError());
 }
@@ -465,10 +516,14 @@ bool convpool_tc_eligible(int Cin, int Cout, int KH, int KW, int pk, int ps) {
            (Cout == 16 || Cout == 32 || Cout == 48 || Cout == 64);
 }
 
+// x3 = true: 3xTF32 split (float32-level accuracy); false: one TF32 product per K step.
 fw_status convpool_tc_launch(const float *x, int N, int H, int W, const float *w, const float *cb, int Cout,
-                             float scale, const float *bias, int pk, float *out, int Ho, int Wo, cudaStream_t st) {
-#define FW_CP_CASE(PP, NN) \
-    if (pk == PP && Cout == NN) return launch_pn<PP, NN, false>(x, N, H, W, w, cb, bias, scale, out, Ho, Wo, st);
+                             float scale, const float *bias, int pk, float *out, int Ho, int Wo, bool x3,
+                             cudaStream_t st) {
+#define FW_CP_CASE(PP, NN)                                                                                      \
+    if (pk == PP && Cout == NN)                                                                                 \
+        return x3 ? launch_pn<PP, NN, false, true>(x, N, H, W, w, cb, bias, scale, out, Ho, Wo, st)             \
+                  : launch_pn<PP, NN, false, false>(x, N, H, W, w, cb, bias, scale, out, Ho, Wo, st);
     FW_CP_CASE(4, 64) FW_CP_CASE(4, 48) FW_CP_CASE(4, 32) FW_CP_CASE(4, 16)
     FW_CP_CASE(2, 64) FW_CP_CASE(2, 48) FW_CP_CASE(2, 32) FW_CP_CASE(2, 16)
 #undef FW_CP_CASE
@@ -520,7 +575,7 @@ __global__ void __launch_bounds__(256) pool_tanh_scale_bias_kernel(const float *
 fw_status convpool_tc_launch_raw(const float *x, int N, int H, int W, const float *w, const float *cb, int Cout,
                                  int pk, float *y, int Ho, int Wo, cudaStream_t st) {
 #define FW_CP_CASE(PP, NN) \
-    if (pk == PP && Cout == NN) return launch_pn<PP, NN, true>(x, N, H, W, w, cb, nullptr, 0.f, y, Ho, Wo, st);
+    if (pk == PP && Cout == NN) return launch_pn<PP, NN, true, true>(x, N, H, W, w, cb, nullptr, 0.f, y, Ho, Wo, st);
     FW_CP_CASE(4, 64) FW_CP_CASE(4, 48) FW_CP_CASE(4, 32) FW_CP_CASE(4, 16)
     FW_CP_CASE(2, 64) FW_CP_CASE(2, 48) FW_CP_CASE(2, 32) FW_CP_CASE(2, 16)
 #undef FW_CP_CASE

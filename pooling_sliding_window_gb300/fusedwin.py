@@ -37,7 +37,7 @@ EXPORTS = ("fw_status_string", "fw_version", "fw_conv2d_pool_out_shape", "fw_max
            "fw_maxpool2d_host", "fw_maxpool2d_host_workspace_size",
            "fw_convtranspose2d_softmax_bias_scale_sigmoid_host",
            "fw_convtranspose2d_softmax_bias_scale_sigmoid_host_workspace_size",
-           "fw_convtranspose2d_softmax_bias_scale_sigmoid_nhwc")
+           "fw_convtranspose2d_softmax_bias_scale_sigmoid_nhwc", "fw_conv2d_tanh_scale_bias_maxpool_tf32")
 
 
 class FusedWinError(RuntimeError):
@@ -68,8 +68,9 @@ def lib():
             f = getattr(L, name)
             f.restype = I
             f.argtypes = [I] * n + [IP, IP]
-        L.fw_conv2d_tanh_scale_bias_maxpool.restype = I
-        L.fw_conv2d_tanh_scale_bias_maxpool.argtypes = [P, I, I, I, I, P, P, I, I, I, F, P, I, I, P, P]
+        for name in ("fw_conv2d_tanh_scale_bias_maxpool", "fw_conv2d_tanh_scale_bias_maxpool_tf32"):
+            getattr(L, name).restype = I
+            getattr(L, name).argtypes = [P, I, I, I, I, P, P, I, I, I, F, P, I, I, P, P]
         L.fw_maxpool2d.restype = I
         L.fw_maxpool2d.argtypes = [P, I, I, I, I, I, I, I, I, P, P]
         L.fw_convtranspose2d_softmax_bias_scale_sigmoid.restype = I
@@ -200,6 +201,15 @@ def _finish(out_dev, out, host):
 
 def fw_conv2d_tanh_scale_bias_maxpool(x, w, conv_b, bias, scale, pool_k, pool_s=0, out=None):
     """out = MaxPool2d(pool_k, pool_s)(bias + scale * tanh(conv2d(x, w, conv_b)))."""
+    return _conv_pool("fw_conv2d_tanh_scale_bias_maxpool", x, w, conv_b, bias, scale, pool_k, pool_s, out)
+
+
+def fw_conv2d_tanh_scale_bias_maxpool_tf32(x, w, conv_b, bias, scale, pool_k, pool_s=0, out=None):
+    """The same operator with the convolution's products taken once in TF32 on the tensor-core shapes."""
+    return _conv_pool("fw_conv2d_tanh_scale_bias_maxpool_tf32", x, w, conv_b, bias, scale, pool_k, pool_s, out)
+
+
+def _conv_pool(fname, x, w, conv_b, bias, scale, pool_k, pool_s, out):
     host = x.device.type != "cuda"
     dev = _device_of(x)
     xd, wd = _dev(x, "x", dev), _dev(w, "w", dev)
@@ -211,9 +221,9 @@ def fw_conv2d_tanh_scale_bias_maxpool(x, w, conv_b, bias, scale, pool_k, pool_s=
                                                                  dtype=torch.float32)
     stream = torch.cuda.current_stream(dev).cuda_stream
     with torch.cuda.device(dev):
-        _check(lib().fw_conv2d_tanh_scale_bias_maxpool(
+        _check(getattr(lib(), fname)(
             _ptr(xd), N, Cin, H, W, _ptr(wd), _ptr(cbd), Cout, KH, KW, float(scale), _ptr(bd),
-            pool_k, pool_s, _ptr(od), C.c_void_p(stream)), "fw_conv2d_tanh_scale_bias_maxpool")
+            pool_k, pool_s, _ptr(od), C.c_void_p(stream)), fname)
     return _finish(od, out, host)
 
 

@@ -13,6 +13,8 @@ from pooling_sliding_window_gb300 import synth
 
 # Tolerance of the FP32-FMA conv paths against the oracle (max abs error).
 TOL_FFMA = 1e-5
+# Tolerance of the plain-TF32 conv path (one TF32 product per multiply-add).
+TOL_TF32 = 5e-3
 
 POOL = ThreadPoolExecutor(max(1, min(16, os.cpu_count() or 1)))  # oracle calls release the GIL
 
@@ -50,6 +52,14 @@ def assert_close(got, want, tol, what=""):
     return m
 
 
+def tf32_round(a):
+    """Round float32 values to TF32 (10 explicit mantissa bits), to nearest with ties
+    away from zero: add half of the dropped 13-bit field to the magnitude and clear
+    it (finite inputs; a carry into the exponent is the correct rounding)."""
+    u = np.ascontiguousarray(a, np.float32).view(np.uint32)
+    return ((u + np.uint32(0x1000)) & np.uint32(0xFFFFE000)).view(np.float32)
+
+
 def pmap(fn, items):
     return list(POOL.map(fn, items))
 
@@ -59,5 +69,5 @@ def sample_indices(shape, count, seed):
     return [tuple(int(rng.integers(0, s)) for s in shape) for _ in range(count)]
 
 
-__all__ = ["O", "FW", "synth", "TOL_FFMA", "dev", "host", "assert_bits_equal", "assert_close", "pmap",
+__all__ = ["O", "FW", "synth", "TOL_FFMA", "TOL_TF32", "tf32_round", "dev", "host", "assert_bits_equal", "assert_close", "pmap",
            "sample_indices", "bits_equal"]

@@ -94,18 +94,19 @@ def test_operator_argument_errors_without_launch():
     # conv+pool
     args = lambda **kw: dict(dict(x=x, N=1, Cin=8, H=16, W=16, w=w, cb=None, Cout=4, KH=3, KW=3,
                                   scale=2.0, bias=b, pk=4, ps=0, out=o), **kw)
-    call = lambda a: L.fw_conv2d_tanh_scale_bias_maxpool(a["x"], a["N"], a["Cin"], a["H"], a["W"], a["w"],
-                                                          a["cb"], a["Cout"], a["KH"], a["KW"], a["scale"],
-                                                          a["bias"], a["pk"], a["ps"], a["out"], None)
-    assert call(args(bias=None)) == 1
-    assert call(args(Cout=0)) == 2
-    assert call(args(H=4)) == 2
-    assert call(args(scale=float("inf"))) == 3
-    assert call(args(scale=float("nan"))) == 3
-    assert call(args(pk=0)) == 3
-    assert call(args(out=P(0x20000 + 16))) == 4  # out overlaps w
-    assert call(args(out=b)) == 4
-    assert call(args(w=P(0x20001))) == 5
+    for fname in ("fw_conv2d_tanh_scale_bias_maxpool", "fw_conv2d_tanh_scale_bias_maxpool_tf32"):
+        f = getattr(L, fname)
+        call = lambda a: f(a["x"], a["N"], a["Cin"], a["H"], a["W"], a["w"], a["cb"], a["Cout"], a["KH"], a["KW"],
+                           a["scale"], a["bias"], a["pk"], a["ps"], a["out"], None)
+        assert call(args(bias=None)) == 1
+        assert call(args(Cout=0)) == 2
+        assert call(args(H=4)) == 2
+        assert call(args(scale=float("inf"))) == 3
+        assert call(args(scale=float("nan"))) == 3
+        assert call(args(pk=0)) == 3
+        assert call(args(out=P(0x20000 + 16))) == 4  # out overlaps w
+        assert call(args(out=b)) == 4
+        assert call(args(w=P(0x20001))) == 5
     # conv-transpose
     need = FW.fw_convt_workspace_size(64, 128, 4, 2, 1)
     assert need == 16 * 64 * 128 * 4
