@@ -58,23 +58,22 @@ constexpr int MAX_STAGE = 4;  // slab ring depth bound (Cfg::NST stages are used
 // the issuer's sub-partition slow MMA issue (measured: 2.3x with two FMA-bound
 // warps there, none with the same warps on the other three).
 constexpr int MMA_WARP = 0;
-constexpr int EPI_WARP0 = 4;     // warps 4-11: epilogue
-constexpr int NEPI = 8;
-constexpr int NPROD = 6;         // warps 1-3 and 13-15: producers (warp 12 idles)
-constexpr int NTHREADS = 16 * 32;
-__device__ __forceinline__ int producer_index(int warp) {  // 0..5, or -1
-    return (warp >= 1 && warp <= 3) ? warp - 1 : (warp >= 13 ? warp - 10 : -1);
+constexpr int EPI_WARP0 = 4;     // warps 4 .. 4 + NEPI - 1: epilogue
+constexpr int NPROD = 6;         // warps 1-3 and the last three: producers (the one before idles)
+// nw warps in the CTA (a multiple of 4): producer number 0..5 of a warp, or -1
+__device__ __forceinline__ int producer_index(int warp, int nw) {
+    return (warp >= 1 && warp <= 3) ? warp - 1 : (warp >= nw - 3 ? warp - (nw - 6) : -1);
 }
-constexpr int NSLOT = 4;         // TMEM accumulator ring, one conv row per slot
-constexpr int SLOT_COLS = 128;
+constexpr int TMEM_COLS = 512;   // all of the SM's tensor memory (one CTA per SM)
+constexpr int MAX_SLOT = 8;
 constexpr float LOG2E = 1.4426950408889634f;
 
 struct Bars {
     uint64_t slab_full[MAX_STAGE];
     uint64_t slab_empty[MAX_STAGE];
-    uint64_t slot_full[NSLOT];
-    uint64_t slot_empty[NSLOT];
-    uint64_t stg_full[2];
+    uint64_t slot_full[MAX_SLOT];
+    uint64_t slot_empty[MAX_SLOT];
+    uint64_t stg_full[4];  // [group][buffer]
     uint64_t raw_full[2];  // raw mode: a conv row staged by all epilogue warps
     uint32_t tmem_base;
     int abort;
@@ -86,14 +85,26 @@ struct Cfg {
     static constexpr int SPLIT = ROWS * RB;           // hi (or lo) half of a slab
     static constexpr int SLAB = (X3 ? 2 : 1) * SPLIT;
     static constexpr int NST = 2;                     // slab ring stages
+    // TMEM accumulator ring, one conv row per slot: [x*w_hi (+ x_lo*w_hi) | x_hi*w_lo]
+    static constexpr int SLOT_COLS = X3 ? 128 : 64;
+    static constexpr int NSLOT = TMEM_COLS / SLOT_COLS;
+    static_assert((X3 ? 2 : 1) * N <= SLOT_COLS && NSLOT <= MAX_SLOT, "slots");
     static constexpr int BTAP = ((X3 ? 2 : 1) * N / 8) * CORE;  // one tap of [w_hi | w_lo] (or w_hi)
     static constexpr int B_BYTES = 9 * BTAP;
     static constexpr int PW = MT / P;                 // pooled columns per item
     // floats of one staging buffer: a pooled row, or (raw mode) one conv row of the block
     static constexpr int STG = RAW ? N * MT : N * PW;
+    // Epilogue: NGRP groups of 8 warps; a group reads every conv row of its items
+    // (warp w: lane quarter w % 4, half the channels) and the groups take the items
+    // in turn, so one group's pooling tail overlaps the next group's TMEM rows.  Two
+    // groups where the tensor work per item is short (plain TF32), one otherwise.
+    static constexpr int NGRP = (!RAW && !X3) ? 2 : 1;
+    static constexpr int NEPI = 8 * NGRP;
+    static constexpr int NTHREADS = (8 + NEPI) * 32;  // + MMA warp, 6 producers, 1 idle
     static constexpr int NH = N / 2;                  // channels per epilogue warp
+    static constexpr int LDC = NGRP > 1 && NH % 16 == 0 ? 16 : NH;  // TMEM columns per load round
     static constexpr size_t SMEM =
-        (size_t)B_BYTES + NST * SLAB + 2 * STG * 4 + 2 * N * 4 + sizeof(Bars);
+        (size_t)B_BYTES + NST * SLAB + 2 * NGRP * STG * 4 + 2 * N * 4 + sizeof(Bars);
     static_assert(NST <= MAX_STAGE, "slab ring");
 };
 
@@ -154,17 +165,17 @@ __device__ __forceinline__ float tanh_fast(float z) {
 // outputs the pool reads ([Nimg, N, P*Ho, P*Wo]); scale and bias are unused.
 // X3 selects the 3xTF32 split (true) or a single TF32 product (false).
 template <int P, int N, bool RAW, bool X3>
-__global__ void __launch_bounds__(NTHREADS, 1)
+__global__ void __launch_bounds__(Cfg<P, N, RAW, X3>::NTHREADS, 1)
 convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, const float *__restrict__ cb,
                    const float *__restrict__ bias, float scale, float *__restrict__ out, int Nimg, int H, int W,
                    int Ho, int Wo, int ncb, bool vec) {
     using C = Cfg<P, N, RAW, X3>;
-    constexpr int CIN = 8;
+    constexpr int CIN = 8, NEPI = C::NEPI, NTHREADS = C::NTHREADS, NW = NTHREADS / 32;
     extern __shared__ __align__(1024) unsigned char smem[];
     unsigned char *sB = smem;
     unsigned char *sSlab = smem + C::B_BYTES;
-    float *sStg = reinterpret_cast<float *>(sSlab + C::NST * C::SLAB);  // 2 staging buffers
-    float *sCb = sStg + 2 * C::STG;
+    float *sStg = reinterpret_cast<float *>(sSlab + C::NST * C::SLAB);  // 2 staging buffers per group
+    float *sCb = sStg + 2 * C::NGRP * C::STG;
     float *sBias = sCb + N;
     Bars &bars = *reinterpret_cast<Bars *>(sBias + N);
 
@@ -191,18 +202,16 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
             mbar_init(smem_u32(&bars.slab_full[s]), NPROD);
             mbar_init(smem_u32(&bars.slab_empty[s]), 1);
         }
-        for (int b = 0; b < NSLOT; ++b) {
+        for (int b = 0; b < C::NSLOT; ++b) {
             mbar_init(smem_u32(&bars.slot_full[b]), 1);
-            mbar_init(smem_u32(&bars.slot_empty[b]), NEPI);
+            mbar_init(smem_u32(&bars.slot_empty[b]), 8);  // one group reads a row
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(smem_u32(&bars.stg_full[b]), NEPI);
-            mbar_init(smem_u32(&bars.raw_full[b]), NEPI);
-        }
+        for (int b = 0; b < 2 * C::NGRP; ++b) mbar_init(smem_u32(&bars.stg_full[b]), 8);
+        for (int b = 0; b < 2; ++b) mbar_init(smem_u32(&bars.raw_full[b]), NEPI);
         bars.abort = 0;
         fence_mbar_init();
     }
-    if (warp == MMA_WARP) tc::alloc(smem_u32(&bars.tmem_base), NSLOT * SLOT_COLS);
+    if (warp == MMA_WARP) tc::alloc(smem_u32(&bars.tmem_base), TMEM_COLS);
     fence_proxy_async_smem();
     tc::fence_before_sync();
     __syncthreads();
@@ -214,7 +223,7 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
         atomicOr(&g_err_convpool_tc, DEVERR_TIMEOUT);
     };
 
-    if (producer_index(warp) >= 0) {
+    if (producer_index(warp, NW) >= 0) {
         // ------------------------------------------------------------ producers
         // Main task (row rr, group a, r): the 4 input columns 4a + 16r .. +3 of the
         // block, i.e. row r of cores 4a .. 4a+3.  Lane r + 8a of a warp, so a warp's
@@ -225,7 +234,7 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
         // column 128 / 129 for r = 7).
         constexpr int NPT = NPROD * 32;  // producer threads
         constexpr int MTASK = C::ROWS * 32, MITER = (MTASK + NPT - 1) / NPT, TTASK = C::ROWS * 16;
-        const int ptid = producer_index(warp) * 32 + lane;
+        const int ptid = producer_index(warp, NW) * 32 + lane;
         const long long plane_stride = (long long)H * W;
         int k = 0;
         ItemCursor cur(blockIdx.x, gridDim.x, Ho, ncb);
@@ -326,14 +335,14 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
                 const uint64_t b0 = tc::smem_desc(sB_addr, 128, CORE);
 #pragma unroll
                 for (int j = 0; j < P; ++j, ++rowc) {
-                    const int slot = rowc % NSLOT, sus = rowc / NSLOT;
+                    const int slot = rowc % C::NSLOT, sus = rowc / C::NSLOT;
                     if (sus > 0 && !mbar_wait_bounded(smem_u32(&bars.slot_empty[slot]), (sus - 1) & 1)) {
                         fail();
                         ok = false;
                         break;
                     }
                     tc::fence_after_sync();
-                    const uint32_t d = tmem + (uint32_t)(slot * SLOT_COLS);
+                    const uint32_t d = tmem + (uint32_t)(slot * C::SLOT_COLS);
 #pragma unroll
                     for (int tap = 0; tap < 9; ++tap) {
                         const uint64_t ah = a0 + (uint64_t)((((j + tap / 3) * RB) + (tap % 3) * CORE) >> 4);
@@ -354,39 +363,47 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
         // quarter q is MMA row m = 32q + l = 8*i + r with i = 4q + l/8, r = l % 8:
         // conv column i + 16r.  The P columns of a pooling window are lanes l ^ 8
         // (and l ^ 16 for P = 4) of the same warp.
-        constexpr int NH = C::NH;
+        constexpr int NH = C::NH, NG = C::NGRP;
+        const int ew = warp - EPI_WARP0, grp = ew >> 3, gw = ew & 7;  // group, warp within the group
         const int q = warp & 3;
-        const int h = (warp - EPI_WARP0) >> 2;
+        const int h = gw >> 2;
         const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(h * NH);
-        int k = 0, rowc = 0;
         bool ok = true;
-        ItemCursor cur(blockIdx.x, gridDim.x, Ho, ncb);
-        for (long long item = blockIdx.x; ok && item < n_items && !*abort_flag;
-             item += gridDim.x, ++k, cur.advance(Ho, ncb)) {
+        // this group's items: the CTA's item sequence numbers k = grp, grp + NG, ...
+        ItemCursor cur(blockIdx.x + (long long)grp * gridDim.x, (long long)NG * gridDim.x, Ho, ncb);
+        int k = grp, kk = 0;
+        for (long long item = blockIdx.x + (long long)grp * gridDim.x; ok && item < n_items && !*abort_flag;
+             item += (long long)NG * gridDim.x, k += NG, ++kk, cur.advance(Ho, ncb)) {
             float m[NH];
 #pragma unroll
             for (int c = 0; c < NH; ++c) m[c] = use_min ? INFINITY : -INFINITY;
 #pragma unroll 1
-            for (int j = 0; j < P; ++j, ++rowc) {
-                const int slot = rowc % NSLOT, sus = rowc / NSLOT;
+            for (int j = 0; j < P; ++j) {
+                const int rowc = k * P + j;  // conv rows in MMA order
+                const int slot = rowc % C::NSLOT, sus = rowc / C::NSLOT;
                 if (!mbar_wait_bounded(smem_u32(&bars.slot_full[slot]), sus & 1)) {
                     fail();
                     ok = false;
                     break;
                 }
                 tc::fence_after_sync();
-                float a[NH], b[NH];
-                const uint32_t ts = tq + (uint32_t)(slot * SLOT_COLS);
+                const uint32_t ts = tq + (uint32_t)(slot * C::SLOT_COLS);
+                // NH channels in rounds of C::LDC TMEM columns (fewer live registers)
 #pragma unroll
-                for (int c = 0; c < NH; c += 8) {
-                    tc::ld8(ts + c, a + c);      // x_hi*w_hi + x_lo*w_hi
-                    if constexpr (X3) tc::ld8(ts + N + c, b + c);  // x_hi*w_lo
-                }
-                tc::wait_ld();
-                tc::fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&bars.slot_empty[slot]));
-                if constexpr (RAW) {
+                for (int c0 = 0; c0 < NH; c0 += C::LDC) {
+                    float a[C::LDC], b[C::LDC];
+#pragma unroll
+                    for (int c = 0; c < C::LDC; c += 8) {
+                        tc::ld8(ts + c0 + c, a + c);                   // x_hi*w_hi + x_lo*w_hi
+                        if constexpr (X3) tc::ld8(ts + N + c0 + c, b + c);  // x_hi*w_lo
+                    }
+                    tc::wait_ld();
+                    if (c0 + C::LDC == NH) {
+                        tc::fence_before_sync();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(smem_u32(&bars.slot_empty[slot]));
+                    }
+                    if constexpr (RAW) {
                     // Stage the row as [channel][position]; conv column i + 16r sits at
                     // 8i + (r ^ 2(i/4)), so both the writes here and the column-order
                     // reads below hit 32 distinct banks.
@@ -394,7 +411,9 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
                     const int i = 4 * q + (lane >> 3), r = lane & 7;
                     const int pos = 8 * i + (r ^ (2 * (i >> 2)));
 #pragma unroll
-                    for (int c = 0; c < NH; ++c) rs[(h * NH + c) * MT + pos] = (a[c] + b[c]) + sCb[h * NH + c];
+                    for (int c = 0; c < C::LDC; ++c)
+                        rs[(h * NH + c0 + c) * MT + pos] = (a[c] + b[c]) + sCb[h * NH + c0 + c];
+                    if (c0 + C::LDC < NH) continue;
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_u32(&bars.raw_full[rowc & 1]));
                     if (!mbar_wait_bounded(smem_u32(&bars.raw_full[rowc & 1]), (rowc >> 1) & 1)) {
@@ -410,13 +429,15 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
                         const int ci = cc & 15, cr = cc >> 4;
                         if (col0 + cc < WI) yrow[(long long)co * HI * WI + cc] = rs[co * MT + 8 * ci + (cr ^ (2 * (ci >> 2)))];
                     }
-                } else if (use_min) {  // warp-uniform: one instruction per conv value
+                    } else if (use_min) {  // warp-uniform: one instruction per conv value
 #pragma unroll
-                    for (int c = 0; c < NH; ++c) m[c] = min_nan(m[c], X3 ? a[c] + b[c] : a[c]);
-                } else {
+                        for (int c = 0; c < C::LDC; ++c) m[c0 + c] = min_nan(m[c0 + c], X3 ? a[c] + b[c] : a[c]);
+                    } else {
 #pragma unroll
-                    for (int c = 0; c < NH; ++c) m[c] = max_nan(m[c], X3 ? a[c] + b[c] : a[c]);
+                        for (int c = 0; c < C::LDC; ++c) m[c0 + c] = max_nan(m[c0 + c], X3 ? a[c] + b[c] : a[c]);
+                    }
                 }
+                if (!ok) break;
             }
             if (!ok) break;
             if constexpr (RAW) continue;
@@ -448,25 +469,26 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
                 for (int i = 0; i < NH / 2; ++i) res[i] = hbuf[i];
                 pwl = 2 * q + ((lane >> 4) & 1) + 8 * (lane & 7);  // base column 4q + 2*(l/16) + 16r
             }
-            float *stg = sStg + (k & 1) * C::STG;
+            const int sb = grp * 2 + (kk & 1);  // this group's staging buffer for the item
+            float *stg = sStg + sb * C::STG;
 #pragma unroll
             for (int i = 0; i < NRES; ++i) {
                 const int co = cbase + i;
                 const float tv = tanh_fast(res[i] + sCb[co]);
                 stg[co * C::PW + pwl] = __fadd_rn(__fmul_rn(tv, scale), sBias[co]);
             }
-            // all eight warps have staged this item (the other buffer is still
+            // the group's eight warps have staged this item (its other buffer is still
             // being read only by warps that have not reached this point)
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&bars.stg_full[k & 1]));
-            if (!mbar_wait_bounded(smem_u32(&bars.stg_full[k & 1]), (k >> 1) & 1)) {
+            if (lane == 0) mbar_arrive(smem_u32(&bars.stg_full[sb]));
+            if (!mbar_wait_bounded(smem_u32(&bars.stg_full[sb]), (kk >> 1) & 1)) {
                 fail();
                 break;
             }
             // thread et stores column pw of channels co0, co0 + CSTEP, ...: row-contiguous
             // warps, a pointer stride per store
-            constexpr int CSTEP = NEPI * 32 / C::PW;
-            const int et = tid - EPI_WARP0 * 32, pw = et % C::PW, co0 = et / C::PW;
+            constexpr int CSTEP = 8 * 32 / C::PW;
+            const int et = gw * 32 + lane, pw = et % C::PW, co0 = et / C::PW;
             const int pw0 = cur.cblk * C::PW;
             if (pw0 + pw < Wo) {
                 const long long cstride = (long long)Ho * Wo;
@@ -483,7 +505,7 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
     __syncthreads();
     if (warp == MMA_WARP) {
         tc::fence_after_sync();
-        tc::dealloc(tmem, NSLOT * SLOT_COLS);
+        tc::dealloc(tmem, TMEM_COLS);
     }
 }
 
@@ -503,7 +525,7 @@ fw_status launch_pn(const float *x, int Nimg, int H, int W, const float *w, cons
     const long long items = (long long)Nimg * Ho * ncb;
     const int grid = (int)(items < sms ? items : sms);
     const bool vec = W % 4 == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0;  // float4 input rows
-    convpool_tc_kernel<P, N, RAW, X3><<<grid, NTHREADS, smem, st>>>(x, w, cb, bias, scale, out, Nimg, H, W, Ho, Wo,
+    convpool_tc_kernel<P, N, RAW, X3><<<grid, C::NTHREADS, smem, st>>>(x, w, cb, bias, scale, out, Nimg, H, W, Ho, Wo,
                                                                     ncb, vec);
     note_launch();
     return launch_status(cudaGetLastError());
