@@ -87,6 +87,9 @@ struct Cfg {
     static constexpr int NST = 2;                     // slab ring stages
     // TMEM accumulator ring, one conv row per slot: [x*w_hi (+ x_lo*w_hi) | x_hi*w_lo]
     static constexpr int SLOT_COLS = X3 ? 128 : 64;
+    // Plain TF32 at N = 64: the three kh taps of a kw are stacked along N, so one
+    // MMA of an input row feeds up to three conv rows (adjacent slots) at once.
+    static constexpr bool STACK = !X3 && !RAW && N == SLOT_COLS;
     static constexpr int NSLOT = TMEM_COLS / SLOT_COLS;
     static_assert((X3 ? 2 : 1) * N <= SLOT_COLS && NSLOT <= MAX_SLOT, "slots");
     static constexpr int BTAP = ((X3 ? 2 : 1) * N / 8) * CORE;  // one tap of [w_hi | w_lo] (or w_hi)
@@ -188,11 +191,18 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
         sBias[i] = bias ? __ldg(bias + i) : 0.f;  // raw mode passes no bias
     }
     // Weights split into TF32 hi/lo: B[tap][co' / 8][plane][co' % 8][c4] with
-    // co' = co for w_hi and N + co for w_lo.
+    // co' = co for w_hi and N + co for w_lo.  Stacked form: B[kw][n' / 8][plane][n' % 8][c4]
+    // with n' = (2 - kh) * N + co (the kh blocks in descending order).
     for (int e = tid; e < 9 * CIN * N; e += NTHREADS) {
         const int co = e % N, t = e / N, ci = t % CIN, tap = t / CIN;
         const float v = __ldg(w + ((long long)co * CIN + ci) * 9 + tap);
         const float hi = tc::to_tf32(v), lo = tc::to_tf32(v - hi);
+        if constexpr (C::STACK) {
+            const int np = (2 - tap / 3) * N + co;
+            *reinterpret_cast<float *>(sB + (tap % 3) * 3 * C::BTAP + (np / 8) * CORE + (ci / 4) * 128 +
+                                       (np % 8) * 16 + (ci % 4) * 4) = hi;
+            continue;
+        }
         const int base = tap * C::BTAP + (ci / 4) * 128 + (ci % 4) * 4;
         *reinterpret_cast<float *>(sB + base + (co / 8) * CORE + (co % 8) * 16) = hi;
         if constexpr (X3) *reinterpret_cast<float *>(sB + base + ((N + co) / 8) * CORE + ((N + co) % 8) * 16) = lo;
@@ -333,6 +343,43 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
                 // addresses stay below 2^18).
                 const uint64_t a0 = tc::smem_desc(sSlab_addr + stage * C::SLAB, 128, CORE);
                 const uint64_t b0 = tc::smem_desc(sB_addr, 128, CORE);
+                if constexpr (C::STACK) {
+                    // Input row i feeds conv rows jlo..jhi (tap kh = i - j).  Conv row i
+                    // starts with its own kh = 0, kw = 0 MMA (accumulate off); the rows
+                    // before it take the stacked blocks kh = i - jlo .. 1 (kw = 0) or
+                    // .. i - jhi (kw = 1, 2) in one MMA, N = 64 per row.  Row i - 2 is
+                    // complete after input row i.
+                    constexpr int BKW = 3 * C::BTAP;          // one kw of the stacked weights
+#pragma unroll
+                    for (int i = 0; i < P + 2; ++i) {
+                        const int jlo = i < 2 ? 0 : i - 2, jhi = i < P - 1 ? i : P - 1;
+                        const bool fresh = i < P;
+                        if (fresh) {
+                            const int rc = rowc + i, slot = rc % C::NSLOT, sus = rc / C::NSLOT;
+                            if (sus > 0 && !mbar_wait_bounded(smem_u32(&bars.slot_empty[slot]), (sus - 1) & 1)) {
+                                fail();
+                                ok = false;
+                                break;
+                            }
+                            tc::fence_after_sync();
+                        }
+                        const uint32_t dlo = tmem + (uint32_t)(((rowc + jlo) % C::NSLOT) * C::SLOT_COLS);
+#pragma unroll
+                        for (int kw = 0; kw < 3; ++kw) {
+                            const uint64_t a = a0 + (uint64_t)((i * RB + kw * CORE) >> 4);
+                            const int top = fresh && kw == 0 ? i - 1 : jhi;  // last row of the stacked MMA
+                            if (fresh && kw == 0)
+                                tc::mma_tf32(tmem + (uint32_t)(((rowc + i) % C::NSLOT) * C::SLOT_COLS), a,
+                                             b0 + (uint64_t)((kw * BKW + 2 * C::BTAP) >> 4),
+                                             tc::idesc_tf32(128, N), 0u);
+                            if (top >= jlo)
+                                tc::mma_tf32(dlo, a, b0 + (uint64_t)((kw * BKW + (2 - (i - jlo)) * C::BTAP) >> 4),
+                                             tc::idesc_tf32(128, (top - jlo + 1) * N), 1u);
+                        }
+                        if (i >= 2) tc::commit(smem_u32(&bars.slot_full[(rowc + i - 2) % C::NSLOT]));
+                    }
+                    rowc += P;
+                } else {
 #pragma unroll
                 for (int j = 0; j < P; ++j, ++rowc) {
                     const int slot = rowc % C::NSLOT, sus = rowc / C::NSLOT;
@@ -352,6 +399,7 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
                         if constexpr (X3) tc::mma_tf32(d, al, bd, IDESC_LH, 1u);
                     }
                     tc::commit(smem_u32(&bars.slot_full[slot]));
+                }
                 }
                 tc::commit(smem_u32(&bars.slab_empty[stage]));
             }
