@@ -336,9 +336,11 @@ def run_gpu(args):
                                                       4, out=h_cp, workspace=hws_cp)
         specs.append(dict(name="convpool", work=cp_flops(N=n), unit="TFLOP/s", scale=1e12, bound="tensor",
                           run=lambda: op_cp(d, out_cp), e2e=lambda: host_cp(), out=h_cp,
-                          kernel="convpool_tc_kernel<4,64> (tcgen05 kind::tf32, 3xTF32 split as two MMAs "
-                                 "per tap, N = 128 [w_hi|w_lo] and N = 64: executed tensor FLOPs = 3 x "
-                                 "algorithmic)", source="convpool_tc.cu"))
+                          kernel=("convpool_tc_kernel<4,64,false,false> (tcgen05 kind::tf32, one TF32 product per "
+                                  "MAC, kh taps stacked along N, two epilogue groups)" if args.convpool_precision == "tf32"
+                                  else "convpool_tc_kernel<4,64,false,true> (tcgen05 kind::tf32, 3xTF32 split as two "
+                                       "MMAs per tap, N = 128 [w_hi|w_lo] and N = 64: executed tensor FLOPs = 3 x "
+                                       "algorithmic)"), source="convpool_tc.cu"))
     if mp:
         n = mp["x"].shape[0]
         out_mp = torch.empty(n, MP["C"], 511, 511, device=dev)
@@ -473,8 +475,9 @@ def run_gpu(args):
             tf_ms = med_ms(lambda: FW.fw_conv2d_tanh_scale_bias_maxpool_tf32(
                 d[("cp", "x")], d[("cp", "w")], d[("cp", "conv_b")], d[("cp", "bias")], CP["scale"], 4, out=out_tf))
             fusion["convpool_tf32"] = {"ms": tf_ms, "x3_ms": f_ms, "work_per_launch": cp_flops(N=n),
-                                       "kernel": "convpool_tc_kernel<4,64,false,false>: one kind::tf32 MMA "
-                                                 "(N = 64) per tap",
+                                       "kernel": "convpool_tc_kernel<4,64,false,false>: one TF32 product per MAC "
+                                                 "(kh taps stacked along N: 21 MMAs of N = 64..192 per item), two "
+                                                 "epilogue groups",
                                        "max_abs_diff_vs_x3": float((out_tf - out_cp).abs().max())}
             del out_tf
         if ct:
