@@ -9,8 +9,10 @@
 // v = hi + lo with hi = tf32(v) and lo = tf32(v - hi), and the product is
 // accumulated as hi*hi + lo*hi + hi*lo (the lo*lo term, ~2^-22 relative, is
 // dropped): three MMAs per K step, float32 accumulation in TMEM.  X3 = false
-// is the plain TF32 variant (one product, hi*hi, per K step; the 5e-3 bound the
-// pages set for a TF32 path): no lo planes are staged and one MMA runs per tap.
+// is the plain TF32 variant (one product, hi*hi, per K step, bounded at 5e-3: the
+// float32-on-TF32 mode the trace "Kimi-K2.6 l2_p91" describes for convolutions):
+// no lo planes are staged, and at N = 64 the three kh taps of a kw are stacked
+// along N so that one MMA of an input row feeds up to three conv rows.
 //
 // Work item = one pooled output row of one image and a block of 128 conv columns:
 //   * the P conv rows of the pooled row are P GEMMs, M = 128 columns, K = 9 taps x
@@ -28,10 +30,13 @@
 //     apart, M-adjacent ones 256 B apart) that the tensor cores read at full rate.
 //     Columns 16..17 + 16k appear twice (as rows 0/1 of core 16/17 too);
 //   * the weights, split into hi/lo in the CTA prologue, stay resident.
-// CTA roles (512 threads, one CTA per SM, persistent over items):
-//   warps 1-3, 13-15  producers: load and split a slab (two stages);
+// CTA roles (512 threads -- 768 for the plain TF32 variant -- one CTA per SM,
+// persistent over items):
+//   warps 1-3 and the last three  producers: load and split a slab (two stages);
 //   warp  0     allocates TMEM; one lane issues 2 x 9 MMAs per conv row;
-//   warps 4-11  epilogue, every warp on every conv row: warp w reads TMEM lane
+//   warps 4-11  epilogue (4-19: two groups of eight taking the items in turn in the
+//               plain TF32 variant), every warp of a group on every conv row of
+//               its items: warp w reads TMEM lane
 //               quarter w % 4 and half the channels; the max over the P rows of a
 //               window is kept in registers while the rows arrive, the max over
 //               its P columns (lanes 8 apart) by a butterfly that halves the
