@@ -111,6 +111,10 @@ struct Cfg {
     static constexpr int NTHREADS = (8 + NEPI) * 32;  // + MMA warp, 6 producers, 1 idle
     static constexpr int NH = N / 2;                  // channels per epilogue warp
     static constexpr int LDC = NGRP > 1 && NH % 16 == 0 ? 16 : NH;  // TMEM columns per load round
+    // Each group's items must map to slots of their own (item k -> slots (k*P .. k*P+P-1) % NSLOT):
+    // with shared slots a group one item ahead would wait on a slot barrier of the other group's
+    // phase and read its parity as complete.
+    static_assert(NGRP == 1 || NSLOT % (NGRP * P) == 0, "epilogue groups need disjoint TMEM slots");
     static constexpr size_t SMEM =
         (size_t)B_BYTES + NST * SLAB + 2 * NGRP * STG * 4 + 2 * N * 4 + sizeof(Bars);
     static_assert(NST <= MAX_STAGE, "slab ring");
