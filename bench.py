@@ -570,6 +570,8 @@ def run_gpu(args):
             v = fusion["convpool_tf32"]
             v["tflops"] = v["work_per_launch"] / (v["ms"] * 1e-3) / 1e12
             v["frac_of_tf32_peak"] = v["tflops"] / pk["tf32_tflops"]
+            line["convpool_tf32_tflops"] = v["tflops"]  # the plain-TF32 call, timed beside the step
+            line["convpool_tf32_tensor_frac"] = v["frac_of_tf32_peak"]
         line["fusion"] = fusion
     if args.only or args.batch or args.convt_layout != "nchw" or args.convpool_precision != "x3":
         line["config"]["subset"] = {"only": args.only, "batch": args.batch, "convt_layout": args.convt_layout,
