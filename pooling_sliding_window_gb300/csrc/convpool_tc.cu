@@ -527,12 +527,16 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
                 pwl = 2 * q + ((lane >> 4) & 1) + 8 * (lane & 7);  // base column 4q + 2*(l/16) + 16r
             }
             const int sb = grp * 2 + (kk & 1);  // this group's staging buffer for the item
+            // A pooled row is staged [channel][column] with the column rotated by rot(co): the lanes
+            // that hold the same window column for different channels (lane bits 3 and 4) then
+            // write different banks, and the row-order reads below stay conflict-free.
+            auto rot = [](int co) { return P == 4 ? (co / (NH / 4)) & 3 : 2 * ((co / (NH / 2)) & 1); };
             float *stg = sStg + sb * C::STG;
 #pragma unroll
             for (int i = 0; i < NRES; ++i) {
                 const int co = cbase + i;
                 const float tv = tanh_fast(res[i] + sCb[co]);
-                stg[co * C::PW + pwl] = __fadd_rn(__fmul_rn(tv, scale), sBias[co]);
+                stg[co * C::PW + ((pwl + rot(co)) & (C::PW - 1))] = __fadd_rn(__fmul_rn(tv, scale), sBias[co]);
             }
             // the group's eight warps have staged this item (its other buffer is still
             // being read only by warps that have not reached this point)
@@ -550,10 +554,12 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
             if (pw0 + pw < Wo) {
                 const long long cstride = (long long)Ho * Wo;
                 float *op = out + ((cur.n * N + co0) * Ho + cur.pr) * (long long)Wo + pw0 + pw;
-                const float *sp = stg + co0 * C::PW + pw;
                 static_assert(N % CSTEP == 0, "store passes");
 #pragma unroll
-                for (int i = 0; i < N / CSTEP; ++i, op += CSTEP * cstride, sp += CSTEP * C::PW) *op = *sp;
+                for (int i = 0; i < N / CSTEP; ++i, op += CSTEP * cstride) {
+                    const int co = co0 + i * CSTEP;
+                    *op = stg[co * C::PW + ((pw + rot(co)) & (C::PW - 1))];
+                }
             }
         }
     }
