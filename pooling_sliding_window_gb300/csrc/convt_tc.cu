@@ -188,8 +188,70 @@ convt_k4s2_tc_kernel(const float *__restrict__ x, const float *__restrict__ wtc,
         // are issued before the wait for the stage to be free, so their latency
         // overlaps the tensor cores still reading that stage.
         const long long plane_stride = (long long)H * W;
+        // x address of position q of the stacked sequence (nullptr: a zero position)
+        auto pos_src = [&](long long q) -> const float * {
+            if (q < 0 || q >= n_pos) return nullptr;
+            int R, c;
+            if (n_pos < 0x7fffffffLL) {
+                R = (int)q / BW;
+                c = (int)q - R * BW;
+            } else {
+                R = (int)(q / BW);
+                c = (int)(q - (long long)R * BW);
+            }
+            if (c >= W || R <= 0) return nullptr;
+            const int n = (R - 1) / BH;
+            const int row = R - 1 - n * BH;
+            return row < H ? x + (((long long)n * CIN) * H + row) * (long long)W + c : nullptr;
+        };
+        if (!NHWC && L <= PROD_WARPS * 32) {
+            // One position per thread and slab, software-pipelined: converting and storing
+            // channels 4g..4g+3 of this slab frees their registers, which then load the same
+            // channels of the thread's position in the next slab, so the next slab's loads
+            // are in flight while this one is stored.
+            auto slab_src = [&](int tile, int s) -> const float * {
+                const int dy_lo = nslab == 1 ? dy0 : tap_off(py, s);
+                const long long pbase = (long long)tile * MT + BW + (long long)dy_lo * BW + dx0;
+                return tid < L ? pos_src(pbase + tid) : nullptr;
+            };
+            float r[CIN];
+            {
+                const float *src = rank < n_tiles ? slab_src(rank, 0) : nullptr;
+#pragma unroll
+                for (int ci = 0; ci < CIN; ++ci) r[ci] = src ? __ldg(src + ci * plane_stride) : 0.f;
+            }
+            int k = 0;
+            for (int tile = rank; tile < n_tiles && !*abort_flag; tile += nct) {
+                for (int s = 0; s < nslab; ++s, ++k) {
+                    const int stage = k & 1, use = k >> 1;
+                    int ntile = tile, ns = s + 1;
+                    if (ns == nslab) {
+                        ns = 0;
+                        ntile += nct;
+                    }
+                    const float *nsrc = ntile < n_tiles ? slab_src(ntile, ns) : nullptr;
+                    if (use > 0 && !mbar_wait_bounded(smem_u32(&bars.slab_empty[stage]), (use - 1) & 1)) fail();
+                    unsigned char *slab = sSlab + stage * slab_bytes;
+                    if (tid < L) {
+#pragma unroll
+                        for (int g = 0; g < G; ++g) {
+                            *reinterpret_cast<float4 *>(slab + g * slab_plane + tid * 16) =
+                                make_float4(tc::to_tf32(r[4 * g]), tc::to_tf32(r[4 * g + 1]),
+                                            tc::to_tf32(r[4 * g + 2]), tc::to_tf32(r[4 * g + 3]));
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                r[4 * g + j] = nsrc ? __ldg(nsrc + (4 * g + j) * plane_stride) : 0.f;
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&bars.slab_full[stage]));
+                    if (*abort_flag) break;
+                }
+            }
+        }
         int k = 0;
-        for (int tile = rank; tile < n_tiles && !*abort_flag; tile += nct) {
+        for (int tile = rank; tile < n_tiles && !*abort_flag && (NHWC || L > PROD_WARPS * 32); tile += nct) {
             for (int s = 0; s < nslab; ++s, ++k) {
                 const int stage = k & 1, use = k >> 1;
                 const int dy_lo = nslab == 1 ? dy0 : tap_off(py, s);
