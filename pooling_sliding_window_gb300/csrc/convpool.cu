@@ -8,11 +8,14 @@
 // kernel without recomputation and the conv intermediate never leaves registers.
 //
 // Tiled FFMA kernel (KH = KW = 3, pool_s = pool_k in {2, 4}, Cin <= 16):
-//   * a CTA owns a 16 x 32 block of conv pixels (4x8 pooled outputs for pool 4,
-//     8x16 for pool 2) of one image and a block of up to 32 output channels;
+//   * a work item is a 16 x 32 block of conv pixels (4x8 pooled outputs for pool 4,
+//     8x16 for pool 2) of one image and a block of up to 32 output channels; CTAs
+//     are persistent over items;
 //   * the input tile (16+2) x (32+2) x Cin with its 3x3 halo and the block's
-//     weights are staged in shared memory (rows padded to 36 floats so every
-//     thread's 6-wide row segment is one 16-byte + one 8-byte load);
+//     weights are staged in shared memory by cp.async, two buffers deep: the next
+//     item's copies are in flight while the current item is computed (rows padded
+//     to 36 floats so every thread's 6-wide row segment is one 16-byte + one 8-byte
+//     load);
 //   * each thread accumulates a 4 x 4 conv-pixel block for 4 output channels
 //     (64 FP32 accumulators) -- an implicit GEMM with K = Cin*9 on the FMA pipe;
 //     a warp shares its 4 channels, so weight reads are shared-memory broadcasts;
@@ -42,101 +45,127 @@ template <int POOL>
 __global__ void __launch_bounds__(256, 2)
 convpool3x3_ffma_kernel(const float *__restrict__ x, const float *__restrict__ w,
                         const float *__restrict__ cb, const float *__restrict__ bias, float scale,
-                        float *__restrict__ out, int Cin, int H, int W, int Cout, int Ho, int Wo,
-                        int tiles_w, int cob) {
+                        float *__restrict__ out, int N, int Cin, int H, int W, int Cout, int Ho, int Wo,
+                        int tiles_w, int tiles, int ncob, int cob) {
     extern __shared__ __align__(16) float sm[];
-    float *xs = sm;                    // [Cin][XR][XP]
-    float *ws = sm + Cin * XR * XP;    // [Cin][9][cob]
-
+    // two staging buffers, each [Cin][XR][XP] input floats then [Cin][9][cob] weights
+    const int XS = Cin * XR * XP, BUF = XS + Cin * 9 * cob;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int n = blockIdx.z;
-    const int co0 = blockIdx.y * cob;
-    const int tr = blockIdx.x / tiles_w, tc = blockIdx.x - tr * tiles_w;
-    const int row0 = tr * TILE_R, col0 = tc * TILE_C;
+    const long long total = (long long)N * ncob * tiles;
+    // item = (n * ncob + co block) * tiles + tile
+    auto stage = [&](long long item, int b) {
+        const int tile = (int)(item % tiles);
+        const long long t = item / tiles;
+        const int co0 = (int)(t % ncob) * cob;
+        const long long n = t / ncob;
+        const int tr = tile / tiles_w, tcl = tile - tr * tiles_w;
+        const int row0 = tr * TILE_R, col0 = tcl * TILE_C;
+        const float *xn = x + n * Cin * H * W;
+        float *xsb = sm + b * BUF, *wsb = xsb + XS;
+        for (int e = tid; e < Cin * XR * XC; e += blockDim.x) {
+            const int c = e % XC, u = e / XC, r = u % XR, ci = u / XR;
+            const int ih = row0 + r, iw = col0 + c;
+            const bool ok = ih < H && iw < W;
+            cp_async4(smem_u32(xsb + (ci * XR + r) * XP + c), ok ? xn + ((long long)ci * H + ih) * W + iw : x,
+                      ok ? 4u : 0u);
+        }
+        for (int e = tid; e < Cin * 9 * cob; e += blockDim.x) {
+            const int j = e % cob, u = e / cob, tap = u % 9, ci = u / 9;
+            const int co = co0 + j;
+            const bool ok = co < Cout;
+            cp_async4(smem_u32(wsb + e), ok ? w + ((long long)co * Cin + ci) * 9 + tap : w, ok ? 4u : 0u);
+        }
+        cp_async_commit();
+    };
+    if (blockIdx.x < total) stage(blockIdx.x, 0);
+    int it = 0;
+    for (long long item = blockIdx.x; item < total; item += gridDim.x, ++it) {
+        const int b = it & 1;
+        if (item + gridDim.x < total)
+            stage(item + gridDim.x, b ^ 1);
+        else
+            cp_async_commit();  // an empty group keeps the wait count uniform
+        cp_async_wait<1>();     // this item's copies (of every thread, after the barrier) have landed
+        __syncthreads();
+        const float *xs = sm + b * BUF, *ws = xs + XS;
+        const int tile = (int)(item % tiles);
+        const long long tt = item / tiles;
+        const int co0 = (int)(tt % ncob) * cob;
+        const long long n = tt / ncob;
+        const int tr = tile / tiles_w, tcl = tile - tr * tiles_w;
+        const int row0 = tr * TILE_R, col0 = tcl * TILE_C;
 
-    const float *xn = x + (long long)n * Cin * H * W;
-    for (int e = tid; e < Cin * XR * XC; e += blockDim.x) {
-        const int c = e % XC, t = e / XC, r = t % XR, ci = t / XR;
-        const int ih = row0 + r, iw = col0 + c;
-        float v = 0.f;
-        if (ih < H && iw < W) v = __ldg(xn + ((long long)ci * H + ih) * W + iw);
-        xs[(ci * XR + r) * XP + c] = v;
-    }
-    for (int e = tid; e < Cin * 9 * cob; e += blockDim.x) {
-        const int j = e % cob, t = e / cob, tap = t % 9, ci = t / 9;
-        const int co = co0 + j;
-        ws[e] = co < Cout ? __ldg(w + ((long long)co * Cin + ci) * 9 + tap) : 0.f;
-    }
-    __syncthreads();
-
-    const int pr = lane >> 3, pc = lane & 7;  // 4x4 conv-pixel block (pr, pc)
-    const int cw = warp * 4;                  // this warp's channels [cw, cw+4) of the block
-    float acc[4][4][4];
+        const int pr = lane >> 3, pc = lane & 7;  // 4x4 conv-pixel block (pr, pc)
+        const int cw = warp * 4;                  // this warp's channels [cw, cw+4) of the block
+        float acc[4][4][4];
 #pragma unroll
-    for (int r = 0; r < 4; ++r)
+        for (int r = 0; r < 4; ++r)
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+            for (int c = 0; c < 4; ++c)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) acc[r][c][j] = 0.f;
+                for (int j = 0; j < 4; ++j) acc[r][c][j] = 0.f;
 
 #pragma unroll 2
-    for (int ci = 0; ci < Cin; ++ci) {
-        float xv[6][6];
-        const float *xr = xs + (ci * XR + 4 * pr) * XP + 4 * pc;
+        for (int ci = 0; ci < Cin; ++ci) {
+            float xv[6][6];
+            const float *xr = xs + (ci * XR + 4 * pr) * XP + 4 * pc;
 #pragma unroll
-        for (int r = 0; r < 6; ++r) {
-            const float4 a = *reinterpret_cast<const float4 *>(xr + r * XP);
-            const float2 b = *reinterpret_cast<const float2 *>(xr + r * XP + 4);
-            xv[r][0] = a.x; xv[r][1] = a.y; xv[r][2] = a.z; xv[r][3] = a.w;
-            xv[r][4] = b.x; xv[r][5] = b.y;
+            for (int r = 0; r < 6; ++r) {
+                const float4 a = *reinterpret_cast<const float4 *>(xr + r * XP);
+                const float2 b = *reinterpret_cast<const float2 *>(xr + r * XP + 4);
+                xv[r][0] = a.x; xv[r][1] = a.y; xv[r][2] = a.z; xv[r][3] = a.w;
+                xv[r][4] = b.x; xv[r][5] = b.y;
+            }
+            const float *wr = ws + ci * 9 * cob + cw;
+#pragma unroll
+            for (int kh = 0; kh < 3; ++kh)
+#pragma unroll
+                for (int kw = 0; kw < 3; ++kw) {
+                    const float4 wv = *reinterpret_cast<const float4 *>(wr + (kh * 3 + kw) * cob);
+#pragma unroll
+                    for (int r = 0; r < 4; ++r)
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const float xx = xv[r + kh][c + kw];
+                            acc[r][c][0] = fmaf(xx, wv.x, acc[r][c][0]);
+                            acc[r][c][1] = fmaf(xx, wv.y, acc[r][c][1]);
+                            acc[r][c][2] = fmaf(xx, wv.z, acc[r][c][2]);
+                            acc[r][c][3] = fmaf(xx, wv.w, acc[r][c][3]);
+                        }
+                }
         }
-        const float *wr = ws + ci * 9 * cob + cw;
-#pragma unroll
-        for (int kh = 0; kh < 3; ++kh)
-#pragma unroll
-            for (int kw = 0; kw < 3; ++kw) {
-                const float4 wv = *reinterpret_cast<const float4 *>(wr + (kh * 3 + kw) * cob);
-#pragma unroll
-                for (int r = 0; r < 4; ++r)
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const float xx = xv[r + kh][c + kw];
-                        acc[r][c][0] = fmaf(xx, wv.x, acc[r][c][0]);
-                        acc[r][c][1] = fmaf(xx, wv.y, acc[r][c][1]);
-                        acc[r][c][2] = fmaf(xx, wv.z, acc[r][c][2]);
-                        acc[r][c][3] = fmaf(xx, wv.w, acc[r][c][3]);
-                    }
-            }
-    }
 
-    // Window reduction + epilogue.  Pool windows tile the 4x4 block exactly.
-    constexpr int NW = 4 / POOL;  // windows per block side
-    const bool use_min = scale < 0.f;
+        // Window reduction + epilogue.  Pool windows tile the 4x4 block exactly.
+        constexpr int NW = 4 / POOL;  // windows per block side
+        const bool use_min = scale < 0.f;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int co = co0 + cw + j;
-        if (co >= Cout) continue;
-        const float cbv = cb ? __ldg(cb + co) : 0.f;
-        const float bv = __ldg(bias + co);
-        float *oc = out + ((long long)n * Cout + co) * Ho * Wo;
+        for (int j = 0; j < 4; ++j) {
+            const int co = co0 + cw + j;
+            if (co >= Cout) continue;
+            const float cbv = cb ? __ldg(cb + co) : 0.f;
+            const float bv = __ldg(bias + co);
+            float *oc = out + ((long long)n * Cout + co) * Ho * Wo;
 #pragma unroll
-        for (int wr_ = 0; wr_ < NW; ++wr_)
+            for (int wr_ = 0; wr_ < NW; ++wr_)
 #pragma unroll
-            for (int wc = 0; wc < NW; ++wc) {
-                float m = acc[wr_ * POOL][wc * POOL][j];
+                for (int wc = 0; wc < NW; ++wc) {
+                    float m = acc[wr_ * POOL][wc * POOL][j];
 #pragma unroll
-                for (int u = 0; u < POOL; ++u)
+                    for (int u = 0; u < POOL; ++u)
 #pragma unroll
-                    for (int v = 0; v < POOL; ++v) {
-                        if (u == 0 && v == 0) continue;
-                        const float y = acc[wr_ * POOL + u][wc * POOL + v][j];
-                        m = use_min ? min_update(m, y) : max_update(m, y);
-                    }
-                const int ph = (row0 + 4 * pr) / POOL + wr_;
-                const int pw = (col0 + 4 * pc) / POOL + wc;
-                if (ph < Ho && pw < Wo) oc[(long long)ph * Wo + pw] = epilogue(m, cbv, scale, bv);
-            }
+                        for (int v = 0; v < POOL; ++v) {
+                            if (u == 0 && v == 0) continue;
+                            const float y = acc[wr_ * POOL + u][wc * POOL + v][j];
+                            m = use_min ? min_update(m, y) : max_update(m, y);
+                        }
+                    const int ph = (row0 + 4 * pr) / POOL + wr_;
+                    const int pw = (col0 + 4 * pc) / POOL + wc;
+                    if (ph < Ho && pw < Wo) oc[(long long)ph * Wo + pw] = epilogue(m, cbv, scale, bv);
+                }
+        }
+        __syncthreads();  // buffer b is free for the item after next
     }
+    cp_async_wait<0>();
 }
 
 // One thread per pooled output: the window's conv values computed directly.
@@ -181,13 +210,22 @@ fw_status launch_tiled(const float *x, int N, int Cin, int H, int W, const float
     const int tiles_w = (Wo * POOL + TILE_C - 1) / TILE_C;
     const int cob = min(MAX_COB, (Cout + 3) / 4 * 4);
     const int threads = cob / 4 * 32;
-    const size_t smem = (size_t)Cin * (XR * XP + 9 * cob) * sizeof(float);
+    const size_t smem = 2 * (size_t)Cin * (XR * XP + 9 * cob) * sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(convpool3x3_ffma_kernel<POOL>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return launch_status(e);
-    dim3 grid(tiles_h * tiles_w, (Cout + cob - 1) / cob, N);
-    convpool3x3_ffma_kernel<POOL><<<grid, threads, smem, st>>>(x, w, cb, bias, scale, out, Cin, H, W,
-                                                              Cout, Ho, Wo, tiles_w, cob);
+    int dev = 0, sms = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, convpool3x3_ffma_kernel<POOL>, threads, smem) !=
+            cudaSuccess)
+        return FW_ERR_LAUNCH;
+    const int tiles = tiles_h * tiles_w, ncob = (Cout + cob - 1) / cob;
+    const long long total = (long long)N * ncob * tiles;
+    const long long cap = (long long)sms * (per_sm > 0 ? per_sm : 1);  // persistent: one wave
+    const int grid = (int)(total < cap ? total : cap);
+    convpool3x3_ffma_kernel<POOL><<<grid, threads, smem, st>>>(x, w, cb, bias, scale, out, N, Cin, H, W, Cout, Ho,
+                                                              Wo, tiles_w, tiles, ncob, cob);
     note_launch();
     return launch_status(cudaGetLastError());
 }
@@ -216,7 +254,7 @@ fw_status convpool_launch(const float *x, int N, int Cin, int H, int W, const fl
                           int pk, int ps, float *out, int Ho, int Wo, bool tf32, cudaStream_t st) {
     if (convpool_tc_eligible(Cin, Cout, KH, KW, pk, ps) && !convpool_force_ffma())
         return convpool_tc_launch(x, N, H, W, w, cb, Cout, scale, bias, pk, out, Ho, Wo, !tf32, st);
-    if (KH == 3 && KW == 3 && pk == ps && Cin <= MAX_CIN && N <= 65535 && (pk == 4 || pk == 2)) {
+    if (KH == 3 && KW == 3 && pk == ps && Cin <= MAX_CIN && (pk == 4 || pk == 2)) {
         if (pk == 4) return launch_tiled<4>(x, N, Cin, H, W, w, cb, Cout, scale, bias, out, Ho, Wo, st);
         return launch_tiled<2>(x, N, Cin, H, W, w, cb, Cout, scale, bias, out, Ho, Wo, st);
     }

@@ -103,6 +103,19 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
         : "memory");
 }
 
+// Asynchronous 4-byte global -> shared copy (cp.async): `valid` (4 or 0) bytes are read
+// from src and the rest of the destination is zero-filled (valid = 0 reads nothing; src
+// must still be a valid global address).  A thread sees its own copies once
+// cp_async_wait<n> has left at most n of its committed groups pending.
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src, uint32_t valid) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(valid) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 }  // namespace fw
 
 // ------------------------------------------------ tcgen05 (5th-gen tensor cores) --
