@@ -19,8 +19,8 @@
 //   * each thread accumulates a 4 x 4 conv-pixel block for 4 output channels
 //     (64 FP32 accumulators) -- an implicit GEMM with K = Cin*9 on the FMA pipe;
 //     a warp shares its 4 channels, so weight reads are shared-memory broadcasts;
-//   * the window max (min when scale < 0) is taken in registers, the conv bias
-//     is added, and tanh / scale / bias run once per pooled output.
+//   * the window max (min when scale < 0; max.NaN / min.NaN) is taken in registers,
+//     the conv bias is added, and tanh / scale / bias run once per pooled output.
 // Direct kernel: one thread per pooled output, every other shape.
 #include <cstdlib>
 
@@ -46,52 +46,72 @@ __global__ void __launch_bounds__(256, 2)
 convpool3x3_ffma_kernel(const float *__restrict__ x, const float *__restrict__ w,
                         const float *__restrict__ cb, const float *__restrict__ bias, float scale,
                         float *__restrict__ out, int N, int Cin, int H, int W, int Cout, int Ho, int Wo,
-                        int tiles_w, int tiles, int ncob, int cob) {
+                        int tiles_w, int tiles, int ncob, int cob, bool vec) {
     extern __shared__ __align__(16) float sm[];
-    // two staging buffers, each [Cin][XR][XP] input floats then [Cin][9][cob] weights
-    const int XS = Cin * XR * XP, BUF = XS + Cin * 9 * cob;
+    // The weights [Cin][9][cob] of this CTA's channel block (resident), then two input
+    // buffers [Cin][XR][XP].  CTA b serves channel block b % ncob; its items are the
+    // (image, tile) pairs j = b / ncob, b / ncob + gridDim.x / ncob, ...
+    const int XS = Cin * XR * XP, WSZ = Cin * 9 * cob;
+    float *ws = sm, *xbuf = sm + WSZ;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const long long total = (long long)N * ncob * tiles;
-    // item = (n * ncob + co block) * tiles + tile
-    auto stage = [&](long long item, int b) {
-        const int tile = (int)(item % tiles);
-        const long long t = item / tiles;
-        const int co0 = (int)(t % ncob) * cob;
-        const long long n = t / ncob;
+    const int co0 = (int)(blockIdx.x % ncob) * cob;
+    const long long per_block = (long long)N * tiles;
+    const int gstride = gridDim.x / ncob;
+    for (int e = tid; e < WSZ; e += blockDim.x) {
+        const int j = e % cob, u = e / cob, tap = u % 9, ci = u / 9;
+        const int co = co0 + j;
+        const bool ok = co < Cout;
+        cp_async4(smem_u32(ws + e), ok ? w + ((long long)co * Cin + ci) * 9 + tap : w, ok ? 4u : 0u);
+    }
+    // copies of item j's input tile into buffer b, zero-filled outside x: per staged row, eight
+    // 16-byte copies and two 4-byte ones when x rows are 16-byte aligned, else 34 4-byte ones
+    auto stage = [&](long long j, int b) {
+        const long long n = j / tiles;
+        const int tile = (int)(j - n * tiles);
         const int tr = tile / tiles_w, tcl = tile - tr * tiles_w;
         const int row0 = tr * TILE_R, col0 = tcl * TILE_C;
         const float *xn = x + n * Cin * H * W;
-        float *xsb = sm + b * BUF, *wsb = xsb + XS;
-        for (int e = tid; e < Cin * XR * XC; e += blockDim.x) {
-            const int c = e % XC, u = e / XC, r = u % XR, ci = u / XR;
-            const int ih = row0 + r, iw = col0 + c;
-            const bool ok = ih < H && iw < W;
-            cp_async4(smem_u32(xsb + (ci * XR + r) * XP + c), ok ? xn + ((long long)ci * H + ih) * W + iw : x,
-                      ok ? 4u : 0u);
-        }
-        for (int e = tid; e < Cin * 9 * cob; e += blockDim.x) {
-            const int j = e % cob, u = e / cob, tap = u % 9, ci = u / 9;
-            const int co = co0 + j;
-            const bool ok = co < Cout;
-            cp_async4(smem_u32(wsb + e), ok ? w + ((long long)co * Cin + ci) * 9 + tap : w, ok ? 4u : 0u);
+        float *xsb = xbuf + b * XS;
+        if (vec) {
+            for (int e = tid; e < Cin * XR * 10; e += blockDim.x) {
+                const int row = e / 10, k = e - row * 10, ci = row / XR, r = row - ci * XR;
+                const int ih = row0 + r;
+                const int c = k < 8 ? 4 * k : 24 + k;  // k = 8, 9: columns 32, 33
+                const bool ok = ih < H && col0 + c < W;  // W % 4 == 0: a 16-byte piece is all in or out
+                const float *src = ok ? xn + ((long long)ci * H + ih) * W + col0 + c : x;
+                if (k < 8)
+                    cp_async16(smem_u32(xsb + row * XP + c), src, ok ? 16u : 0u);
+                else
+                    cp_async4(smem_u32(xsb + row * XP + c), src, ok ? 4u : 0u);
+            }
+        } else {
+            for (int e = tid; e < Cin * XR * XC; e += blockDim.x) {
+                const int c = e % XC, u = e / XC, r = u % XR, ci = u / XR;
+                const int ih = row0 + r, iw = col0 + c;
+                const bool ok = ih < H && iw < W;
+                cp_async4(smem_u32(xsb + (ci * XR + r) * XP + c), ok ? xn + ((long long)ci * H + ih) * W + iw : x,
+                          ok ? 4u : 0u);
+            }
         }
         cp_async_commit();
     };
-    if (blockIdx.x < total) stage(blockIdx.x, 0);
+    const long long j0 = blockIdx.x / ncob;
+    if (j0 < per_block)
+        stage(j0, 0);  // (the weights' copies join this group)
+    else
+        cp_async_commit();
     int it = 0;
-    for (long long item = blockIdx.x; item < total; item += gridDim.x, ++it) {
+    for (long long j = j0; j < per_block; j += gstride, ++it) {
         const int b = it & 1;
-        if (item + gridDim.x < total)
-            stage(item + gridDim.x, b ^ 1);
+        if (j + gstride < per_block)
+            stage(j + gstride, b ^ 1);
         else
             cp_async_commit();  // an empty group keeps the wait count uniform
         cp_async_wait<1>();     // this item's copies (of every thread, after the barrier) have landed
         __syncthreads();
-        const float *xs = sm + b * BUF, *ws = xs + XS;
-        const int tile = (int)(item % tiles);
-        const long long tt = item / tiles;
-        const int co0 = (int)(tt % ncob) * cob;
-        const long long n = tt / ncob;
+        const float *xs = xbuf + b * XS;
+        const long long n = j / tiles;
+        const int tile = (int)(j - n * tiles);
         const int tr = tile / tiles_w, tcl = tile - tr * tiles_w;
         const int row0 = tr * TILE_R, col0 = tcl * TILE_C;
 
@@ -135,9 +155,30 @@ convpool3x3_ffma_kernel(const float *__restrict__ x, const float *__restrict__ w
                 }
         }
 
-        // Window reduction + epilogue.  Pool windows tile the 4x4 block exactly.
+        // Window reduction + epilogue.  Pool windows tile the 4x4 block exactly; the window
+        // extreme is max.NaN (min.NaN when scale < 0), one instruction per value.
         constexpr int NW = 4 / POOL;  // windows per block side
-        const bool use_min = scale < 0.f;
+        float mw[4][NW][NW];
+        auto reduce = [&](auto ext) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int wr_ = 0; wr_ < NW; ++wr_)
+#pragma unroll
+                    for (int wc = 0; wc < NW; ++wc) {
+                        float m = acc[wr_ * POOL][wc * POOL][j];
+#pragma unroll
+                        for (int u = 0; u < POOL; ++u)
+#pragma unroll
+                            for (int v = 0; v < POOL; ++v)
+                                if (u != 0 || v != 0) m = ext(m, acc[wr_ * POOL + u][wc * POOL + v][j]);
+                        mw[j][wr_][wc] = m;
+                    }
+        };
+        if (scale < 0.f)
+            reduce([](float a, float b) { return min_nan(a, b); });
+        else
+            reduce([](float a, float b) { return max_nan(a, b); });
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int co = co0 + cw + j;
@@ -149,18 +190,9 @@ convpool3x3_ffma_kernel(const float *__restrict__ x, const float *__restrict__ w
             for (int wr_ = 0; wr_ < NW; ++wr_)
 #pragma unroll
                 for (int wc = 0; wc < NW; ++wc) {
-                    float m = acc[wr_ * POOL][wc * POOL][j];
-#pragma unroll
-                    for (int u = 0; u < POOL; ++u)
-#pragma unroll
-                        for (int v = 0; v < POOL; ++v) {
-                            if (u == 0 && v == 0) continue;
-                            const float y = acc[wr_ * POOL + u][wc * POOL + v][j];
-                            m = use_min ? min_update(m, y) : max_update(m, y);
-                        }
                     const int ph = (row0 + 4 * pr) / POOL + wr_;
                     const int pw = (col0 + 4 * pc) / POOL + wc;
-                    if (ph < Ho && pw < Wo) oc[(long long)ph * Wo + pw] = epilogue(m, cbv, scale, bv);
+                    if (ph < Ho && pw < Wo) oc[(long long)ph * Wo + pw] = epilogue(mw[j][wr_][wc], cbv, scale, bv);
                 }
         }
         __syncthreads();  // buffer b is free for the item after next
@@ -210,7 +242,7 @@ fw_status launch_tiled(const float *x, int N, int Cin, int H, int W, const float
     const int tiles_w = (Wo * POOL + TILE_C - 1) / TILE_C;
     const int cob = min(MAX_COB, (Cout + 3) / 4 * 4);
     const int threads = cob / 4 * 32;
-    const size_t smem = 2 * (size_t)Cin * (XR * XP + 9 * cob) * sizeof(float);
+    const size_t smem = (size_t)Cin * (2 * XR * XP + 9 * cob) * sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(convpool3x3_ffma_kernel<POOL>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return launch_status(e);
@@ -221,11 +253,14 @@ fw_status launch_tiled(const float *x, int N, int Cin, int H, int W, const float
             cudaSuccess)
         return FW_ERR_LAUNCH;
     const int tiles = tiles_h * tiles_w, ncob = (Cout + cob - 1) / cob;
-    const long long total = (long long)N * ncob * tiles;
-    const long long cap = (long long)sms * (per_sm > 0 ? per_sm : 1);  // persistent: one wave
-    const int grid = (int)(total < cap ? total : cap);
+    const long long per_block = (long long)N * tiles;
+    long long per_cob = (long long)sms * (per_sm > 0 ? per_sm : 1) / ncob;  // persistent: one wave
+    if (per_cob < 1) per_cob = 1;
+    if (per_cob > per_block) per_cob = per_block;
+    const int grid = (int)(per_cob * ncob);
+    const bool vec = W % 4 == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0;
     convpool3x3_ffma_kernel<POOL><<<grid, threads, smem, st>>>(x, w, cb, bias, scale, out, N, Cin, H, W, Cout, Ho,
-                                                              Wo, tiles_w, tiles, ncob, cob);
+                                                              Wo, tiles_w, tiles, ncob, cob, vec);
     note_launch();
     return launch_status(cudaGetLastError());
 }

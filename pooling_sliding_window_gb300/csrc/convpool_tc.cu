@@ -120,19 +120,6 @@ struct Cfg {
     static_assert(NST <= MAX_STAGE, "slab ring");
 };
 
-// Window extreme of conv values: max.NaN / min.NaN, one instruction, a NaN
-// propagates.  The sign of a zero extreme is left to the hardware, which the
-// absolute-error bound of this operator cannot see (+0 and -0 differ by 0).
-__device__ __forceinline__ float max_nan(float a, float b) {
-    float r;
-    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
-    return r;
-}
-__device__ __forceinline__ float min_nan(float a, float b) {
-    float r;
-    asm("min.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
-    return r;
-}
 // Item index -> (image n, pooled row pr, column block cblk), item = (n*Ho + pr)*ncb + cblk,
 // advanced by the grid stride without a division per item (one at the start).
 struct ItemCursor {

@@ -46,6 +46,19 @@ __device__ __forceinline__ float max_update(float m, float v) {
 __device__ __forceinline__ float min_update(float m, float v) {
     return (m == m && !(v >= m)) ? v : m;
 }
+// One-instruction window extreme for the conv+pool epilogues: max.NaN / min.NaN (a NaN
+// propagates).  The sign of a zero extreme is left to the hardware, which that
+// operator's absolute-error bound cannot see (+0 and -0 differ by 0).
+__device__ __forceinline__ float max_nan(float a, float b) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ float min_nan(float a, float b) {
+    float r;
+    asm("min.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
 
 // ------------------------------------------------------------- mbarriers --
 
@@ -109,6 +122,10 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
 // cp_async_wait<n> has left at most n of its committed groups pending.
 __device__ __forceinline__ void cp_async4(uint32_t dst, const void *src, uint32_t valid) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(valid) : "memory");
+}
+// 16-byte variant: both addresses 16-byte aligned, `valid` 16 or 0.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
