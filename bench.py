@@ -480,6 +480,15 @@ def run_gpu(args):
                                                  "epilogue groups",
                                        "max_abs_diff_vs_x3": float((out_tf - out_cp).abs().max())}
             del out_tf
+            # the same operator on the float32 FMA pipe only (no tensor cores)
+            out_ff = torch.empty_like(out_cp)
+            ff_ms = med_ms(lambda: FW.fw_conv2d_tanh_scale_bias_maxpool_ffma(
+                d[("cp", "x")], d[("cp", "w")], d[("cp", "conv_b")], d[("cp", "bias")], CP["scale"], 4, out=out_ff))
+            fusion["convpool_ffma"] = {"ms": ff_ms, "work_per_launch": cp_flops(N=n),
+                                       "kernel": "convpool3x3_ffma_kernel<4>: persistent FP32-FMA implicit GEMM, "
+                                                 "4x4 conv pixels x 4 channels per thread, cp.async staging",
+                                       "max_abs_diff_vs_x3": float((out_ff - out_cp).abs().max())}
+            del out_ff
         if ct:
             n = ct["x"].shape[0]
             wsz = FW.fw_convt_unfused_workspace_size(n, CT["Cin"], CT["H"], CT["W"], CT["Cout"], 4, 2, 1, 1)
@@ -572,6 +581,12 @@ def run_gpu(args):
             v["frac_of_tf32_peak"] = v["tflops"] / pk["tf32_tflops"]
             line["convpool_tf32_tflops"] = v["tflops"]  # the plain-TF32 call, timed beside the step
             line["convpool_tf32_tensor_frac"] = v["frac_of_tf32_peak"]
+        if "convpool_ffma" in fusion:
+            v = fusion["convpool_ffma"]
+            v["tflops"] = v["work_per_launch"] / (v["ms"] * 1e-3) / 1e12
+            v["frac_of_fp32_peak"] = v["tflops"] / fp32_peak
+            line["convpool_ffma_tflops"] = v["tflops"]  # the FP32-FMA call, timed beside the step
+            line["convpool_ffma_fp32_frac"] = v["frac_of_fp32_peak"]
         line["fusion"] = fusion
     if args.only or args.batch or args.convt_layout != "nchw" or args.convpool_precision != "x3":
         line["config"]["subset"] = {"only": args.only, "batch": args.batch, "convt_layout": args.convt_layout,

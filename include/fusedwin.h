@@ -119,6 +119,20 @@ fw_status fw_conv2d_tanh_scale_bias_maxpool_tf32(const float *x, int N, int Cin,
                                                  int pool_k, int pool_s, float *out, void *stream);
 
 /*
+ * The same operator as fw_conv2d_tanh_scale_bias_maxpool computed on the float32
+ * FMA pipe only (no tensor cores): the implicit GEMM with K = Cin*9 that the trace
+ * "Kimi-K2.6 l2_p82" reasons about, float32 products and sums.  KH = KW = 3 and
+ * pool_s = pool_k in {2, 4} with Cin <= 16 take the tiled FMA kernel (persistent,
+ * 4x4 conv pixels x 4 channels per thread); other shapes take the direct kernel.
+ * Within 1e-5 of a float64 evaluation on the tested shapes.  Arguments, statuses,
+ * layout and ownership are those of fw_conv2d_tanh_scale_bias_maxpool.
+ */
+fw_status fw_conv2d_tanh_scale_bias_maxpool_ffma(const float *x, int N, int Cin, int H, int W,
+                                                 const float *w, const float *conv_b, int Cout,
+                                                 int KH, int KW, float scale, const float *bias,
+                                                 int pool_k, int pool_s, float *out, void *stream);
+
+/*
  * MaxPool2d (trace "Kimi-K2.6 l1_p42", problem statement and the -inf padding
  * semantics it quotes):
  *

@@ -282,13 +282,13 @@ static bool convpool_force_ffma() {
     return v;
 }
 
-// tf32 = true: the tensor-core kernel runs one TF32 product per K step (the other
-// kernels are float32 FMA either way).
+// mode 0: the tensor-core kernel with the 3xTF32 split where it applies; 1: the same
+// with one TF32 product per K step; 2: float32 FMA kernels only.
 fw_status convpool_launch(const float *x, int N, int Cin, int H, int W, const float *w,
                           const float *cb, int Cout, int KH, int KW, float scale, const float *bias,
-                          int pk, int ps, float *out, int Ho, int Wo, bool tf32, cudaStream_t st) {
-    if (convpool_tc_eligible(Cin, Cout, KH, KW, pk, ps) && !convpool_force_ffma())
-        return convpool_tc_launch(x, N, H, W, w, cb, Cout, scale, bias, pk, out, Ho, Wo, !tf32, st);
+                          int pk, int ps, float *out, int Ho, int Wo, int mode, cudaStream_t st) {
+    if (mode != 2 && convpool_tc_eligible(Cin, Cout, KH, KW, pk, ps) && !convpool_force_ffma())
+        return convpool_tc_launch(x, N, H, W, w, cb, Cout, scale, bias, pk, out, Ho, Wo, mode == 0, st);
     if (KH == 3 && KW == 3 && pk == ps && Cin <= MAX_CIN && (pk == 4 || pk == 2)) {
         if (pk == 4) return launch_tiled<4>(x, N, Cin, H, W, w, cb, Cout, scale, bias, out, Ho, Wo, st);
         return launch_tiled<2>(x, N, Cin, H, W, w, cb, Cout, scale, bias, out, Ho, Wo, st);

@@ -17,7 +17,7 @@ unsigned convt_tc_read_and_clear_error();
 unsigned convpool_tc_read_and_clear_error();
 fw_status convpool_launch(const float *x, int N, int Cin, int H, int W, const float *w, const float *cb,
                           int Cout, int KH, int KW, float scale, const float *bias, int pk, int ps,
-                          float *out, int Ho, int Wo, bool tf32, cudaStream_t st);
+                          float *out, int Ho, int Wo, int mode, cudaStream_t st);
 fw_status convt_launch(const float *x, int N, int Cin, int H, int W, const float *w, const float *cb,
                        int Cout, int k, int s, int p, int op, const float *bias, float scale, float *out,
                        int Ho, int Wo, void *ws, size_t ws_bytes, cudaStream_t st);
@@ -202,7 +202,7 @@ unsigned long long fw_convt_workspace_size(int Cin, int Cout, int k, int s, int 
 
 static fw_status conv_pool_call(const float *x, int N, int Cin, int H, int W, const float *w, const float *conv_b,
                                 int Cout, int KH, int KW, float scale, const float *bias, int pool_k, int pool_s,
-                                float *out, bool tf32, void *stream) {
+                                float *out, int mode, void *stream) {
     if (!x || !w || !bias || !out) return FW_ERR_NULL;
     if (N < 1 || Cin < 1 || Cout < 1) return FW_ERR_SHAPE;
     if (!std::isfinite(scale)) return FW_ERR_PARAM;
@@ -219,23 +219,28 @@ static fw_status conv_pool_call(const float *x, int N, int Cin, int H, int W, co
         overlaps(out, ob, conv_b, 4LL * Cout))
         return FW_ERR_ALIAS;
     return convpool_launch(x, N, Cin, H, W, w, conv_b, Cout, KH, KW, scale, bias, pool_k, pool_s, out, Ho, Wo,
-                           tf32, static_cast<cudaStream_t>(stream));
+                           mode, static_cast<cudaStream_t>(stream));
 }
 
 fw_status fw_conv2d_tanh_scale_bias_maxpool(const float *x, int N, int Cin, int H, int W, const float *w,
                                             const float *conv_b, int Cout, int KH, int KW, float scale,
                                             const float *bias, int pool_k, int pool_s, float *out,
                                             void *stream) {
-    return conv_pool_call(x, N, Cin, H, W, w, conv_b, Cout, KH, KW, scale, bias, pool_k, pool_s, out, false,
-                          stream);
+    return conv_pool_call(x, N, Cin, H, W, w, conv_b, Cout, KH, KW, scale, bias, pool_k, pool_s, out, 0, stream);
 }
 
 fw_status fw_conv2d_tanh_scale_bias_maxpool_tf32(const float *x, int N, int Cin, int H, int W, const float *w,
                                                  const float *conv_b, int Cout, int KH, int KW, float scale,
                                                  const float *bias, int pool_k, int pool_s, float *out,
                                                  void *stream) {
-    return conv_pool_call(x, N, Cin, H, W, w, conv_b, Cout, KH, KW, scale, bias, pool_k, pool_s, out, true,
-                          stream);
+    return conv_pool_call(x, N, Cin, H, W, w, conv_b, Cout, KH, KW, scale, bias, pool_k, pool_s, out, 1, stream);
+}
+
+fw_status fw_conv2d_tanh_scale_bias_maxpool_ffma(const float *x, int N, int Cin, int H, int W, const float *w,
+                                                 const float *conv_b, int Cout, int KH, int KW, float scale,
+                                                 const float *bias, int pool_k, int pool_s, float *out,
+                                                 void *stream) {
+    return conv_pool_call(x, N, Cin, H, W, w, conv_b, Cout, KH, KW, scale, bias, pool_k, pool_s, out, 2, stream);
 }
 
 fw_status fw_maxpool2d(const float *x, int N, int C, int H, int W, int k, int s, int p, int d, float *out,

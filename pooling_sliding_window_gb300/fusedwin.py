@@ -37,7 +37,8 @@ EXPORTS = ("fw_status_string", "fw_version", "fw_conv2d_pool_out_shape", "fw_max
            "fw_maxpool2d_host", "fw_maxpool2d_host_workspace_size",
            "fw_convtranspose2d_softmax_bias_scale_sigmoid_host",
            "fw_convtranspose2d_softmax_bias_scale_sigmoid_host_workspace_size",
-           "fw_convtranspose2d_softmax_bias_scale_sigmoid_nhwc", "fw_conv2d_tanh_scale_bias_maxpool_tf32")
+           "fw_convtranspose2d_softmax_bias_scale_sigmoid_nhwc", "fw_conv2d_tanh_scale_bias_maxpool_tf32",
+           "fw_conv2d_tanh_scale_bias_maxpool_ffma")
 
 
 class FusedWinError(RuntimeError):
@@ -68,7 +69,8 @@ def lib():
             f = getattr(L, name)
             f.restype = I
             f.argtypes = [I] * n + [IP, IP]
-        for name in ("fw_conv2d_tanh_scale_bias_maxpool", "fw_conv2d_tanh_scale_bias_maxpool_tf32"):
+        for name in ("fw_conv2d_tanh_scale_bias_maxpool", "fw_conv2d_tanh_scale_bias_maxpool_tf32",
+                     "fw_conv2d_tanh_scale_bias_maxpool_ffma"):
             getattr(L, name).restype = I
             getattr(L, name).argtypes = [P, I, I, I, I, P, P, I, I, I, F, P, I, I, P, P]
         L.fw_maxpool2d.restype = I
@@ -207,6 +209,11 @@ def fw_conv2d_tanh_scale_bias_maxpool(x, w, conv_b, bias, scale, pool_k, pool_s=
 def fw_conv2d_tanh_scale_bias_maxpool_tf32(x, w, conv_b, bias, scale, pool_k, pool_s=0, out=None):
     """The same operator with the convolution's products taken once in TF32 on the tensor-core shapes."""
     return _conv_pool("fw_conv2d_tanh_scale_bias_maxpool_tf32", x, w, conv_b, bias, scale, pool_k, pool_s, out)
+
+
+def fw_conv2d_tanh_scale_bias_maxpool_ffma(x, w, conv_b, bias, scale, pool_k, pool_s=0, out=None):
+    """The same operator on the float32 FMA pipe only (no tensor cores)."""
+    return _conv_pool("fw_conv2d_tanh_scale_bias_maxpool_ffma", x, w, conv_b, bias, scale, pool_k, pool_s, out)
 
 
 def _conv_pool(fname, x, w, conv_b, bias, scale, pool_k, pool_s, out):

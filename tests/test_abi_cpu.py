@@ -94,7 +94,8 @@ def test_operator_argument_errors_without_launch():
     # conv+pool
     args = lambda **kw: dict(dict(x=x, N=1, Cin=8, H=16, W=16, w=w, cb=None, Cout=4, KH=3, KW=3,
                                   scale=2.0, bias=b, pk=4, ps=0, out=o), **kw)
-    for fname in ("fw_conv2d_tanh_scale_bias_maxpool", "fw_conv2d_tanh_scale_bias_maxpool_tf32"):
+    for fname in ("fw_conv2d_tanh_scale_bias_maxpool", "fw_conv2d_tanh_scale_bias_maxpool_tf32",
+                  "fw_conv2d_tanh_scale_bias_maxpool_ffma"):
         f = getattr(L, fname)
         call = lambda a: f(a["x"], a["N"], a["Cin"], a["H"], a["W"], a["w"], a["cb"], a["Cout"], a["KH"], a["KW"],
                            a["scale"], a["bias"], a["pk"], a["ps"], a["out"], None)
