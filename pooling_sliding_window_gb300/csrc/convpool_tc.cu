@@ -59,9 +59,10 @@ constexpr int RB = NCORE * CORE;   // bytes of one staged input row (per split)
 constexpr int MAX_STAGE = 4;  // slab ring depth bound (Cfg::NST stages are used)
 // Warp roles.  A warp runs on SM sub-partition warp % 4 and reads TMEM lane quarter
 // warp % 4, so every sub-partition hosts epilogue warps; the MMA issuer (warp 0)
-// shares sub-partition 0 only with the two quarter-0 epilogue warps: busy warps on
-// the issuer's sub-partition slow MMA issue (measured: 2.3x with two FMA-bound
-// warps there, none with the same warps on the other three).
+// shares sub-partition 0 only with the quarter-0 epilogue warps (two; four in the
+// plain-TF32 variant) and the idle warp: busy warps on the issuer's sub-partition
+// slow MMA issue (measured: 2.3x with two FMA-bound warps there, none with the same
+// warps on the other three), so the producers run on sub-partitions 1-3.
 constexpr int MMA_WARP = 0;
 constexpr int EPI_WARP0 = 4;     // warps 4 .. 4 + NEPI - 1: epilogue
 constexpr int NPROD = 6;         // warps 1-3 and the last three: producers (the one before idles)
