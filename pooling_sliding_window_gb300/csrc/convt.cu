@@ -44,6 +44,12 @@ constexpr int OS_PITCH = COUT_T + 1;          // output transpose pitch (conflic
 // Tap tables of the k4 s2 p1 phase decomposition: for output parity q and tap
 // index t in {0, 1}: kernel index and input offset (ih = m + off).
 __host__ __device__ __forceinline__ int tap_k(int q, int t) { return q == 0 ? (t == 0 ? 1 : 3) : (t == 0 ? 0 : 2); }
+constexpr float LOG2E_F = 1.4426950408889634f;
+__device__ __forceinline__ float ex2_fast(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 __host__ __device__ __forceinline__ int tap_off(int q, int t) { return q == 0 ? (t == 0 ? 0 : -1) : (t == 0 ? 1 : 0); }
 
 __global__ void convt_prepack_kernel(const float *__restrict__ w, float *__restrict__ wp, int Cin,
@@ -89,17 +95,30 @@ convt_k4s2_ffma_kernel(const float *__restrict__ x, const float *__restrict__ wp
     for (int c0 = 0; c0 < Cin; c0 += CK) {
         const int ck = min(CK, Cin - c0);
         __syncthreads();  // previous chunk fully consumed
-        for (int e = tid; e < CK * XS_CHUNK; e += blockDim.x) {
-            const int c = e % T_N;
-            int t = e / T_N;
-            const int sx = t % 3;
-            t /= 3;
-            const int r = t % XS_ROWS, ci = t / XS_ROWS;
-            const int ih = m0 - 1 + r, iw = n0 + c + sx - 1;
-            float v = 0.f;
-            if (ci < ck && ih >= 0 && ih < H && iw >= 0 && iw < W)
-                v = __ldg(xn + ((long long)(c0 + ci) * H + ih) * W + iw);
-            xs[e] = v;
+        {
+            // element e = ((ci * XS_ROWS + r) * 3 + sx) * T_N + c of the chunk; with 256 threads
+            // and T_N = 16 a thread's column c stays fixed and each step adds 16 to
+            // (ci, r, sx) in mixed radix (16 = 5 * 3 + 1), so no division per element
+            static_assert(T_N == 16, "column per thread");
+            const int c = tid % T_N;
+            int t = tid / T_N, sx = t % 3, r = (t / 3) % XS_ROWS, ci = t / (3 * XS_ROWS);
+            for (int e = tid; e < CK * XS_CHUNK; e += 256) {
+                const int ih = m0 - 1 + r, iw = n0 + c + sx - 1;
+                float v = 0.f;
+                if (ci < ck && ih >= 0 && ih < H && iw >= 0 && iw < W)
+                    v = __ldg(xn + ((long long)(c0 + ci) * H + ih) * W + iw);
+                xs[e] = v;
+                sx += 1;
+                r += 5;
+                if (sx >= 3) {
+                    sx -= 3;
+                    r += 1;
+                }
+                if (r >= XS_ROWS) {
+                    r -= XS_ROWS;
+                    ci += 1;
+                }
+            }
         }
         {
             const float4 *src = reinterpret_cast<const float4 *>(wph + (long long)c0 * WS_CHUNK);
@@ -139,6 +158,10 @@ convt_k4s2_ffma_kernel(const float *__restrict__ x, const float *__restrict__ wp
         cbv[j] = cb ? __ldg(cb + co) : 0.f;
         bv[j] = __ldg(bias + co);
     }
+    // Exponentials in base 2 (ex2.approx) on log2(e)-scaled arguments and one reciprocal
+    // of the sum per pixel, as in the tensor-core kernel's epilogue (the softmax scales
+    // an error in its argument by p(1 - p) <= 1/4, so the result stays within 1e-5).
+    const float ks = -scale * LOG2E_F;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         float mx = -INFINITY;
@@ -152,17 +175,15 @@ convt_k4s2_ffma_kernel(const float *__restrict__ x, const float *__restrict__ wp
         float sum = 0.f;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            acc[i][j] = expf(acc[i][j] - mx);
+            acc[i][j] = ex2_fast((acc[i][j] - mx) * LOG2E_F);
             sum += acc[i][j];
         }
 #pragma unroll
         for (int o = 1; o < 16; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        const float kp = ks / sum;  // 2^(-(p + b) * scale * log2 e) = 2^(e * kp - b * scale * log2 e)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const float p = __fdiv_rn(acc[i][j], sum);
-            const float r = __fmul_rn(__fadd_rn(p, bv[j]), scale);
-            acc[i][j] = __fdiv_rn(1.f, 1.f + expf(-r));
-        }
+        for (int j = 0; j < 8; ++j)
+            acc[i][j] = __fdividef(1.f, 1.f + ex2_fast(fmaf(acc[i][j], kp, bv[j] * ks)));
     }
 
     // Transpose through shared memory, pixel-major with an odd pitch:
