@@ -37,7 +37,7 @@ constexpr int MAX_CIN = 16;
 constexpr int MAX_COB = 32;                       // output channels per CTA
 
 __device__ __forceinline__ float epilogue(float m, float cbv, float scale, float b) {
-    const float t = tanhf(m + cbv);
+    const float t = tanh_fast(m + cbv);
     return __fadd_rn(__fmul_rn(t, scale), b);
 }
 

@@ -72,7 +72,6 @@ __device__ __forceinline__ int producer_index(int warp, int nw) {
 }
 constexpr int TMEM_COLS = 512;   // all of the SM's tensor memory (one CTA per SM)
 constexpr int MAX_SLOT = 8;
-constexpr float LOG2E = 1.4426950408889634f;
 
 struct Bars {
     uint64_t slab_full[MAX_STAGE];
@@ -151,14 +150,6 @@ __device__ __forceinline__ float upd(float m, float v, bool use_min) {
     return use_min ? min_nan(m, v) : max_nan(m, v);
 }
 
-// tanh(z) = 1 - 2 / (1 + e^(2z)) with a base-2 exponential and a fast reciprocal:
-// absolute error a few 1e-7 over all z (e^(2z) overflows to inf for large z and
-// gives exactly 1; underflows to 0 for very negative z and gives exactly -1).
-__device__ __forceinline__ float tanh_fast(float z) {
-    float e;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(z * (2.f * LOG2E)));
-    return 1.f - __fdividef(2.f, 1.f + e);
-}
 
 // RAW = false: the fused operator.  RAW = true: the first kernel of the unfused
 // comparison path -- `out` receives y = conv(x) + conv_b for the P*Ho x P*Wo conv

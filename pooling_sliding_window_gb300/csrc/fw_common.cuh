@@ -60,6 +60,15 @@ __device__ __forceinline__ float min_nan(float a, float b) {
     return r;
 }
 
+// tanh(z) = 1 - 2 / (1 + e^(2z)) with a base-2 exponential and a fast reciprocal:
+// absolute error a few 1e-7 over all z (e^(2z) overflows to inf for large z and
+// gives exactly 1; underflows to 0 for very negative z and gives exactly -1).
+__device__ __forceinline__ float tanh_fast(float z) {
+    float e;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(z * 2.8853900817779268f));  // 2 log2(e)
+    return 1.f - __fdividef(2.f, 1.f + e);
+}
+
 // ------------------------------------------------------------- mbarriers --
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
