@@ -10,6 +10,12 @@
  *   fw_convtranspose2d_softmax_bias_scale_sigmoid -- trace "Kimi-K2.6 l2_p91":
  *        ConvTranspose2d(k, s, p, output_padding) -> softmax(dim=1) -> +bias -> *scale -> sigmoid
  *
+ * Variants, declared below the call they extend: *_tf32 and *_ffma (conv+pool on
+ * plain-TF32 tensor cores or on the float32 FMA pipe only), fw_maxpool2d_ex (ceil
+ * mode, argmax indices), *_unfused (the two-kernel design, for comparison),
+ * *_nhwc (channels-last conv-transpose), *_noalloc (conv-transpose without a
+ * caller workspace) and *_host (host buffers, copies pipelined with the kernels).
+ *
  * Conventions shared by every call:
  *   - Tensors are caller-owned device pointers to dense, contiguous NCHW float32
  *     (row-major, W fastest).  Pointers must be 4-byte aligned; 16-byte aligned
