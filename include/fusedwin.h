@@ -10,11 +10,12 @@
  *   fw_convtranspose2d_softmax_bias_scale_sigmoid -- trace "Kimi-K2.6 l2_p91":
  *        ConvTranspose2d(k, s, p, output_padding) -> softmax(dim=1) -> +bias -> *scale -> sigmoid
  *
- * Variants, declared below the call they extend: *_tf32 and *_ffma (conv+pool on
- * plain-TF32 tensor cores or on the float32 FMA pipe only), fw_maxpool2d_ex (ceil
- * mode, argmax indices), *_unfused (the two-kernel design, for comparison),
- * *_nhwc (channels-last conv-transpose), *_noalloc (conv-transpose without a
- * caller workspace) and *_host (host buffers, copies pipelined with the kernels).
+ * Variants, declared below the call they extend: *_tf32 (conv+pool on plain-TF32
+ * tensor cores), *_ffma (conv+pool or conv-transpose on the float32 FMA pipe
+ * only), fw_maxpool2d_ex (ceil mode, argmax indices), *_unfused (the two-kernel
+ * design, for comparison), *_nhwc (channels-last conv-transpose), *_noalloc
+ * (conv-transpose without a caller workspace) and *_host (host buffers, copies
+ * pipelined with the kernels).
  *
  * Conventions shared by every call:
  *   - Tensors are caller-owned device pointers to dense, contiguous NCHW float32
@@ -198,6 +199,17 @@ fw_status fw_maxpool2d_out_shape_ex(int H, int W, int k, int s, int p, int d, in
  * k = 4, s = 2, p = 1 and Cout = 128 take the phase-decomposed tiled kernel
  * (each output parity class is a 2x2 convolution); other arguments take a
  * direct one.
+ * Precision: with Cin in {8, 16, 32, 64} the tiled kernel runs on the tensor
+ * cores in TF32 (both operands rounded to 10 mantissa bits, float32
+ * accumulation), the mode the l2_p91 trace describes; its bound is 5e-3
+ * absolute.  An error dy in the conv-transpose output moves an output by at
+ * most |scale|/2 * p(1-p) * max|dy| (softmax slope p(1-p) per channel, doubled
+ * for the normaliser, times the sigmoid slope <= 1/4): on the [128,64,64,64]
+ * workload (unit-variance x, weights within +-1/32) the softmax is nearly flat
+ * (p ~ 1/128) and the result stays within 1e-5 of a float64 evaluation; inputs
+ * that make one channel dominate (x or w several times larger) reach a few
+ * 1e-4.  Other Cin take the float32 FMA kernels, as does
+ * fw_convtranspose2d_softmax_bias_scale_sigmoid_ffma for every shape.
  */
 fw_status fw_convtranspose2d_softmax_bias_scale_sigmoid(const float *x, int N, int Cin, int H, int W,
                                                         const float *w, const float *conv_b,
@@ -205,6 +217,22 @@ fw_status fw_convtranspose2d_softmax_bias_scale_sigmoid(const float *x, int N, i
                                                         const float *bias, float scale, float *out,
                                                         void *workspace, unsigned long long workspace_bytes,
                                                         void *stream);
+
+/*
+ * The same operator as fw_convtranspose2d_softmax_bias_scale_sigmoid (trace
+ * "Kimi-K2.6 l2_p91", model) on the float32 FMA pipe only: float32 products
+ * and sums, so its error does not grow with a sharp softmax (within 1e-5 of a
+ * float64 evaluation on the tested inputs, dominant channels included).
+ * k = 4, s = 2, p = 1, Cout = 128 take the tiled FMA kernel, other arguments
+ * the direct one.  Arguments, workspace, statuses, layout and ownership are
+ * those of fw_convtranspose2d_softmax_bias_scale_sigmoid.
+ */
+fw_status fw_convtranspose2d_softmax_bias_scale_sigmoid_ffma(const float *x, int N, int Cin, int H, int W,
+                                                             const float *w, const float *conv_b,
+                                                             int Cout, int k, int s, int p, int op,
+                                                             const float *bias, float scale, float *out,
+                                                             void *workspace, unsigned long long workspace_bytes,
+                                                             void *stream);
 
 /*
  * Channels-last variant (the l2_p91 trace considers the channels_last memory
@@ -241,7 +269,8 @@ unsigned long long fw_convt_workspace_size(int Cin, int Cout, int k, int s, int 
  *     bytes; 16*Cin*Cout*4 for the tiled k4 s2 p1 Cout=128 path, so Cin <= 128).
  *   - The first call on a device looks up the array's device address (with that
  *     device current) and caches it; make that first call before any stream
- *     capture.
+ *     capture.  A cudaDeviceReset on that device invalidates the cached address:
+ *     do not call this entry point on a device after resetting it.
  *   - Every call shares the one array and leaves its contents behind (each call
  *     rewrites all it reads, nothing has to start at zero); calls that overlap on
  *     the GPU -- on different streams, or from different host threads -- race on
@@ -265,7 +294,8 @@ fw_status fw_convtranspose2d_softmax_bias_scale_sigmoid_noalloc(const float *x, 
  * (and the conv-transpose weight rewrite).  The batch is split into up to 8
  * chunks of images; each chunk's host->device copy, operator launch (on
  * `stream`, through the device entry point above, so the same checks and kernels
- * apply) and device->host copy are pipelined on two copy streams the library
+ * apply; the conv-transpose's weight rewrite is made once, by the first chunk)
+ * and device->host copy are pipelined on two copy streams the library
  * creates once per device, so copies overlap the kernels of neighbouring chunks.
  * The call is ordered after earlier work on `stream`, and later work on `stream`
  * (e.g. a synchronisation) runs after the last output copy: out is complete once

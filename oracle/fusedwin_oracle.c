@@ -41,6 +41,12 @@
  *
  * Parity pins for every function here live in the CPU test-suite (brute force,
  * library special cases, closed forms, invariants, the adjoint identity).
+ *
+ * Threads.  The file is built twice from this one source: single-threaded (the
+ * oracle proper; the OpenMP pragmas are ignored) and with -fopenmp, which only
+ * spreads independent images / channels / planes over the host cores to time the
+ * definition at full size.  No pragma changes an operation or its order within
+ * an output, so both builds give bit-identical results.
  */
 #include <math.h>
 #include <stddef.h>
@@ -119,6 +125,7 @@ int oracle_conv2d(const float *x, long N, long Cin, long H, long W,
     long Ho = oracle_conv2d_out_size(H, KH, s, p);
     long Wo = oracle_conv2d_out_size(W, KW, s, p);
     if (Ho < 1 || Wo < 1) return ORACLE_EINVAL;
+#pragma omp parallel for collapse(2) schedule(dynamic)
     for (long n = 0; n < N; ++n)
         for (long co = 0; co < Cout; ++co)
             for (long oh = 0; oh < Ho; ++oh)
@@ -204,6 +211,7 @@ int oracle_maxpool2d(const float *x, long N, long C, long H, long W,
     long Ho = oracle_pool_out_size(H, k, s, p, d);
     long Wo = oracle_pool_out_size(W, k, s, p, d);
     if (Ho < 1 || Wo < 1) return ORACLE_EINVAL;
+#pragma omp parallel for schedule(dynamic)
     for (long nc = 0; nc < N * C; ++nc) {
         const float *plane = x + nc * H * W;
         for (long oh = 0; oh < Ho; ++oh)
@@ -257,6 +265,7 @@ int oracle_conv2d_tanh_scale_bias_maxpool(const float *x, long N, long Cin, long
     float *v = (float *)malloc(inter * sizeof(float));
     if (!y || !v) { free(y); free(v); return ORACLE_ENOMEM; }
     oracle_conv2d(x, N, Cin, H, W, w, cb, Cout, KH, KW, 1, 0, y);
+#pragma omp parallel for collapse(2) schedule(dynamic)
     for (long n = 0; n < N; ++n)
         for (long co = 0; co < Cout; ++co)
             for (long e = 0; e < Hc * Wc; ++e) {
@@ -279,10 +288,13 @@ int oracle_convt2d(const float *x, long N, long Cin, long H, long W,
                    long s, long p, long op, double *y) {
     long Ho = oracle_convt_out_size(H, K, s, p, op), Wo = oracle_convt_out_size(W, K, s, p, op);
     if (Ho < 1 || Wo < 1) return ORACLE_EINVAL;
+#pragma omp parallel for collapse(2) schedule(dynamic)
     for (long n = 0; n < N; ++n)
         for (long co = 0; co < Cout; ++co)
             for (long e = 0; e < Ho * Wo; ++e)
                 y[(n * Cout + co) * Ho * Wo + e] = cb ? (double)cb[co] : 0.0;
+    /* images are independent: each iteration writes only its own y[n] */
+#pragma omp parallel for schedule(dynamic)
     for (long n = 0; n < N; ++n)
         for (long ci = 0; ci < Cin; ++ci)
             for (long ih = 0; ih < H; ++ih)
@@ -372,17 +384,26 @@ int oracle_convtranspose2d_softmax_bias_scale_sigmoid(const float *x, long N, lo
     if (Ho < 1 || Wo < 1) return ORACLE_EINVAL;
     size_t plane = (size_t)Ho * Wo;
     double *y = (double *)malloc((size_t)N * Cout * plane * sizeof(double));
-    float *yc = (float *)malloc((size_t)Cout * sizeof(float));
-    float *oc = (float *)malloc((size_t)Cout * sizeof(float));
-    double *e = (double *)malloc((size_t)Cout * sizeof(double));
-    if (!y || !yc || !oc || !e) { free(y); free(yc); free(oc); free(e); return ORACLE_ENOMEM; }
+    if (!y) return ORACLE_ENOMEM;
     oracle_convt2d(x, N, Cin, H, W, w, cb, Cout, K, s, p, op, y);
-    for (long n = 0; n < N; ++n)
-        for (size_t q = 0; q < plane; ++q) {
-            for (long c = 0; c < Cout; ++c) yc[c] = (float)y[(n * Cout + c) * plane + q];
-            oracle_softmax_bias_scale_sigmoid_pixel(yc, Cout, bias, scale, e, oc);
-            for (long c = 0; c < Cout; ++c) out[(n * Cout + c) * plane + q] = oc[c];
+    int rc = ORACLE_OK;
+    /* per-image scratch, so that images are independent */
+#pragma omp parallel for schedule(dynamic)
+    for (long n = 0; n < N; ++n) {
+        float *yc = (float *)malloc((size_t)Cout * sizeof(float));
+        float *oc = (float *)malloc((size_t)Cout * sizeof(float));
+        double *e = (double *)malloc((size_t)Cout * sizeof(double));
+        if (!yc || !oc || !e) {
+            rc = ORACLE_ENOMEM;
+        } else {
+            for (size_t q = 0; q < plane; ++q) {
+                for (long c = 0; c < Cout; ++c) yc[c] = (float)y[(n * Cout + c) * plane + q];
+                oracle_softmax_bias_scale_sigmoid_pixel(yc, Cout, bias, scale, e, oc);
+                for (long c = 0; c < Cout; ++c) out[(n * Cout + c) * plane + q] = oc[c];
+            }
         }
-    free(y); free(yc); free(oc); free(e);
-    return ORACLE_OK;
+        free(yc); free(oc); free(e);
+    }
+    free(y);
+    return rc;
 }

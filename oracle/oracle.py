@@ -21,23 +21,33 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "fusedwin_oracle.c")
 _LIB = os.path.join(_HERE, "_build", "liboracle.so")
+_LIB_OMP = os.path.join(_HERE, "_build", "liboracle_omp.so")
 _lock = threading.Lock()
 _lib = None
+_lib_omp = None
 
 _f32p = np.ctypeslib.ndpointer(dtype=np.float32, flags="C_CONTIGUOUS")
 _f64p = np.ctypeslib.ndpointer(dtype=np.float64, flags="C_CONTIGUOUS")
 _L = C.c_long
 
 
-def build(force: bool = False) -> str:
-    """Compile the oracle into ``oracle/_build/liboracle.so`` (if stale)."""
-    os.makedirs(os.path.dirname(_LIB), exist_ok=True)
-    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
-        tmp = _LIB + f".{os.getpid()}.tmp"
+def build(force: bool = False, openmp: bool = False) -> str:
+    """Compile the oracle into ``oracle/_build/liboracle.so`` (if stale).
+
+    ``openmp=True`` builds the same source with ``-fopenmp`` into
+    ``liboracle_omp.so``: its pragmas spread independent images, channels and planes
+    over the host cores (used only to time the definition at full size); nothing
+    else differs, and the results are bit-identical to the single-threaded build.
+    """
+    out = _LIB_OMP if openmp else _LIB
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    if force or not os.path.exists(out) or os.path.getmtime(out) < os.path.getmtime(_SRC):
+        tmp = out + f".{os.getpid()}.tmp"
         subprocess.run(["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math",
-                        "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"], check=True)
-        os.replace(tmp, _LIB)
-    return _LIB
+                        *(["-fopenmp"] if openmp else []), "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"],
+                       check=True)
+        os.replace(tmp, out)
+    return out
 
 
 def _ptr_or_null(a):
@@ -91,9 +101,15 @@ def load(path: str):
     return L
 
 
-def lib():
-    global _lib
+def lib(openmp: bool = False):
+    """The loaded oracle library (``openmp=True``: the multi-threaded build; its
+    thread count is fixed by OMP_NUM_THREADS when it is first loaded)."""
+    global _lib, _lib_omp
     with _lock:
+        if openmp:
+            if _lib_omp is None:
+                _lib_omp = load(build(openmp=True))
+            return _lib_omp
         if _lib is None:
             _lib = load(build())
     return _lib
@@ -162,14 +178,14 @@ def convt2d_one(x, w, cb, stride, pad, n, co, oh, ow):
 
 # -------------------------------------------------------------- operators --
 
-def maxpool2d(x, k, s=None, p=0, d=1):
+def maxpool2d(x, k, s=None, p=0, d=1, openmp=False):
     """MaxPool2d (floor mode, -inf padding): float32 out."""
     x = _f32(x)
     s = k if s is None else s
     N, Cc, H, W = x.shape
     Ho, Wo = pool_out_size(H, k, s, p, d), pool_out_size(W, k, s, p, d)
     out = np.empty((N, Cc, max(Ho, 0), max(Wo, 0)), dtype=np.float32)
-    _check(lib().oracle_maxpool2d(x, N, Cc, H, W, k, s, p, d, out))
+    _check(lib(openmp).oracle_maxpool2d(x, N, Cc, H, W, k, s, p, d, out))
     return out
 
 
@@ -201,7 +217,7 @@ def maxpool2d_at(x, k, s, p, d, n, c, oh, ow):
                                                  H, W, k, s, p, d, oh, ow))
 
 
-def conv2d_tanh_scale_bias_maxpool(x, w, cb, scale, bias, pool_k, pool_s=None):
+def conv2d_tanh_scale_bias_maxpool(x, w, cb, scale, bias, pool_k, pool_s=None, openmp=False):
     """The conv -> tanh -> *scale -> +bias -> MaxPool2d model, stage by stage."""
     x, w, bias = _f32(x), _f32(w), _f32(bias).reshape(-1)
     cb = None if cb is None else _f32(cb)
@@ -211,7 +227,7 @@ def conv2d_tanh_scale_bias_maxpool(x, w, cb, scale, bias, pool_k, pool_s=None):
     Ho = pool_out_size(conv2d_out_size(H, KH), pool_k, pool_s)
     Wo = pool_out_size(conv2d_out_size(W, KW), pool_k, pool_s)
     out = np.empty((N, Cout, max(Ho, 0), max(Wo, 0)), dtype=np.float32)
-    _check(lib().oracle_conv2d_tanh_scale_bias_maxpool(x, N, Cin, H, W, w, _ptr_or_null(cb), Cout,
+    _check(lib(openmp).oracle_conv2d_tanh_scale_bias_maxpool(x, N, Cin, H, W, w, _ptr_or_null(cb), Cout,
                                                        KH, KW, scale, bias, pool_k, pool_s, out))
     return out
 
@@ -246,7 +262,7 @@ def softmax_bias_scale_sigmoid_pixel(y, bias, scale):
 
 
 def convtranspose2d_softmax_bias_scale_sigmoid(x, w, cb, bias, scale, stride=2, pad=1,
-                                               output_padding=1):
+                                               output_padding=1, openmp=False):
     """The convT -> softmax(dim 1) -> +bias -> *scale -> sigmoid model."""
     x, w, bias = _f32(x), _f32(w), _f32(bias).reshape(-1)
     cb = None if cb is None else _f32(cb)
@@ -255,7 +271,7 @@ def convtranspose2d_softmax_bias_scale_sigmoid(x, w, cb, bias, scale, stride=2, 
     Ho = convt_out_size(H, K, stride, pad, output_padding)
     Wo = convt_out_size(W, K, stride, pad, output_padding)
     out = np.empty((N, Cout, Ho, Wo), dtype=np.float32)
-    _check(lib().oracle_convtranspose2d_softmax_bias_scale_sigmoid(
+    _check(lib(openmp).oracle_convtranspose2d_softmax_bias_scale_sigmoid(
         x, N, Cin, H, W, w, _ptr_or_null(cb), Cout, K, stride, pad, output_padding, bias, scale, out))
     return out
 

@@ -273,26 +273,33 @@ bool force_ffma() {
 
 bool convt_tc_eligible(int Cin, int Cout, int k, int s, int p);
 fw_status convt_tc_launch(const float *x, int N, int Cin, int H, int W, const float *w, const float *cb,
-                          const float *bias, float scale, float *out, int Ho, int Wo, void *ws, cudaStream_t st);
+                          const float *bias, float scale, float *out, int Ho, int Wo, void *ws, cudaStream_t st,
+                          bool prepack);
 
 size_t convt_workspace_bytes(int Cin, int Cout, int k, int s, int p) {
     if (k == 4 && s == 2 && p == 1 && Cout == COUT_T) return (size_t)16 * Cin * Cout * sizeof(float);
     return 0;
 }
 
+// ffma = true keeps the call on the FP32-FMA kernels (tiled, else direct).
+// weights_ready = true: the workspace already holds the weight rewrite of these
+// arguments (written by an earlier call on the same stream), so it is not redone.
 fw_status convt_launch(const float *x, int N, int Cin, int H, int W, const float *w, const float *cb,
                        int Cout, int k, int s, int p, int op, const float *bias, float scale, float *out,
-                       int Ho, int Wo, void *ws, size_t ws_bytes, cudaStream_t st) {
+                       int Ho, int Wo, void *ws, size_t ws_bytes, bool ffma, bool weights_ready, cudaStream_t st) {
     const size_t need = convt_workspace_bytes(Cin, Cout, k, s, p);
     if (need > 0) {
         if (!ws || ws_bytes < need) return FW_ERR_NULL;
-        if (convt_tc_eligible(Cin, Cout, k, s, p) && !force_ffma())
-            return convt_tc_launch(x, N, Cin, H, W, w, cb, bias, scale, out, Ho, Wo, ws, st);
+        if (!ffma && convt_tc_eligible(Cin, Cout, k, s, p) && !force_ffma())
+            return convt_tc_launch(x, N, Cin, H, W, w, cb, bias, scale, out, Ho, Wo, ws, st, !weights_ready);
         float *wp = static_cast<float *>(ws);
-        convt_prepack_kernel<<<(unsigned)min(1024LL, (16LL * Cin * Cout + 255) / 256), 256, 0, st>>>(w, wp, Cin, Cout);
-        note_launch();
-        fw_status rc = launch_status(cudaGetLastError());
-        if (rc != FW_OK) return rc;
+        if (!weights_ready) {
+            convt_prepack_kernel<<<(unsigned)min(1024LL, (16LL * Cin * Cout + 255) / 256), 256, 0, st>>>(w, wp, Cin,
+                                                                                                         Cout);
+            note_launch();
+            const fw_status rc = launch_status(cudaGetLastError());
+            if (rc != FW_OK) return rc;
+        }
         const int Mp = (Ho + 1) / 2, Np = (Wo + 1) / 2;  // phase-grid extent (phase 0)
         const int tiles_m = (Mp + T_M - 1) / T_M, tiles_n = (Np + T_N - 1) / T_N;
         const size_t smem = (size_t)CK * (XS_CHUNK + WS_CHUNK) * sizeof(float);

@@ -39,9 +39,14 @@
 // bias of the accumulators is conv_b * log2(e), so an accumulator holds
 // z = (conv-transpose + conv_b) * log2(e) directly.  The phase's weights (2*Cin KB)
 // stay resident in shared memory.
-// TF32 operands (10-bit mantissa) are enough here: the channel softmax scales an
-// error dy in the conv-transpose output by p(1-p) <= 1/4 and then by the sigmoid
-// slope times the scale, so the result stays within 1e-5 of the float64 oracle.
+// TF32 operands (10-bit mantissa), float32 accumulation: an error dy in the
+// conv-transpose output moves out_c by at most sigma' * |scale| * |dp_c| with
+// |dp_c| = p_c |dy_c - sum_j p_j dy_j| <= 2 p_c (1 - p_c) max|dy| and sigma' <= 1/4,
+// i.e. by |scale|/2 * p_c(1-p_c) * max|dy|.  With unit-variance x and weights within
+// +-1/32 (the l2_p91 workload) the softmax is nearly flat (p ~ 1/128) and the result
+// stays within 1e-5 of the float64 oracle; logits a few times larger, or one
+// dominant channel, give errors of a few 1e-4, inside the 5e-3 bound of the TF32
+// path.  The float32 FMA kernels (convt.cu) keep 1e-5 for any softmax.
 #include "fw_common.cuh"
 
 namespace fw {
@@ -580,15 +585,20 @@ bool convt_tc_eligible(int Cin, int Cout, int k, int s, int p) {
 
 namespace {
 
+// prepack = false: the workspace already holds this call's weight rewrite (an earlier
+// launch on the same stream wrote it), so only the main kernel runs.
 template <bool RAW, bool NHWC = false>
 fw_status tc_launch(const float *x, int N, int Cin, int H, int W, const float *w, const float *cb,
-                    const float *bias, float scale, float *out, int Ho, int Wo, void *ws, cudaStream_t st) {
+                    const float *bias, float scale, float *out, int Ho, int Wo, void *ws, cudaStream_t st,
+                    bool prepack = true) {
     float *wtc = static_cast<float *>(ws);
-    const long long total = 16LL * Cin * COUT;
-    convt_tc_prepack_kernel<<<(unsigned)min(1024LL, (total + 255) / 256), 256, 0, st>>>(w, wtc, Cin);
-    note_launch();
-    fw_status rc = launch_status(cudaGetLastError());
-    if (rc != FW_OK) return rc;
+    if (prepack) {
+        const long long total = 16LL * Cin * COUT;
+        convt_tc_prepack_kernel<<<(unsigned)min(1024LL, (total + 255) / 256), 256, 0, st>>>(w, wtc, Cin);
+        note_launch();
+        const fw_status rc = launch_status(cudaGetLastError());
+        if (rc != FW_OK) return rc;
+    }
     switch (Cin) {
         case 8: return launch_g<2, RAW, NHWC>(x, N, H, W, wtc, cb, bias, scale, out, Ho, Wo, st);
         case 16: return launch_g<4, RAW, NHWC>(x, N, H, W, wtc, cb, bias, scale, out, Ho, Wo, st);
@@ -631,8 +641,9 @@ __global__ void __launch_bounds__(256) softmax_bias_scale_sigmoid_kernel(const f
 }  // namespace
 
 fw_status convt_tc_launch(const float *x, int N, int Cin, int H, int W, const float *w, const float *cb,
-                          const float *bias, float scale, float *out, int Ho, int Wo, void *ws, cudaStream_t st) {
-    return tc_launch<false>(x, N, Cin, H, W, w, cb, bias, scale, out, Ho, Wo, ws, st);
+                          const float *bias, float scale, float *out, int Ho, int Wo, void *ws, cudaStream_t st,
+                          bool prepack) {
+    return tc_launch<false>(x, N, Cin, H, W, w, cb, bias, scale, out, Ho, Wo, ws, st, prepack);
 }
 
 // Channels-last: x [N, H, W, Cin], out [N, Ho, Wo, 128] (out 32-byte aligned).

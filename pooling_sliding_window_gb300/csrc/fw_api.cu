@@ -20,7 +20,7 @@ fw_status convpool_launch(const float *x, int N, int Cin, int H, int W, const fl
                           float *out, int Ho, int Wo, int mode, cudaStream_t st);
 fw_status convt_launch(const float *x, int N, int Cin, int H, int W, const float *w, const float *cb,
                        int Cout, int k, int s, int p, int op, const float *bias, float scale, float *out,
-                       int Ho, int Wo, void *ws, size_t ws_bytes, cudaStream_t st);
+                       int Ho, int Wo, void *ws, size_t ws_bytes, bool ffma, bool weights_ready, cudaStream_t st);
 size_t convt_workspace_bytes(int Cin, int Cout, int k, int s, int p);
 bool convpool_tc_eligible(int Cin, int Cout, int KH, int KW, int pk, int ps);
 fw_status convpool_tc_launch_raw(const float *x, int N, int H, int W, const float *w, const float *cb, int Cout,
@@ -278,11 +278,14 @@ fw_status fw_maxpool2d_ex(const float *x, int N, int C, int H, int W, int k, int
     return maxpool2d_ex_launch(x, (long long)N * C, H, W, k, s, p, d, Ho, Wo, out, indices, st);
 }
 
-fw_status fw_convtranspose2d_softmax_bias_scale_sigmoid(const float *x, int N, int Cin, int H, int W,
-                                                        const float *w, const float *conv_b, int Cout,
-                                                        int k, int s, int p, int op, const float *bias,
-                                                        float scale, float *out, void *workspace,
-                                                        unsigned long long workspace_bytes, void *stream) {
+}  // extern "C"
+
+// The conv-transpose entry points' checks and dispatch.  weights_ready: see
+// convt_launch (the host-buffer call sets it for every chunk after the first).
+fw_status fw::convt_call(const float *x, int N, int Cin, int H, int W, const float *w, const float *conv_b,
+                         int Cout, int k, int s, int p, int op, const float *bias, float scale, float *out,
+                         void *workspace, unsigned long long workspace_bytes, bool ffma, bool weights_ready,
+                         void *stream) {
     if (!x || !w || !bias || !out) return FW_ERR_NULL;
     if (N < 1 || Cin < 1 || Cout < 1) return FW_ERR_SHAPE;
     if (Cout > 1024) return FW_ERR_UNSUPPORTED;
@@ -303,10 +306,33 @@ fw_status fw_convtranspose2d_softmax_bias_scale_sigmoid(const float *x, int N, i
     if (overlaps(out, ob, x, nx * 4) || overlaps(out, ob, w, nw * 4) || overlaps(out, ob, bias, 4LL * Cout) ||
         overlaps(out, ob, conv_b, 4LL * Cout) || (need && overlaps(out, ob, workspace, (long long)need)))
         return FW_ERR_ALIAS;
-    if (need && (overlaps(workspace, (long long)need, x, nx * 4) || overlaps(workspace, (long long)need, w, nw * 4)))
+    // The weight rewrite into the workspace runs before the main kernel reads any input.
+    if (need && (overlaps(workspace, (long long)need, x, nx * 4) || overlaps(workspace, (long long)need, w, nw * 4) ||
+                 overlaps(workspace, (long long)need, bias, 4LL * Cout) ||
+                 overlaps(workspace, (long long)need, conv_b, 4LL * Cout)))
         return FW_ERR_ALIAS;
     return convt_launch(x, N, Cin, H, W, w, conv_b, Cout, k, s, p, op, bias, scale, out, Ho, Wo, workspace,
-                        (size_t)workspace_bytes, static_cast<cudaStream_t>(stream));
+                        (size_t)workspace_bytes, ffma, weights_ready, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" {
+
+fw_status fw_convtranspose2d_softmax_bias_scale_sigmoid(const float *x, int N, int Cin, int H, int W,
+                                                        const float *w, const float *conv_b, int Cout,
+                                                        int k, int s, int p, int op, const float *bias,
+                                                        float scale, float *out, void *workspace,
+                                                        unsigned long long workspace_bytes, void *stream) {
+    return convt_call(x, N, Cin, H, W, w, conv_b, Cout, k, s, p, op, bias, scale, out, workspace, workspace_bytes,
+                      false, false, stream);
+}
+
+fw_status fw_convtranspose2d_softmax_bias_scale_sigmoid_ffma(const float *x, int N, int Cin, int H, int W,
+                                                             const float *w, const float *conv_b, int Cout,
+                                                             int k, int s, int p, int op, const float *bias,
+                                                             float scale, float *out, void *workspace,
+                                                             unsigned long long workspace_bytes, void *stream) {
+    return convt_call(x, N, Cin, H, W, w, conv_b, Cout, k, s, p, op, bias, scale, out, workspace, workspace_bytes,
+                      true, false, stream);
 }
 
 unsigned long long fw_conv2d_pool_unfused_workspace_size(int N, int H, int W, int Cout, int KH, int KW,

@@ -25,6 +25,11 @@ constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;  // 2 s
 void note_launch(int n = 1);
 fw_status launch_status(cudaError_t e);
 
+// Checks and dispatch of the conv-transpose entry points (fw_api.cu).
+fw_status convt_call(const float *x, int N, int Cin, int H, int W, const float *w, const float *conv_b, int Cout,
+                     int k, int s, int p, int op, const float *bias, float scale, float *out, void *workspace,
+                     unsigned long long workspace_bytes, bool ffma, bool weights_ready, void *stream);
+
 // ---------------------------------------------------------------- device --
 
 __device__ __forceinline__ unsigned long long globaltimer_ns() {

@@ -15,11 +15,6 @@ fw_status fw_conv2d_tanh_scale_bias_maxpool(const float *x, int N, int Cin, int 
                                             const float *bias, int pool_k, int pool_s, float *out, void *stream);
 fw_status fw_maxpool2d(const float *x, int N, int C, int H, int W, int k, int s, int p, int d, float *out,
                        void *stream);
-fw_status fw_convtranspose2d_softmax_bias_scale_sigmoid(const float *x, int N, int Cin, int H, int W,
-                                                        const float *w, const float *conv_b, int Cout, int k, int s,
-                                                        int p, int op, const float *bias, float scale, float *out,
-                                                        void *workspace, unsigned long long workspace_bytes,
-                                                        void *stream);
 fw_status fw_conv2d_pool_out_shape(int H, int W, int KH, int KW, int pool_k, int pool_s, int *Ho, int *Wo);
 fw_status fw_maxpool2d_out_shape(int H, int W, int k, int s, int p, int d, int *Ho, int *Wo);
 fw_status fw_convt_out_shape(int H, int W, int k, int s, int p, int op, int *Ho, int *Wo);
@@ -65,13 +60,10 @@ Pipe *pipe_for_current_device() {
 // One pipelined call: `small` copies (weights) first, then per chunk of images the
 // input copy, the operator (`run`, on the caller's stream) and the output copy.
 template <class Run>
-fw_status pipelined(cudaStream_t st, int N, size_t in_img_bytes, const void *x_host, void *x_dev,
-                    size_t out_img_bytes, void *out_host, const void *out_dev,
-                    const void *const *small_src, void *const *small_dst, const size_t *small_bytes, int nsmall,
-                    Run run) {
-    std::lock_guard<std::mutex> lock(g_pipe_mu);
-    Pipe *p = pipe_for_current_device();
-    if (!p) return FW_ERR_LAUNCH;
+fw_status pipelined_enqueue(Pipe *p, cudaStream_t st, int N, size_t in_img_bytes, const void *x_host, void *x_dev,
+                            size_t out_img_bytes, void *out_host, const void *out_dev,
+                            const void *const *small_src, void *const *small_dst, const size_t *small_bytes,
+                            int nsmall, Run run) {
     const int nch = N < MAX_CHUNKS ? N : MAX_CHUNKS;
     const int per = (N + nch - 1) / nch;
     auto ck = [](cudaError_t e) { return e == cudaSuccess; };
@@ -100,6 +92,25 @@ fw_status pipelined(cudaStream_t st, int N, size_t in_img_bytes, const void *x_h
     // the caller's stream continues after the last output copy
     if (!ck(cudaEventRecord(p->done, p->d2h)) || !ck(cudaStreamWaitEvent(st, p->done, 0))) return FW_ERR_LAUNCH;
     return FW_OK;
+}
+
+template <class Run>
+fw_status pipelined(cudaStream_t st, int N, size_t in_img_bytes, const void *x_host, void *x_dev,
+                    size_t out_img_bytes, void *out_host, const void *out_dev,
+                    const void *const *small_src, void *const *small_dst, const size_t *small_bytes, int nsmall,
+                    Run run) {
+    std::lock_guard<std::mutex> lock(g_pipe_mu);
+    Pipe *p = pipe_for_current_device();
+    if (!p) return FW_ERR_LAUNCH;
+    const fw_status rc = pipelined_enqueue(p, st, N, in_img_bytes, x_host, x_dev, out_img_bytes, out_host, out_dev,
+                                           small_src, small_dst, small_bytes, nsmall, run);
+    if (rc != FW_OK) {
+        // A failed call returns only once no copy it enqueued is still in flight, so
+        // the caller may free or reuse the workspace and the host buffers at once.
+        cudaStreamSynchronize(p->h2d);
+        cudaStreamSynchronize(p->d2h);
+    }
+    return rc;
 }
 
 bool valid_sizes(int N, int a, int b) { return N >= 1 && a >= 1 && b >= 1; }
@@ -215,10 +226,12 @@ fw_status fw_convtranspose2d_softmax_bias_scale_sigmoid_host(const float *x, int
     const size_t bytes[] = {wb, conv_b ? cbb : 0, cbb};
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     const size_t in_img = 4ull * Cin * H * W, out_img = 4ull * Cout * Ho * Wo;
+    // the weight rewrite into `tws` is made by the first chunk only: the chunks run in
+    // order on `stream`, so the later ones find it in place
     return pipelined(st, N, in_img, x, xd, out_img, out, od, src, dst, bytes, 3, [&](int i0, int n) {
-        return fw_convtranspose2d_softmax_bias_scale_sigmoid(
-            xd + (size_t)i0 * Cin * H * W, n, Cin, H, W, wd, conv_b ? cbd : nullptr, Cout, k, s, p, op, bd, scale,
-            od + (size_t)i0 * Cout * Ho * Wo, tws_bytes ? tws : nullptr, tws_bytes, stream);
+        return convt_call(xd + (size_t)i0 * Cin * H * W, n, Cin, H, W, wd, conv_b ? cbd : nullptr, Cout, k, s, p,
+                          op, bd, scale, od + (size_t)i0 * Cout * Ho * Wo, tws_bytes ? tws : nullptr, tws_bytes,
+                          false, i0 > 0, stream);
     });
 }
 

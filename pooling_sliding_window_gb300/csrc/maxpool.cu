@@ -38,12 +38,16 @@ __device__ __forceinline__ float max_nan(float a, float b) {
 }
 
 // The definition's window maximum for one output (taps in row-major order,
-// -inf padding, first of equal values kept), read from global memory.
+// -inf padding, first of equal values kept), read from global memory.  Inlined
+// and unrolled: as a called function it made the kernels keep registers in local
+// memory (spills), although the branch that needs it is rarely taken.
 template <int K, int P>
-__device__ __noinline__ float window_max_exact(const float *__restrict__ plane, int H, int W, int oh, int ow) {
+__device__ __forceinline__ float window_max_exact(const float *__restrict__ plane, int H, int W, int oh, int ow) {
     float m = -INFINITY;
+#pragma unroll
     for (int i = 0; i < K; ++i) {
         const int ih = oh - P + i;
+#pragma unroll
         for (int j = 0; j < K; ++j) {
             const int iw = ow - P + j;
             const float v = (ih >= 0 && ih < H && iw >= 0 && iw < W) ? __ldg(plane + (long long)ih * W + iw) : -INFINITY;
@@ -189,11 +193,10 @@ __global__ void __launch_bounds__(512) maxpool_s1_stream_kernel(const float *__r
                 // definition keeps the first zero of the window, so a zero result
                 // is recomputed tap by tap (rare).
                 if (m.x == 0.f || m.y == 0.f || m.z == 0.f || m.w == 0.f) {
-                    float r[4] = {m.x, m.y, m.z, m.w};
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        if (r[j] == 0.f) r[j] = window_max_exact<K, P>(xplane, H, W, oh, 4 * tid + j);
-                    m = make_float4(r[0], r[1], r[2], r[3]);
+                    if (m.x == 0.f) m.x = window_max_exact<K, P>(xplane, H, W, oh, 4 * tid);
+                    if (m.y == 0.f) m.y = window_max_exact<K, P>(xplane, H, W, oh, 4 * tid + 1);
+                    if (m.z == 0.f) m.z = window_max_exact<K, P>(xplane, H, W, oh, 4 * tid + 2);
+                    if (m.w == 0.f) m.w = window_max_exact<K, P>(xplane, H, W, oh, 4 * tid + 3);
                 }
                 float *os = ostage + warp * 128;
                 __syncwarp();
@@ -278,9 +281,10 @@ __global__ void __launch_bounds__(256) maxpool_direct_ex_kernel(const float *__r
     }
 }
 
-// The definition's window maximum for one output with any stride and dilation.
-__device__ __noinline__ float window_max_exact_sd(const float *__restrict__ plane, int H, int W, int k, int s, int p,
-                                                  int d, int oh, int ow) {
+// The definition's window maximum for one output with any stride and dilation
+// (inlined, like window_max_exact).
+__device__ __forceinline__ float window_max_exact_sd(const float *__restrict__ plane, int H, int W, int k, int s,
+                                                     int p, int d, int oh, int ow) {
     float m = -INFINITY;
     for (int i = 0; i < k; ++i) {
         const int ih = oh * s - p + i * d;
@@ -415,11 +419,10 @@ __global__ void __launch_bounds__(512) maxpool_stream_sd_kernel(const float *__r
                     }
                     // a zero maximum: the sign is the first zero's by the definition
                     if (m.x == 0.f || m.y == 0.f || m.z == 0.f || m.w == 0.f) {
-                        float r[4] = {m.x, m.y, m.z, m.w};
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            if (r[j] == 0.f) r[j] = window_max_exact_sd(src, H, W, K, S, P, D, oh, 4 * tid + j);
-                        m = make_float4(r[0], r[1], r[2], r[3]);
+                        if (m.x == 0.f) m.x = window_max_exact_sd(src, H, W, K, S, P, D, oh, 4 * tid);
+                        if (m.y == 0.f) m.y = window_max_exact_sd(src, H, W, K, S, P, D, oh, 4 * tid + 1);
+                        if (m.z == 0.f) m.z = window_max_exact_sd(src, H, W, K, S, P, D, oh, 4 * tid + 2);
+                        if (m.w == 0.f) m.w = window_max_exact_sd(src, H, W, K, S, P, D, oh, 4 * tid + 3);
                     }
                     float *os = ostage + warp * 128;
                     __syncwarp();

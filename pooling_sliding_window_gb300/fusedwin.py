@@ -38,7 +38,7 @@ EXPORTS = ("fw_status_string", "fw_version", "fw_conv2d_pool_out_shape", "fw_max
            "fw_convtranspose2d_softmax_bias_scale_sigmoid_host",
            "fw_convtranspose2d_softmax_bias_scale_sigmoid_host_workspace_size",
            "fw_convtranspose2d_softmax_bias_scale_sigmoid_nhwc", "fw_conv2d_tanh_scale_bias_maxpool_tf32",
-           "fw_conv2d_tanh_scale_bias_maxpool_ffma")
+           "fw_conv2d_tanh_scale_bias_maxpool_ffma", "fw_convtranspose2d_softmax_bias_scale_sigmoid_ffma")
 
 
 class FusedWinError(RuntimeError):
@@ -75,9 +75,10 @@ def lib():
             getattr(L, name).argtypes = [P, I, I, I, I, P, P, I, I, I, F, P, I, I, P, P]
         L.fw_maxpool2d.restype = I
         L.fw_maxpool2d.argtypes = [P, I, I, I, I, I, I, I, I, P, P]
-        L.fw_convtranspose2d_softmax_bias_scale_sigmoid.restype = I
-        L.fw_convtranspose2d_softmax_bias_scale_sigmoid.argtypes = [
-            P, I, I, I, I, P, P, I, I, I, I, I, P, F, P, P, U64, P]
+        for name in ("fw_convtranspose2d_softmax_bias_scale_sigmoid",
+                     "fw_convtranspose2d_softmax_bias_scale_sigmoid_ffma"):
+            getattr(L, name).restype = I
+            getattr(L, name).argtypes = [P, I, I, I, I, P, P, I, I, I, I, I, P, F, P, P, U64, P]
         L.fw_convt_workspace_size.restype = U64
         L.fw_convt_workspace_size.argtypes = [I, I, I, I, I]
         L.fw_check_device_errors.restype = I
@@ -181,6 +182,63 @@ def _ptr(t):
     return C.c_void_p(0 if t is None else t.data_ptr())
 
 
+# Shape checks made before any C call: a kernel trusts the sizes it is given, so an
+# `out` or a bias smaller than the arguments imply would be written or read past its
+# end on the GPU.
+
+def _check_out(out, shape, device_type=None, name="out"):
+    """`out` (if given) must be a contiguous float32 tensor of exactly `shape`."""
+    if out is None:
+        return
+    if not isinstance(out, torch.Tensor) or out.dtype != torch.float32 or not out.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous float32 tensor")
+    if tuple(out.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(out.shape)}, the call needs {tuple(shape)}")
+    if device_type is not None and out.device.type != device_type:
+        raise ValueError(f"{name} must be a {device_type} tensor")
+
+
+def _check_dims(name, t, ndim):
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions, got shape {tuple(t.shape)}")
+
+
+def _check_vec(name, t, n):
+    if t is not None and t.numel() != n:
+        raise ValueError(f"{name} must hold {n} values (one per output channel), got {t.numel()}")
+
+
+def _conv_pool_dims(x, w, conv_b, bias):
+    """(N, Cin, H, W, Cout, KH, KW) of a conv+pool call, checked for consistency."""
+    _check_dims("x", x, 4)
+    _check_dims("w", w, 4)
+    N, Cin, H, W = x.shape
+    Cout, Cw, KH, KW = w.shape
+    if Cw != Cin:
+        raise ValueError(f"w has {Cw} input channels, x has {Cin}")
+    _check_vec("conv_b", conv_b, Cout)
+    _check_vec("bias", bias, Cout)
+    return N, Cin, H, W, Cout, KH, KW
+
+
+def _convt_dims(x, w, conv_b, bias, channels_last=False):
+    """(N, Cin, H, W, Cout, K) of a conv-transpose call, checked for consistency."""
+    _check_dims("x", x, 4)
+    _check_dims("w", w, 4)
+    if channels_last:
+        N, H, W, Cin = x.shape
+    else:
+        N, Cin, H, W = x.shape
+    Cw, Cout, K, K2 = w.shape
+    if Cw != Cin:
+        raise ValueError(f"w has {Cw} input channels, x has {Cin}")
+    if K != K2:
+        raise ValueError(f"w must have a square kernel, got {K}x{K2}")
+    _check_vec("conv_b", conv_b, Cout)
+    _check_vec("bias", bias, Cout)
+    return N, Cin, H, W, Cout, K
+
+
 def _device_of(x):
     if x.device.type == "cuda":
         return x.device
@@ -218,12 +276,12 @@ def fw_conv2d_tanh_scale_bias_maxpool_ffma(x, w, conv_b, bias, scale, pool_k, po
 
 def _conv_pool(fname, x, w, conv_b, bias, scale, pool_k, pool_s, out):
     host = x.device.type != "cuda"
+    N, Cin, H, W, Cout, KH, KW = _conv_pool_dims(x, w, conv_b, bias.reshape(-1))
+    Ho, Wo = fw_conv2d_pool_out_shape(H, W, KH, KW, pool_k, pool_s)
+    _check_out(out, (N, Cout, Ho, Wo), "cpu" if host else "cuda")
     dev = _device_of(x)
     xd, wd = _dev(x, "x", dev), _dev(w, "w", dev)
     cbd, bd = _dev(conv_b, "conv_b", dev), _dev(bias.reshape(-1), "bias", dev)
-    N, Cin, H, W = xd.shape
-    Cout, _, KH, KW = wd.shape
-    Ho, Wo = fw_conv2d_pool_out_shape(H, W, KH, KW, pool_k, pool_s)
     od = out if (out is not None and not host) else torch.empty((N, Cout, Ho, Wo), device=dev,
                                                                  dtype=torch.float32)
     stream = torch.cuda.current_stream(dev).cuda_stream
@@ -238,10 +296,12 @@ def fw_maxpool2d(x, k, s=None, p=0, d=1, out=None):
     """MaxPool2d(kernel k, stride s (default k), padding p (-inf), dilation d)."""
     s = k if s is None else s
     host = x.device.type != "cuda"
+    _check_dims("x", x, 4)
+    N, Cc, H, W = x.shape
+    Ho, Wo = fw_maxpool2d_out_shape(H, W, k, s, p, d)
+    _check_out(out, (N, Cc, Ho, Wo), "cpu" if host else "cuda")
     dev = _device_of(x)
     xd = _dev(x, "x", dev)
-    N, Cc, H, W = xd.shape
-    Ho, Wo = fw_maxpool2d_out_shape(H, W, k, s, p, d)
     od = out if (out is not None and not host) else torch.empty((N, Cc, Ho, Wo), device=dev,
                                                                  dtype=torch.float32)
     stream = torch.cuda.current_stream(dev).cuda_stream
@@ -254,13 +314,25 @@ def fw_maxpool2d(x, k, s=None, p=0, d=1, out=None):
 def fw_convtranspose2d_softmax_bias_scale_sigmoid(x, w, conv_b, bias, scale, stride=2, padding=1,
                                                   output_padding=1, out=None, workspace=None):
     """out = sigmoid((softmax(conv_transpose2d(x, w, conv_b), dim=1) + bias) * scale)."""
+    return _convt("fw_convtranspose2d_softmax_bias_scale_sigmoid", x, w, conv_b, bias, scale, stride, padding,
+                  output_padding, out, workspace)
+
+
+def fw_convtranspose2d_softmax_bias_scale_sigmoid_ffma(x, w, conv_b, bias, scale, stride=2, padding=1,
+                                                       output_padding=1, out=None, workspace=None):
+    """The same operator on the float32 FMA pipe only (float32 products and sums)."""
+    return _convt("fw_convtranspose2d_softmax_bias_scale_sigmoid_ffma", x, w, conv_b, bias, scale, stride, padding,
+                  output_padding, out, workspace)
+
+
+def _convt(fname, x, w, conv_b, bias, scale, stride, padding, output_padding, out, workspace):
     host = x.device.type != "cuda"
+    N, Cin, H, W, Cout, K = _convt_dims(x, w, conv_b, bias.reshape(-1))
+    Ho, Wo = fw_convt_out_shape(H, W, K, stride, padding, output_padding)
+    _check_out(out, (N, Cout, Ho, Wo), "cpu" if host else "cuda")
     dev = _device_of(x)
     xd, wd = _dev(x, "x", dev), _dev(w, "w", dev)
     cbd, bd = _dev(conv_b, "conv_b", dev), _dev(bias.reshape(-1), "bias", dev)
-    N, Cin, H, W = xd.shape
-    _, Cout, K, _ = wd.shape
-    Ho, Wo = fw_convt_out_shape(H, W, K, stride, padding, output_padding)
     need = fw_convt_workspace_size(Cin, Cout, K, stride, padding)
     if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
         workspace = torch.empty((need + 3) // 4, device=dev, dtype=torch.float32)
@@ -269,10 +341,9 @@ def fw_convtranspose2d_softmax_bias_scale_sigmoid(x, w, conv_b, bias, scale, str
     stream = torch.cuda.current_stream(dev).cuda_stream
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     with torch.cuda.device(dev):
-        _check(lib().fw_convtranspose2d_softmax_bias_scale_sigmoid(
+        _check(getattr(lib(), fname)(
             _ptr(xd), N, Cin, H, W, _ptr(wd), _ptr(cbd), Cout, K, stride, padding, output_padding,
-            _ptr(bd), float(scale), _ptr(od), _ptr(workspace), ws_bytes, C.c_void_p(stream)),
-            "fw_convtranspose2d_softmax_bias_scale_sigmoid")
+            _ptr(bd), float(scale), _ptr(od), _ptr(workspace), ws_bytes, C.c_void_p(stream)), fname)
     return _finish(od, out, host)
 
 
@@ -290,8 +361,8 @@ def fw_convtranspose2d_softmax_bias_scale_sigmoid_noalloc(x, w, conv_b, bias, sc
         if not isinstance(t, torch.Tensor) or t.device.type != "cuda" or t.dtype != torch.float32 \
                 or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous float32 CUDA tensor")
-    N, Cin, H, W = x.shape
-    _, Cout, K, _ = w.shape
+    N, Cin, H, W, Cout, K = _convt_dims(x, w, conv_b, bias.reshape(-1))
+    _check_out(out, (N, Cout) + fw_convt_out_shape(H, W, K, stride, padding, output_padding), "cuda")
     stream = torch.cuda.current_stream(x.device).cuda_stream
     with torch.cuda.device(x.device):
         _check(lib().fw_convtranspose2d_softmax_bias_scale_sigmoid_noalloc(
@@ -324,9 +395,9 @@ def fw_conv2d_tanh_scale_bias_maxpool_unfused(x, w, conv_b, bias, scale, pool_k,
     dev = _device_of(x)
     xd, wd = _dev(x, "x", dev), _dev(w, "w", dev)
     cbd, bd = _dev(conv_b, "conv_b", dev), _dev(bias.reshape(-1), "bias", dev)
-    N, Cin, H, W = xd.shape
-    Cout, _, KH, KW = wd.shape
+    N, Cin, H, W, Cout, KH, KW = _conv_pool_dims(xd, wd, cbd, bd)
     Ho, Wo = fw_conv2d_pool_out_shape(H, W, KH, KW, pool_k, pool_s)
+    _check_out(out, (N, Cout, Ho, Wo), "cuda")
     workspace, ws_bytes = _workspace(fw_conv2d_pool_unfused_workspace_size(N, H, W, Cout, KH, KW, pool_k, pool_s),
                                      workspace, dev)
     od = out if out is not None else torch.empty((N, Cout, Ho, Wo), device=dev, dtype=torch.float32)
@@ -346,9 +417,9 @@ def fw_convtranspose2d_softmax_bias_scale_sigmoid_unfused(x, w, conv_b, bias, sc
     dev = _device_of(x)
     xd, wd = _dev(x, "x", dev), _dev(w, "w", dev)
     cbd, bd = _dev(conv_b, "conv_b", dev), _dev(bias.reshape(-1), "bias", dev)
-    N, Cin, H, W = xd.shape
-    _, Cout, K, _ = wd.shape
+    N, Cin, H, W, Cout, K = _convt_dims(xd, wd, cbd, bd)
     Ho, Wo = fw_convt_out_shape(H, W, K, stride, padding, output_padding)
+    _check_out(out, (N, Cout, Ho, Wo), "cuda")
     workspace, ws_bytes = _workspace(
         fw_convt_unfused_workspace_size(N, Cin, H, W, Cout, K, stride, padding, output_padding), workspace, dev)
     od = out if out is not None else torch.empty((N, Cout, Ho, Wo), device=dev, dtype=torch.float32)
@@ -373,8 +444,10 @@ def fw_maxpool2d_ex(x, k, s=None, p=0, d=1, ceil_mode=False, return_indices=Fals
     s = k if s is None else s
     dev = _device_of(x)
     xd = _dev(x, "x", dev)
+    _check_dims("x", xd, 4)
     N, Cc, H, W = xd.shape
     Ho, Wo = fw_maxpool2d_out_shape_ex(H, W, k, s, p, d, ceil_mode)
+    _check_out(out, (N, Cc, Ho, Wo), "cuda")
     od = out if out is not None else torch.empty((N, Cc, Ho, Wo), device=dev, dtype=torch.float32)
     idx = torch.empty((N, Cc, Ho, Wo), device=dev, dtype=torch.int64) if return_indices else None
     stream = torch.cuda.current_stream(dev).cuda_stream
@@ -410,9 +483,9 @@ def _dev_workspace(need, workspace):
 def fw_conv2d_tanh_scale_bias_maxpool_host(x, w, conv_b, bias, scale, pool_k, pool_s=0, out=None, workspace=None,
                                            stream=None):
     x, w, conv_b, bias = _host(x, "x"), _host(w, "w"), _host(conv_b, "conv_b"), _host(bias.reshape(-1), "bias")
-    N, Cin, H, W = x.shape
-    Cout, _, KH, KW = w.shape
+    N, Cin, H, W, Cout, KH, KW = _conv_pool_dims(x, w, conv_b, bias)
     Ho, Wo = fw_conv2d_pool_out_shape(H, W, KH, KW, pool_k, pool_s)
+    _check_out(out, (N, Cout, Ho, Wo), "cpu")
     out = torch.empty((N, Cout, Ho, Wo), pin_memory=True) if out is None else _host(out, "out")
     workspace, wsb = _dev_workspace(int(lib().fw_conv2d_tanh_scale_bias_maxpool_host_workspace_size(
         N, Cin, H, W, Cout, KH, KW, pool_k, pool_s)), workspace)
@@ -428,8 +501,10 @@ def fw_conv2d_tanh_scale_bias_maxpool_host(x, w, conv_b, bias, scale, pool_k, po
 def fw_maxpool2d_host(x, k, s=None, p=0, d=1, out=None, workspace=None, stream=None):
     s = k if s is None else s
     x = _host(x, "x")
+    _check_dims("x", x, 4)
     N, Cc, H, W = x.shape
     Ho, Wo = fw_maxpool2d_out_shape(H, W, k, s, p, d)
+    _check_out(out, (N, Cc, Ho, Wo), "cpu")
     out = torch.empty((N, Cc, Ho, Wo), pin_memory=True) if out is None else _host(out, "out")
     workspace, wsb = _dev_workspace(int(lib().fw_maxpool2d_host_workspace_size(N, Cc, H, W, k, s, p, d)), workspace)
     st = torch.cuda.current_stream(workspace.device) if stream is None else stream
@@ -443,9 +518,9 @@ def fw_maxpool2d_host(x, k, s=None, p=0, d=1, out=None, workspace=None, stream=N
 def fw_convtranspose2d_softmax_bias_scale_sigmoid_host(x, w, conv_b, bias, scale, stride=2, padding=1,
                                                        output_padding=1, out=None, workspace=None, stream=None):
     x, w, conv_b, bias = _host(x, "x"), _host(w, "w"), _host(conv_b, "conv_b"), _host(bias.reshape(-1), "bias")
-    N, Cin, H, W = x.shape
-    _, Cout, K, _ = w.shape
+    N, Cin, H, W, Cout, K = _convt_dims(x, w, conv_b, bias)
     Ho, Wo = fw_convt_out_shape(H, W, K, stride, padding, output_padding)
+    _check_out(out, (N, Cout, Ho, Wo), "cpu")
     out = torch.empty((N, Cout, Ho, Wo), pin_memory=True) if out is None else _host(out, "out")
     workspace, wsb = _dev_workspace(int(lib().fw_convtranspose2d_softmax_bias_scale_sigmoid_host_workspace_size(
         N, Cin, H, W, Cout, K, stride, padding, output_padding)), workspace)
@@ -468,9 +543,9 @@ def fw_convtranspose2d_softmax_bias_scale_sigmoid_nhwc(x, w, conv_b, bias, scale
     dev = _device_of(x)
     xd, wd = _dev(x, "x", dev), _dev(w, "w", dev)
     cbd, bd = _dev(conv_b, "conv_b", dev), _dev(bias.reshape(-1), "bias", dev)
-    N, H, W, Cin = xd.shape
-    _, Cout, K, _ = wd.shape
+    N, Cin, H, W, Cout, K = _convt_dims(xd, wd, cbd, bd, channels_last=True)
     Ho, Wo = fw_convt_out_shape(H, W, K, stride, padding, output_padding)
+    _check_out(out, (N, Ho, Wo, Cout), "cuda")
     need = fw_convt_workspace_size(Cin, Cout, K, stride, padding)
     if workspace is None or workspace.numel() * workspace.element_size() < need:
         workspace = torch.empty(max(1, (need + 3) // 4), device=dev, dtype=torch.float32)

@@ -60,6 +60,35 @@ def tf32_round(a):
     return ((u + np.uint32(0x1000)) & np.uint32(0xFFFFE000)).view(np.float32)
 
 
+# Canary guards: an output allocated inside a larger buffer whose head and tail hold a
+# NaN bit pattern no kernel produces; after the call both must be untouched, so a
+# kernel that writes past either end of its output fails the test that ran it.
+GUARD = 4096                 # 32-bit words on each side (16 KB: keeps 256-byte alignment)
+SENTINEL = 0x7FBADBAD        # a quiet-NaN payload
+
+
+class Guarded:
+    def __init__(self, shape, dtype=torch.float32):
+        n = int(np.prod(shape))
+        words = n * (2 if dtype == torch.int64 else 1)
+        self.buf = torch.full((words + 2 * GUARD,), SENTINEL, dtype=torch.int32, device="cuda")
+        self.out = self.buf[GUARD:GUARD + words].view(dtype).view(shape)
+
+    def check(self, what=""):
+        torch.cuda.synchronize()
+        head, tail = self.buf[:GUARD], self.buf[-GUARD:]
+        bad = int((head != SENTINEL).sum()) + int((tail != SENTINEL).sum())
+        assert bad == 0, f"{what}: {bad} guard words around the output were overwritten"
+
+
+def guarded_call(fn, shape, *args, **kw):
+    """Run fn(*args, out=<guarded tensor of `shape`>, **kw); check the guards; return the output on the host."""
+    g = Guarded(shape)
+    fn(*args, out=g.out, **kw)
+    g.check(getattr(fn, "__name__", "call"))
+    return host(g.out)
+
+
 def pmap(fn, items):
     return list(POOL.map(fn, items))
 
@@ -70,4 +99,4 @@ def sample_indices(shape, count, seed):
 
 
 __all__ = ["O", "FW", "synth", "TOL_FFMA", "TOL_TF32", "tf32_round", "dev", "host", "assert_bits_equal", "assert_close", "pmap",
-           "sample_indices", "bits_equal"]
+           "sample_indices", "bits_equal", "Guarded", "guarded_call"]

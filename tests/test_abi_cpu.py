@@ -121,6 +121,20 @@ def test_operator_argument_errors_without_launch():
     assert ct(op=2) == 3
     assert ct(Cout=2048) == 6
     assert ct(out=P(0x80000000 + 4096)) == 4  # out overlaps workspace
+    # the weight rewrite would overwrite bias / conv_b before the main kernel reads them
+    ctb = lambda cb, bias: L.fw_convtranspose2d_softmax_bias_scale_sigmoid(
+        x, 1, 64, 8, 8, w, cb, 128, 4, 2, 1, 1, bias, 2.0, o, ws, need, None)
+    assert ctb(None, P(0x80000000 + 256)) == 4
+    assert ctb(P(0x80000000 + need - 4), b) == 4
+    assert ctb(P(0x80000000 + need), b) != 4  # just past the workspace: no overlap
+    # the FP32-FMA conv-transpose entry takes the same arguments and checks
+    ff = lambda **kw: L.fw_convtranspose2d_softmax_bias_scale_sigmoid_ffma(
+        kw.get("x", x), 1, 64, 8, 8, w, None, 128, 4, 2, 1, kw.get("op", 1), b, kw.get("scale", 2.0),
+        kw.get("out", o), kw.get("ws", ws), need, None)
+    assert ff(ws=None) == 1
+    assert ff(op=2) == 3
+    assert ff(scale=float("nan")) == 3
+    assert ff(out=P(0x80000000 + 64)) == 4
     # unfused comparison path: workspace, alignment, support and aliasing checks
     cpn = FW.fw_conv2d_pool_unfused_workspace_size(2, 64, 64, 64, 3, 3, 4)
     assert cpn == 4 * 2 * 64 * 60 * 60
@@ -169,3 +183,41 @@ def test_product_path_fails_loudly_without_gpu():
     x = torch.zeros(1, 1, 8, 8)
     with pytest.raises(RuntimeError, match="CUDA"):
         FW.fw_maxpool2d(x, 2)
+
+
+def test_binding_rejects_wrong_sizes_before_any_call():
+    """The binding checks `out` and the per-channel vectors against the shapes the
+    call implies (a kernel would otherwise write or read past their ends).  Host
+    tensors exercise the checks without a GPU: they run before anything is moved."""
+    x = torch.zeros(2, 8, 16, 16)
+    w = torch.zeros(4, 8, 3, 3)
+    b = torch.zeros(4)
+    n0 = FW.fw_launch_count()
+    with pytest.raises(ValueError, match="shape"):
+        FW.fw_conv2d_tanh_scale_bias_maxpool(x, w, None, b, 2.0, 4, out=torch.zeros(2, 4, 3, 4))
+    with pytest.raises(ValueError, match="one per output channel"):
+        FW.fw_conv2d_tanh_scale_bias_maxpool(x, w, None, torch.zeros(3), 2.0, 4)
+    with pytest.raises(ValueError, match="one per output channel"):
+        FW.fw_conv2d_tanh_scale_bias_maxpool(x, w, torch.zeros(5), b, 2.0, 4)
+    with pytest.raises(ValueError, match="input channels"):
+        FW.fw_conv2d_tanh_scale_bias_maxpool(x, torch.zeros(4, 6, 3, 3), None, b, 2.0, 4)
+    with pytest.raises(ValueError, match="shape"):
+        FW.fw_maxpool2d(x, 2, 2, 0, 1, out=torch.zeros(2, 8, 8, 7))
+    with pytest.raises(ValueError, match="shape"):
+        FW.fw_maxpool2d_host(x, 2, 2, 0, 1, out=torch.zeros(2, 8, 8, 9))
+    xt = torch.zeros(1, 64, 8, 8)
+    wt = torch.zeros(64, 128, 4, 4)
+    bt = torch.zeros(128)
+    with pytest.raises(ValueError, match="shape"):
+        FW.fw_convtranspose2d_softmax_bias_scale_sigmoid(xt, wt, None, bt, 2.0, out=torch.zeros(1, 128, 16, 17))
+    with pytest.raises(ValueError, match="shape"):
+        FW.fw_convtranspose2d_softmax_bias_scale_sigmoid_ffma(xt, wt, None, bt, 2.0, out=torch.zeros(1, 127, 17, 17))
+    with pytest.raises(ValueError, match="one per output channel"):
+        FW.fw_convtranspose2d_softmax_bias_scale_sigmoid(xt, wt, torch.zeros(64), bt, 2.0)
+    with pytest.raises(ValueError, match="square"):
+        FW.fw_convtranspose2d_softmax_bias_scale_sigmoid(xt, torch.zeros(64, 128, 4, 3), None, bt, 2.0)
+    with pytest.raises(ValueError, match="input channels"):
+        FW.fw_convtranspose2d_softmax_bias_scale_sigmoid_host(xt, torch.zeros(32, 128, 4, 4), None, bt, 2.0)
+    with pytest.raises(ValueError, match="shape"):
+        FW.fw_conv2d_tanh_scale_bias_maxpool_host(x, w, None, b, 2.0, 4, out=torch.zeros(2, 4, 4, 4, 1))
+    assert FW.fw_launch_count() == n0

@@ -22,6 +22,17 @@ def test_work_counts():
     assert abs(bench.CT_FLOPS / 1e9 - 136.37) < 0.01
 
 
+def test_sweep_covers_the_sweep_config():
+    """The timed sweep is the conv+pool edge/size sweep's 36 shapes (each run there
+    with seeds 0-2: 108 runs)."""
+    assert len(bench.SWEEP) == 36 and len(set(bench.SWEEP)) == 36
+    assert {s[0] for s in bench.SWEEP} == {1, 16, 128}
+    assert {s[1] for s in bench.SWEEP} == {127, 255, 256}
+    assert {s[2] for s in bench.SWEEP} == {16, 64}
+    assert {s[3] for s in bench.SWEEP} == {2, 4}
+    assert bench.cp_flops(N=2, ho=15) == 2 * 72 * 2 * 64 * 60 * 60  # the tiny config
+
+
 def _free_port():
     s = socket.socket()
     s.bind(("127.0.0.1", 0))

@@ -5,15 +5,17 @@ import numpy as np
 import pytest
 import torch
 
-from tests.parity import FW, O, TOL_FFMA, assert_close, dev, host, pmap, sample_indices, synth
+from tests.parity import FW, O, TOL_FFMA, assert_close, dev, guarded_call, host, pmap, sample_indices, synth
 
 pytestmark = pytest.mark.gpu
 
 
 def run_gpu(d, scale, pk, ps=0, cb=True):
-    return host(FW.fw_conv2d_tanh_scale_bias_maxpool(dev(d["x"]), dev(d["w"]),
-                                                     dev(d["conv_b"]) if cb else None, dev(d["bias"]),
-                                                     scale, pk, ps))
+    """The fused call into an output with canary guards on both sides."""
+    N, Cout, KH = d["x"].shape[0], d["w"].shape[0], d["w"].shape[2]
+    Ho, Wo = FW.fw_conv2d_pool_out_shape(d["x"].shape[2], d["x"].shape[3], KH, d["w"].shape[3], pk, ps)
+    return guarded_call(FW.fw_conv2d_tanh_scale_bias_maxpool, (N, Cout, Ho, Wo), dev(d["x"]), dev(d["w"]),
+                        dev(d["conv_b"]) if cb else None, dev(d["bias"]), scale, pk, ps)
 
 
 def run_oracle(d, scale, pk, ps=0, cb=True):

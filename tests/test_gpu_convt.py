@@ -3,14 +3,18 @@ import numpy as np
 import pytest
 import torch
 
-from tests.parity import FW, O, TOL_FFMA, assert_close, dev, host, pmap, sample_indices, synth
+from tests.parity import FW, O, TOL_FFMA, assert_close, dev, guarded_call, host, pmap, sample_indices, synth
 
 pytestmark = pytest.mark.gpu
 
 
 def run_gpu(d, scale, s=2, p=1, op=1, cb=True):
-    return host(FW.fw_convtranspose2d_softmax_bias_scale_sigmoid(
-        dev(d["x"]), dev(d["w"]), dev(d["conv_b"]) if cb else None, dev(d["bias"]), scale, s, p, op))
+    """The fused call into an output with canary guards on both sides."""
+    N, _, H, W = d["x"].shape
+    Cout, K = d["w"].shape[1], d["w"].shape[2]
+    return guarded_call(FW.fw_convtranspose2d_softmax_bias_scale_sigmoid,
+                        (N, Cout) + FW.fw_convt_out_shape(H, W, K, s, p, op), dev(d["x"]), dev(d["w"]),
+                        dev(d["conv_b"]) if cb else None, dev(d["bias"]), scale, s, p, op)
 
 
 def run_oracle(d, scale, s=2, p=1, op=1, cb=True):

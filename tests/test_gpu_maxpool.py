@@ -3,7 +3,7 @@ import numpy as np
 import pytest
 import torch
 
-from tests.parity import FW, O, assert_bits_equal, dev, host, pmap, sample_indices, synth
+from tests.parity import FW, O, assert_bits_equal, dev, guarded_call, host, pmap, sample_indices, synth
 
 pytestmark = pytest.mark.gpu
 
@@ -31,7 +31,7 @@ CASES = [
 def test_maxpool_small_bit_exact(case):
     N, C, H, W, k, s, p, d = case
     x = synth.maxpool_inputs(N, C, H, W, seed=sum(case))["x"]
-    got = host(FW.fw_maxpool2d(dev(x), k, s, p, d))
+    got = guarded_call(FW.fw_maxpool2d, (N, C) + FW.fw_maxpool2d_out_shape(H, W, k, s, p, d), dev(x), k, s, p, d)
     want = O.maxpool2d(x, k, s, p, d)
     assert got.shape == want.shape
     assert_bits_equal(got, want, str(case))
@@ -46,8 +46,8 @@ SD = [(2, 2, 1, 0), (2, 2, 1, 1), (3, 2, 1, 0), (3, 2, 1, 1), (4, 2, 1, 1), (5, 
 def test_strided_dilated_stream_bit_exact(k, s, d, p):
     for N, C, H, W in ((1, 2, 301, 512), (2, 1, 37, 64), (1, 1, 23, 132)):
         x = synth.maxpool_inputs(N, C, H, W, seed=k + 10 * s + 100 * d + p + W)["x"]
-        assert_bits_equal(host(FW.fw_maxpool2d(dev(x), k, s, p, d)), O.maxpool2d(x, k, s, p, d),
-                          str((N, C, H, W, k, s, p, d)))
+        got = guarded_call(FW.fw_maxpool2d, (N, C) + FW.fw_maxpool2d_out_shape(H, W, k, s, p, d), dev(x), k, s, p, d)
+        assert_bits_equal(got, O.maxpool2d(x, k, s, p, d), str((N, C, H, W, k, s, p, d)))
     rng = np.random.default_rng(k + s + d + p)
     x = rng.choice(np.array([0.0, -0.0, 1.0, -1.0, np.inf, -np.inf, np.nan, 0.5], np.float32),
                    size=(1, 2, 29, 64), p=[.3, .3, .1, .1, .04, .04, .02, .1]).astype(np.float32)

@@ -13,6 +13,7 @@ import numpy as np
 import pytest
 import torch
 
+from oracle import oracle as O
 from pooling_sliding_window_gb300 import fusedwin as FW
 from pooling_sliding_window_gb300 import synth
 from tests.parity import TOL_FFMA
@@ -42,6 +43,12 @@ def test_noalloc_matches_workspace_entry_point_twice():
         torch.cuda.synchronize()
         err = float((out - ref).abs().max())
         assert np.isfinite(err) and err <= TOL_FFMA, f"call {call}: max abs diff {err}"
+        # and against the oracle itself, on the same inputs
+        want = O.convtranspose2d_softmax_bias_scale_sigmoid(d["x"], d["w"], d["conv_b"], d["bias"], 2.0)
+        got = out.cpu().numpy().astype(np.float64)
+        err_o = float(np.abs(got - want).max())
+        assert got.shape == want.shape and np.isfinite(err_o) and err_o <= TOL_FFMA, \
+            f"call {call}: max abs err vs oracle {err_o}"
     FW.fw_check_device_errors()
 
 
