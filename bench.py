@@ -303,6 +303,9 @@ def time_configs(FW, dev, stream, tf32_peak):
     flush = torch.empty(256 * 2 ** 20 // 4, device=dev)
 
     def per_call(fn, reps, flush_l2=False):
+        """Median device time of one call: the GPU is kept busy (a spin kernel) while
+        the call is enqueued, so the events bracket the kernels and not the host's
+        launch overhead."""
         for _ in range(3):
             fn()
         torch.cuda.synchronize()
@@ -310,6 +313,7 @@ def time_configs(FW, dev, stream, tf32_peak):
         for _ in range(reps):
             if flush_l2:
                 flush.fill_(1.0)
+            torch.cuda._sleep(200_000)  # ~0.1 ms of GPU time
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             fn()
@@ -342,7 +346,7 @@ def time_configs(FW, dev, stream, tf32_peak):
     t = {k: torch.from_numpy(v).to(dev) for k, v in a.items()}
     out = torch.empty(2, 64, 15, 15, device=dev)
     fn = lambda: FW.fw_conv2d_tanh_scale_bias_maxpool(t["x"], t["w"], t["conv_b"], t["bias"], 2.0, 4, out=out)
-    warm, flushed, b2b = per_call(fn, 200), per_call(fn, 50, True), back_to_back(fn, 500)
+    warm, flushed, b2b = per_call(fn, 100), per_call(fn, 50, True), back_to_back(fn, 500)
     t0 = time.perf_counter()
     O.conv2d_tanh_scale_bias_maxpool(a["x"], a["w"], a["conv_b"], 2.0, a["bias"], 4)
     o_s = time.perf_counter() - t0
@@ -353,8 +357,9 @@ def time_configs(FW, dev, stream, tf32_peak):
         "outputs_per_s_warm": n_out / (warm * 1e-3), "outputs_per_s_back_to_back": n_out / (b2b * 1e-3),
         "tflops_warm": cp_flops(N=2, ho=15) / (warm * 1e-3) / 1e12,
         "oracle_single_thread_s": o_s, "oracle_outputs_per_s": n_out / o_s,
-        "note": "us_warm / us_l2_flushed: median device time of one call between CUDA events; "
-                "us_back_to_back: 500 calls enqueued back to back, per call"}
+        "note": "us_warm / us_l2_flushed: median device time of one call (events around the call, enqueued "
+                "behind a GPU spin so that host launch overhead is excluded); us_back_to_back: 500 calls "
+                "through the Python binding enqueued back to back, per call (bound by the host's call rate)"}
     # E: the size sweep
     rows, xs = [], {}
     for N, H, Cout, pool in SWEEP:
@@ -494,8 +499,10 @@ def run_gpu(args):
         n = ct["x"].shape[0]
         out_ct = torch.empty(n, CT["Cout"], 129, 129, device=dev)
         h_ct = torch.empty(tuple(out_ct.shape), pin_memory=True)
-        wsz = FW.fw_convt_workspace_size(CT["Cin"], CT["Cout"], 4, 2, 1)
-        wsp = torch.empty(max(1, wsz // 4), device=dev)
+        wsz = FW.fw_convt_workspace_size_ex(n, CT["Cin"], CT["H"], CT["W"], CT["Cout"], 4, 2, 1, 1)
+        if args.convt_kernel == "gather":  # profiling the gathering kernel: the weight rewrite's bytes only
+            wsz = FW.fw_convt_workspace_size(CT["Cin"], CT["Cout"], 4, 2, 1)
+        wsp = torch.empty(max(1, wsz // 4), device=dev)  # room for the staged kernel
 
         if args.convt_layout == "nhwc":  # profiling the channels-last variant through the same step
             x_nhwc = d[("ct", "x")].permute(0, 2, 3, 1).contiguous()
@@ -519,7 +526,8 @@ def run_gpu(args):
                 CT["scale"], out=h_ct, workspace=hws_ct)
         specs.append(dict(name="convt", work=ct_flops(N=n), unit="TFLOP/s", scale=1e12, bound="tensor",
                           run=lambda: op_ct(d, out_ct), e2e=lambda: host_ct(), out=h_ct,
-                          kernel="convt_k4s2_tc_kernel<16> (tcgen05 kind::tf32) + weight prepack",
+                          kernel=("convt_k4s2_tc_kernel<16,0,0,1> (tcgen05 kind::tf32; slabs by bulk copies from "
+                                  "the staged x) + convt_stage_x_kernel + weight prepack"),
                           source="convt_tc.cu"))
 
     def barrier():
@@ -632,6 +640,15 @@ def run_gpu(args):
             u_ms = med_ms(lambda: FW.fw_convtranspose2d_softmax_bias_scale_sigmoid_unfused(
                 d[("ct", "x")], d[("ct", "w")], d[("ct", "conv_b")], d[("ct", "bias")], CT["scale"],
                 out=out_ct, workspace=wsp_ct))
+            # the gathering kernel (workspace of the weight rewrite only), beside the staged one
+            ws_small = torch.empty(FW.fw_convt_workspace_size(CT["Cin"], CT["Cout"], 4, 2, 1) // 4, device=dev)
+            g_ms = med_ms(lambda: FW.fw_convtranspose2d_softmax_bias_scale_sigmoid(
+                d[("ct", "x")], d[("ct", "w")], d[("ct", "conv_b")], d[("ct", "bias")], CT["scale"], out=out_ct,
+                workspace=ws_small))
+            fusion["convt_gather"] = {"ms": g_ms, "staged_ms": f_ms,
+                                      "kernel": "convt_k4s2_tc_kernel<16,0,0,0>: producer warps gather the slabs "
+                                                "from NCHW x (workspace of the weight rewrite only)"}
+            del ws_small
             fusion["convt"] = {"fused_ms": f_ms, "unfused_ms": u_ms, "unfused_over_fused": u_ms / f_ms,
                                "intermediate_bytes": 4 * n * CT["Cout"] * 129 * 129,
                                "unfused": "convt_k4s2_tc_kernel raw mode (conv-transpose + conv_b to memory) + "
@@ -732,9 +749,10 @@ def run_gpu(args):
             line["convpool_ffma_tflops"] = v["tflops"]  # the FP32-FMA call, timed beside the step
             line["convpool_ffma_fp32_frac"] = v["frac_of_fp32_peak"]
         line["fusion"] = fusion
-    if args.only or args.batch or args.convt_layout != "nchw" or args.convpool_precision != "x3":
+    if (args.only or args.batch or args.convt_layout != "nchw" or args.convpool_precision != "x3"
+            or args.convt_kernel != "staged"):
         line["config"]["subset"] = {"only": args.only, "batch": args.batch, "convt_layout": args.convt_layout,
-                                    "convpool_precision": args.convpool_precision}
+                                    "convpool_precision": args.convpool_precision, "convt_kernel": args.convt_kernel}
     print(json.dumps(line), flush=True)
     if ws > 1:
         dist.barrier()
@@ -756,6 +774,8 @@ def main(argv=None):
     ap.add_argument("--batch", type=int, default=0, help="smaller batch for every workload (profiling)")
     ap.add_argument("--convt-layout", default="nchw", choices=["nchw", "nhwc"],
                     help="layout of the conv-transpose in the timed step (nhwc: channels-last variant, profiling)")
+    ap.add_argument("--convt-kernel", default="staged", choices=["staged", "gather"],
+                    help="conv-transpose kernel in the timed step (gather: workspace without the staged x; profiling)")
     ap.add_argument("--convpool-precision", default="x3", choices=["x3", "tf32"],
                     help="conv+pool in the timed step: 3xTF32 split (x3) or plain TF32 (profiling)")
     ap.add_argument("--no-fusion-compare", action="store_true",

@@ -273,8 +273,8 @@ bool force_ffma() {
 
 bool convt_tc_eligible(int Cin, int Cout, int k, int s, int p);
 fw_status convt_tc_launch(const float *x, int N, int Cin, int H, int W, const float *w, const float *cb,
-                          const float *bias, float scale, float *out, int Ho, int Wo, void *ws, cudaStream_t st,
-                          bool prepack);
+                          const float *bias, float scale, float *out, int Ho, int Wo, void *ws, size_t ws_bytes,
+                          cudaStream_t st, bool prepack);
 
 size_t convt_workspace_bytes(int Cin, int Cout, int k, int s, int p) {
     if (k == 4 && s == 2 && p == 1 && Cout == COUT_T) return (size_t)16 * Cin * Cout * sizeof(float);
@@ -291,7 +291,7 @@ fw_status convt_launch(const float *x, int N, int Cin, int H, int W, const float
     if (need > 0) {
         if (!ws || ws_bytes < need) return FW_ERR_NULL;
         if (!ffma && convt_tc_eligible(Cin, Cout, k, s, p) && !force_ffma())
-            return convt_tc_launch(x, N, Cin, H, W, w, cb, bias, scale, out, Ho, Wo, ws, st, !weights_ready);
+            return convt_tc_launch(x, N, Cin, H, W, w, cb, bias, scale, out, Ho, Wo, ws, ws_bytes, st, !weights_ready);
         float *wp = static_cast<float *>(ws);
         if (!weights_ready) {
             convt_prepack_kernel<<<(unsigned)min(1024LL, (16LL * Cin * Cout + 255) / 256), 256, 0, st>>>(w, wp, Cin,
@@ -377,7 +377,8 @@ extern "C" fw_status fw_convtranspose2d_softmax_bias_scale_sigmoid_noalloc(
         const fw_status rc = fw::convt_static_workspace(&ws);
         if (rc != FW_OK) return rc;
     }
+    // exactly the weight rewrite's bytes: the call keeps to the kernels that need no
+    // more workspace than that (never the staged copy of x)
     return fw_convtranspose2d_softmax_bias_scale_sigmoid(x, N, Cin, H, W, w, conv_b, Cout, k, s, p, op, bias,
-                                                         scale, out, ws, need > 0 ? FW_CONVT_STATIC_WS_BYTES : 0,
-                                                         stream);
+                                                         scale, out, ws, need, stream);
 }
