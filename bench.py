@@ -499,10 +499,8 @@ def run_gpu(args):
         n = ct["x"].shape[0]
         out_ct = torch.empty(n, CT["Cout"], 129, 129, device=dev)
         h_ct = torch.empty(tuple(out_ct.shape), pin_memory=True)
-        wsz = FW.fw_convt_workspace_size_ex(n, CT["Cin"], CT["H"], CT["W"], CT["Cout"], 4, 2, 1, 1)
-        if args.convt_kernel == "gather":  # profiling the gathering kernel: the weight rewrite's bytes only
-            wsz = FW.fw_convt_workspace_size(CT["Cin"], CT["Cout"], 4, 2, 1)
-        wsp = torch.empty(max(1, wsz // 4), device=dev)  # room for the staged kernel
+        wsz = FW.fw_convt_workspace_size(CT["Cin"], CT["Cout"], 4, 2, 1)
+        wsp = torch.empty(max(1, wsz // 4), device=dev)
 
         if args.convt_layout == "nhwc":  # profiling the channels-last variant through the same step
             x_nhwc = d[("ct", "x")].permute(0, 2, 3, 1).contiguous()
@@ -526,8 +524,7 @@ def run_gpu(args):
                 CT["scale"], out=h_ct, workspace=hws_ct)
         specs.append(dict(name="convt", work=ct_flops(N=n), unit="TFLOP/s", scale=1e12, bound="tensor",
                           run=lambda: op_ct(d, out_ct), e2e=lambda: host_ct(), out=h_ct,
-                          kernel=("convt_k4s2_tc_kernel<16,0,0,1> (tcgen05 kind::tf32; slabs by bulk copies from "
-                                  "the staged x) + convt_stage_x_kernel + weight prepack"),
+                          kernel="convt_k4s2_tc_kernel<16> (tcgen05 kind::tf32) + weight prepack",
                           source="convt_tc.cu"))
 
     def barrier():
@@ -640,15 +637,6 @@ def run_gpu(args):
             u_ms = med_ms(lambda: FW.fw_convtranspose2d_softmax_bias_scale_sigmoid_unfused(
                 d[("ct", "x")], d[("ct", "w")], d[("ct", "conv_b")], d[("ct", "bias")], CT["scale"],
                 out=out_ct, workspace=wsp_ct))
-            # the gathering kernel (workspace of the weight rewrite only), beside the staged one
-            ws_small = torch.empty(FW.fw_convt_workspace_size(CT["Cin"], CT["Cout"], 4, 2, 1) // 4, device=dev)
-            g_ms = med_ms(lambda: FW.fw_convtranspose2d_softmax_bias_scale_sigmoid(
-                d[("ct", "x")], d[("ct", "w")], d[("ct", "conv_b")], d[("ct", "bias")], CT["scale"], out=out_ct,
-                workspace=ws_small))
-            fusion["convt_gather"] = {"ms": g_ms, "staged_ms": f_ms,
-                                      "kernel": "convt_k4s2_tc_kernel<16,0,0,0>: producer warps gather the slabs "
-                                                "from NCHW x (workspace of the weight rewrite only)"}
-            del ws_small
             fusion["convt"] = {"fused_ms": f_ms, "unfused_ms": u_ms, "unfused_over_fused": u_ms / f_ms,
                                "intermediate_bytes": 4 * n * CT["Cout"] * 129 * 129,
                                "unfused": "convt_k4s2_tc_kernel raw mode (conv-transpose + conv_b to memory) + "
@@ -749,10 +737,9 @@ def run_gpu(args):
             line["convpool_ffma_tflops"] = v["tflops"]  # the FP32-FMA call, timed beside the step
             line["convpool_ffma_fp32_frac"] = v["frac_of_fp32_peak"]
         line["fusion"] = fusion
-    if (args.only or args.batch or args.convt_layout != "nchw" or args.convpool_precision != "x3"
-            or args.convt_kernel != "staged"):
+    if args.only or args.batch or args.convt_layout != "nchw" or args.convpool_precision != "x3":
         line["config"]["subset"] = {"only": args.only, "batch": args.batch, "convt_layout": args.convt_layout,
-                                    "convpool_precision": args.convpool_precision, "convt_kernel": args.convt_kernel}
+                                    "convpool_precision": args.convpool_precision}
     print(json.dumps(line), flush=True)
     if ws > 1:
         dist.barrier()
@@ -774,8 +761,6 @@ def main(argv=None):
     ap.add_argument("--batch", type=int, default=0, help="smaller batch for every workload (profiling)")
     ap.add_argument("--convt-layout", default="nchw", choices=["nchw", "nhwc"],
                     help="layout of the conv-transpose in the timed step (nhwc: channels-last variant, profiling)")
-    ap.add_argument("--convt-kernel", default="staged", choices=["staged", "gather"],
-                    help="conv-transpose kernel in the timed step (gather: workspace without the staged x; profiling)")
     ap.add_argument("--convpool-precision", default="x3", choices=["x3", "tf32"],
                     help="conv+pool in the timed step: 3xTF32 split (x3) or plain TF32 (profiling)")
     ap.add_argument("--no-fusion-compare", action="store_true",

@@ -195,12 +195,7 @@ fw_status fw_maxpool2d_out_shape_ex(int H, int W, int k, int s, int p, int d, in
  *        fw_convt_workspace_size(Cin, Cout, k, s, p) bytes, 256-byte aligned
  *        (NULL/0 when that size is 0).  The call rewrites the weight into it
  *        (one layout per output parity class); its contents are undefined
- *        afterwards.  Two calls that overlap in time must not share it.  With at
- *        least fw_convt_workspace_size_ex(N, Cin, H, W, Cout, k, s, p, op) bytes
- *        (on the tensor-core shapes: the weight rewrite plus a TF32 copy of x laid
- *        out as the kernel reads it, about 1.03x the size of x), the call also
- *        stages x there and takes the staged kernel, whose input tiles are moved
- *        by the bulk-copy engine; the result is bit-identical.
+ *        afterwards.  Two calls that overlap in time must not share it.
  * k = 4, s = 2, p = 1 and Cout = 128 take the phase-decomposed tiled kernel
  * (each output parity class is a 2x2 convolution); other arguments take a
  * direct one.
@@ -258,11 +253,6 @@ fw_status fw_convtranspose2d_softmax_bias_scale_sigmoid_nhwc(const float *x, int
 /* Bytes of device workspace fw_convtranspose2d_softmax_bias_scale_sigmoid
  * needs for these arguments (0 when it needs none). */
 unsigned long long fw_convt_workspace_size(int Cin, int Cout, int k, int s, int p);
-
-/* Bytes of device workspace with which fw_convtranspose2d_softmax_bias_scale_sigmoid
- * takes its fastest kernel for this problem (the staged one on the tensor-core
- * shapes; otherwise the same as fw_convt_workspace_size).  0 for invalid sizes. */
-unsigned long long fw_convt_workspace_size_ex(int N, int Cin, int H, int W, int Cout, int k, int s, int p, int op);
 
 /*
  * Allocation-free variant of fw_convtranspose2d_softmax_bias_scale_sigmoid (no

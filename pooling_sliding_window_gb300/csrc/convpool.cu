@@ -28,6 +28,11 @@
 
 namespace fw {
 
+// Range violations found by the checked build's kernels in this file.
+__device__ unsigned g_err_convpool = 0;
+#define CHK(p, bytes, base, base_bytes) chk(&g_err_convpool, (p), (bytes), (base), (base_bytes))
+#define CHKS(p, bytes) chk_smem(&g_err_convpool, (p), (bytes))
+
 namespace {
 
 constexpr int TILE_R = 16, TILE_C = 32;          // conv pixels per CTA
@@ -57,11 +62,15 @@ convpool3x3_ffma_kernel(const float *__restrict__ x, const float *__restrict__ w
     const int co0 = (int)(blockIdx.x % ncob) * cob;
     const long long per_block = (long long)N * tiles;
     const int gstride = gridDim.x / ncob;
+    // buffer extents for the checked build
+    const long long x_bytes = 4LL * N * Cin * H * W, w_bytes = 4LL * Cout * Cin * 9;
+    const long long out_bytes = 4LL * N * Cout * Ho * Wo;
     for (int e = tid; e < WSZ; e += blockDim.x) {
         const int j = e % cob, u = e / cob, tap = u % 9, ci = u / 9;
         const int co = co0 + j;
         const bool ok = co < Cout;
-        cp_async4(smem_u32(ws + e), ok ? w + ((long long)co * Cin + ci) * 9 + tap : w, ok ? 4u : 0u);
+        const float *src = ok ? w + ((long long)co * Cin + ci) * 9 + tap : w;
+        if (CHK(src, 4, w, w_bytes) && CHKS(ws + e, 4)) cp_async4(smem_u32(ws + e), src, ok ? 4u : 0u);
     }
     // copies of item j's input tile into buffer b, zero-filled outside x: per staged row, eight
     // 16-byte copies and two 4-byte ones when x rows are 16-byte aligned, else 34 4-byte ones
@@ -79,6 +88,8 @@ convpool3x3_ffma_kernel(const float *__restrict__ x, const float *__restrict__ w
                 const int c = k < 8 ? 4 * k : 24 + k;  // k = 8, 9: columns 32, 33
                 const bool ok = ih < H && col0 + c < W;  // W % 4 == 0: a 16-byte piece is all in or out
                 const float *src = ok ? xn + ((long long)ci * H + ih) * W + col0 + c : x;
+                const int nb = k < 8 ? 16 : 4;
+                if (!(CHK(src, ok ? nb : 0, x, x_bytes) && CHKS(xsb + row * XP + c, nb))) continue;
                 if (k < 8)
                     cp_async16(smem_u32(xsb + row * XP + c), src, ok ? 16u : 0u);
                 else
@@ -89,8 +100,9 @@ convpool3x3_ffma_kernel(const float *__restrict__ x, const float *__restrict__ w
                 const int c = e % XC, u = e / XC, r = u % XR, ci = u / XR;
                 const int ih = row0 + r, iw = col0 + c;
                 const bool ok = ih < H && iw < W;
-                cp_async4(smem_u32(xsb + (ci * XR + r) * XP + c), ok ? xn + ((long long)ci * H + ih) * W + iw : x,
-                          ok ? 4u : 0u);
+                const float *src = ok ? xn + ((long long)ci * H + ih) * W + iw : x;
+                if (CHK(src, ok ? 4 : 0, x, x_bytes) && CHKS(xsb + (ci * XR + r) * XP + c, 4))
+                    cp_async4(smem_u32(xsb + (ci * XR + r) * XP + c), src, ok ? 4u : 0u);
             }
         }
         cp_async_commit();
@@ -129,6 +141,8 @@ convpool3x3_ffma_kernel(const float *__restrict__ x, const float *__restrict__ w
         for (int ci = 0; ci < Cin; ++ci) {
             float xv[6][6];
             const float *xr = xs + (ci * XR + 4 * pr) * XP + 4 * pc;
+            const float *wr = ws + ci * 9 * cob + cw;
+            if (!(CHKS(xr, (5 * XP + 6) * 4) && CHKS(wr, (8 * cob + 4) * 4))) continue;
 #pragma unroll
             for (int r = 0; r < 6; ++r) {
                 const float4 a = *reinterpret_cast<const float4 *>(xr + r * XP);
@@ -136,7 +150,6 @@ convpool3x3_ffma_kernel(const float *__restrict__ x, const float *__restrict__ w
                 xv[r][0] = a.x; xv[r][1] = a.y; xv[r][2] = a.z; xv[r][3] = a.w;
                 xv[r][4] = b.x; xv[r][5] = b.y;
             }
-            const float *wr = ws + ci * 9 * cob + cw;
 #pragma unroll
             for (int kh = 0; kh < 3; ++kh)
 #pragma unroll
@@ -192,7 +205,8 @@ convpool3x3_ffma_kernel(const float *__restrict__ x, const float *__restrict__ w
                 for (int wc = 0; wc < NW; ++wc) {
                     const int ph = (row0 + 4 * pr) / POOL + wr_;
                     const int pw = (col0 + 4 * pc) / POOL + wc;
-                    if (ph < Ho && pw < Wo) oc[(long long)ph * Wo + pw] = epilogue(mw[j][wr_][wc], cbv, scale, bv);
+                    if (ph < Ho && pw < Wo && CHK(oc + (long long)ph * Wo + pw, 4, out, out_bytes))
+                        oc[(long long)ph * Wo + pw] = epilogue(mw[j][wr_][wc], cbv, scale, bv);
                 }
         }
         __syncthreads();  // buffer b is free for the item after next
@@ -225,12 +239,16 @@ __global__ void convpool_direct_kernel(const float *__restrict__ x, const float 
                     const float *xp = x + (((long long)n * Cin + ci) * H + oh) * W + ow;
                     const float *wp = w + ((long long)co * Cin + ci) * KH * KW;
                     for (int i = 0; i < KH; ++i)
-                        for (int j = 0; j < KW; ++j) y = fmaf(__ldg(xp + (long long)i * W + j), __ldg(wp + i * KW + j), y);
+                        for (int j = 0; j < KW; ++j) {
+                            const float *xa = xp + (long long)i * W + j, *wa = wp + i * KW + j;
+                            if (CHK(xa, 4, x, 4LL * N * Cin * H * W) && CHK(wa, 4, w, 4LL * Cout * Cin * KH * KW))
+                                y = fmaf(__ldg(xa), __ldg(wa), y);
+                        }
                 }
                 if (u == 0 && v == 0) m = y;
                 else m = use_min ? min_update(m, y) : max_update(m, y);
             }
-        out[idx] = epilogue(m, cb ? __ldg(cb + co) : 0.f, scale, __ldg(bias + co));
+        if (CHK(out + idx, 4, out, 4 * total)) out[idx] = epilogue(m, cb ? __ldg(cb + co) : 0.f, scale, __ldg(bias + co));
     }
 }
 
@@ -301,6 +319,13 @@ fw_status convpool_launch(const float *x, int N, int Cin, int H, int W, const fl
                                                                  W, Cout, KH, KW, pk, ps, Ho, Wo);
     note_launch();
     return launch_status(cudaGetLastError());
+}
+
+unsigned convpool_read_and_clear_error() {
+    unsigned v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_err_convpool, sizeof(v)) != cudaSuccess) return DEVERR_INTERNAL;
+    if (v) cudaMemcpyToSymbol(g_err_convpool, &zero, sizeof(zero));
+    return v;
 }
 
 }  // namespace fw

@@ -49,6 +49,8 @@
 namespace fw {
 
 __device__ unsigned g_err_convpool_tc = 0;
+#define CHK(p, bytes, base, base_bytes) chk(&g_err_convpool_tc, (p), (bytes), (base), (base_bytes))
+#define CHKS(p, bytes) chk_smem(&g_err_convpool_tc, (p), (bytes))
 
 namespace {
 
@@ -173,6 +175,9 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const long long n_items = (long long)Nimg * Ho * ncb;
     const bool use_min = scale < 0.f;
+    // buffer extents for the checked build
+    const long long x_bytes = 4LL * Nimg * CIN * H * W;
+    const long long out_bytes = RAW ? 4LL * Nimg * N * (P * Ho) * (P * Wo) : 4LL * Nimg * N * Ho * Wo;
 
     for (int i = tid; i < N; i += NTHREADS) {
         sCb[i] = cb ? __ldg(cb + i) : 0.f;
@@ -187,13 +192,18 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
         const float hi = tc::to_tf32(v), lo = tc::to_tf32(v - hi);
         if constexpr (C::STACK) {
             const int np = (2 - tap / 3) * N + co;
-            *reinterpret_cast<float *>(sB + (tap % 3) * 3 * C::BTAP + (np / 8) * CORE + (ci / 4) * 128 +
-                                       (np % 8) * 16 + (ci % 4) * 4) = hi;
+            float *d = reinterpret_cast<float *>(sB + (tap % 3) * 3 * C::BTAP + (np / 8) * CORE + (ci / 4) * 128 +
+                                                 (np % 8) * 16 + (ci % 4) * 4);
+            if (CHKS(d, 4)) *d = hi;
             continue;
         }
         const int base = tap * C::BTAP + (ci / 4) * 128 + (ci % 4) * 4;
-        *reinterpret_cast<float *>(sB + base + (co / 8) * CORE + (co % 8) * 16) = hi;
-        if constexpr (X3) *reinterpret_cast<float *>(sB + base + ((N + co) / 8) * CORE + ((N + co) % 8) * 16) = lo;
+        float *dh = reinterpret_cast<float *>(sB + base + (co / 8) * CORE + (co % 8) * 16);
+        if (CHKS(dh, 4)) *dh = hi;
+        if constexpr (X3) {
+            float *dl = reinterpret_cast<float *>(sB + base + ((N + co) / 8) * CORE + ((N + co) % 8) * 16);
+            if (CHKS(dl, 4)) *dl = lo;
+        }
     }
     if (tid == 0) {
         for (int s = 0; s < C::NST; ++s) {
@@ -257,9 +267,16 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
         auto load_main = [&](const float *src, int col, bool ok, int ci) {
             const float *sp = src + ci * plane_stride;
             if (vec)  // W % 4 == 0: the 4 columns are all in or all out
-                return ok && col < W ? __ldg(reinterpret_cast<const float4 *>(sp)) : make_float4(0.f, 0.f, 0.f, 0.f);
+                return ok && col < W && CHK(sp, 16, x, x_bytes) ? __ldg(reinterpret_cast<const float4 *>(sp))
+                                                                : make_float4(0.f, 0.f, 0.f, 0.f);
+            const int nv = ok ? min(4, max(0, W - col)) : 0;  // columns inside the row
+            if (nv > 0 && !CHK(sp, 4 * nv, x, x_bytes)) return make_float4(0.f, 0.f, 0.f, 0.f);
             return make_float4(ok && col < W ? __ldg(sp) : 0.f, ok && col + 1 < W ? __ldg(sp + 1) : 0.f,
                                ok && col + 2 < W ? __ldg(sp + 2) : 0.f, ok && col + 3 < W ? __ldg(sp + 3) : 0.f);
+        };
+        auto load_tail = [&](const float *src, bool ok, int ci) {
+            const float *sp = src + ci * plane_stride;
+            return ok && CHK(sp, 4, x, x_bytes) ? __ldg(sp) : 0.f;
         };
         float4 vm[CIN];
         float vt[CIN];
@@ -273,7 +290,7 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
 #pragma unroll
             for (int ci = 0; ci < CIN; ++ci) {
                 vm[ci] = load_main(ms, col, ok, ci);
-                vt[ci] = tok ? __ldg(ts + ci * plane_stride) : 0.f;
+                vt[ci] = load_tail(ts, tok, ci);
             }
         }
         int k = 0;
@@ -292,10 +309,11 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
             // hi/lo split of 4 channels of one position into the two halves of the slab
             auto put = [&](unsigned char *dst, float c0, float c1, float c2, float c3) {
                 const float h0 = tc::to_tf32(c0), h1 = tc::to_tf32(c1), h2 = tc::to_tf32(c2), h3 = tc::to_tf32(c3);
-                *reinterpret_cast<float4 *>(dst) = make_float4(h0, h1, h2, h3);
+                if (CHKS(dst, 16)) *reinterpret_cast<float4 *>(dst) = make_float4(h0, h1, h2, h3);
                 if constexpr (X3)
-                    *reinterpret_cast<float4 *>(dst + C::SPLIT) = make_float4(
-                        tc::to_tf32(c0 - h0), tc::to_tf32(c1 - h1), tc::to_tf32(c2 - h2), tc::to_tf32(c3 - h3));
+                    if (CHKS(dst + C::SPLIT, 16))
+                        *reinterpret_cast<float4 *>(dst + C::SPLIT) = make_float4(
+                            tc::to_tf32(c0 - h0), tc::to_tf32(c1 - h1), tc::to_tf32(c2 - h2), tc::to_tf32(c3 - h3));
             };
             if (ptid < MTASK) {
                 unsigned char *dst = slab + mr * RB + 4 * ma * CORE + mrr * 16;
@@ -321,7 +339,7 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
                 put(dst, vt[0], vt[1], vt[2], vt[3]);
                 put(dst + 128, vt[4], vt[5], vt[6], vt[7]);
 #pragma unroll
-                for (int ci = 0; ci < CIN; ++ci) vt[ci] = ntok ? __ldg(nts + ci * plane_stride) : 0.f;
+                for (int ci = 0; ci < CIN; ++ci) vt[ci] = load_tail(nts, ntok, ci);
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -333,6 +351,11 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
             constexpr uint32_t IDESC_HH_HL = tc::idesc_tf32(128, (X3 ? 2 : 1) * N);
             constexpr uint32_t IDESC_LH = tc::idesc_tf32(128, N);
             const uint32_t sB_addr = smem_u32(sB), sSlab_addr = smem_u32(sSlab);
+            // checked build: the shared-memory bytes an MMA reads -- A: 16 core groups
+            // CORE apart plus the second K core 128 B on; B: n rows, 8 per CORE
+            auto mma_ok = [&](uint32_t a_addr, uint32_t b_addr, int n) {
+                return CHKS(a_addr, 15 * CORE + 256) && CHKS(b_addr, (uint32_t)((n / 8 - 1) * CORE + 256));
+            };
             int k = 0, rowc = 0;
             bool ok = true;
             for (long long item = blockIdx.x; ok && item < n_items && !*abort_flag; item += gridDim.x, ++k) {
@@ -371,12 +394,14 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
 #pragma unroll
                         for (int kw = 0; kw < 3; ++kw) {
                             const uint64_t a = a0 + (uint64_t)((i * RB + kw * CORE) >> 4);
+                            const uint32_t a_addr = sSlab_addr + stage * C::SLAB + i * RB + kw * CORE;
                             const int top = fresh && kw == 0 ? i - 1 : jhi;  // last row of the stacked MMA
-                            if (fresh && kw == 0)
+                            if (fresh && kw == 0 && mma_ok(a_addr, sB_addr + kw * BKW + 2 * C::BTAP, N))
                                 tc::mma_tf32(tmem + (uint32_t)(((rowc + i) % C::NSLOT) * C::SLOT_COLS), a,
                                              b0 + (uint64_t)((kw * BKW + 2 * C::BTAP) >> 4),
                                              tc::idesc_tf32(128, N), 0u);
-                            if (top >= jlo)
+                            if (top >= jlo &&
+                                mma_ok(a_addr, sB_addr + kw * BKW + (2 - (i - jlo)) * C::BTAP, (top - jlo + 1) * N))
                                 tc::mma_tf32(dlo, a, b0 + (uint64_t)((kw * BKW + (2 - (i - jlo)) * C::BTAP) >> 4),
                                              tc::idesc_tf32(128, (top - jlo + 1) * N), 1u);
                         }
@@ -399,8 +424,13 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
                         const uint64_t ah = a0 + (uint64_t)((((j + tap / 3) * RB) + (tap % 3) * CORE) >> 4);
                         const uint64_t al = ah + (uint64_t)(C::SPLIT >> 4);
                         const uint64_t bd = b0 + (uint64_t)((tap * C::BTAP) >> 4);
-                        tc::mma_tf32(d, ah, bd, IDESC_HH_HL, tap > 0 ? 1u : 0u);
-                        if constexpr (X3) tc::mma_tf32(d, al, bd, IDESC_LH, 1u);
+                        const uint32_t ah_addr =
+                            sSlab_addr + stage * C::SLAB + (j + tap / 3) * RB + (tap % 3) * CORE;
+                        if (mma_ok(ah_addr, sB_addr + tap * C::BTAP, (X3 ? 2 : 1) * N))
+                            tc::mma_tf32(d, ah, bd, IDESC_HH_HL, tap > 0 ? 1u : 0u);
+                        if constexpr (X3)
+                            if (mma_ok(ah_addr + C::SPLIT, sB_addr + tap * C::BTAP, N))
+                                tc::mma_tf32(d, al, bd, IDESC_LH, 1u);
                     }
                     tc::commit(smem_u32(&bars.slot_full[slot]));
                 }
@@ -464,7 +494,8 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
                     const int pos = 8 * i + (r ^ (2 * (i >> 2)));
 #pragma unroll
                     for (int c = 0; c < C::LDC; ++c)
-                        rs[(h * NH + c0 + c) * MT + pos] = (a[c] + b[c]) + sCb[h * NH + c0 + c];
+                        if (CHKS(rs + (h * NH + c0 + c) * MT + pos, 4))
+                            rs[(h * NH + c0 + c) * MT + pos] = (a[c] + b[c]) + sCb[h * NH + c0 + c];
                     if (c0 + C::LDC < NH) continue;
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_u32(&bars.raw_full[rowc & 1]));
@@ -479,7 +510,9 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
                     for (int e = tid - EPI_WARP0 * 32; e < N * MT; e += NEPI * 32) {
                         const int co = e / MT, cc = e - co * MT;
                         const int ci = cc & 15, cr = cc >> 4;
-                        if (col0 + cc < WI) yrow[(long long)co * HI * WI + cc] = rs[co * MT + 8 * ci + (cr ^ (2 * (ci >> 2)))];
+                        float *d = yrow + (long long)co * HI * WI + cc;
+                        const float *sv = rs + co * MT + 8 * ci + (cr ^ (2 * (ci >> 2)));
+                        if (col0 + cc < WI && CHK(d, 4, out, out_bytes) && CHKS(sv, 4)) *d = *sv;
                     }
                     } else if (use_min) {  // warp-uniform: one instruction per conv value
 #pragma unroll
@@ -531,7 +564,8 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
             for (int i = 0; i < NRES; ++i) {
                 const int co = cbase + i;
                 const float tv = tanh_fast(res[i] + sCb[co]);
-                stg[co * C::PW + ((pwl + rot(co)) & (C::PW - 1))] = __fadd_rn(__fmul_rn(tv, scale), sBias[co]);
+                float *d = stg + co * C::PW + ((pwl + rot(co)) & (C::PW - 1));
+                if (CHKS(d, 4)) *d = __fadd_rn(__fmul_rn(tv, scale), sBias[co]);
             }
             // the group's eight warps have staged this item (its other buffer is still
             // being read only by warps that have not reached this point)
@@ -553,7 +587,8 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
 #pragma unroll
                 for (int i = 0; i < N / CSTEP; ++i, op += CSTEP * cstride) {
                     const int co = co0 + i * CSTEP;
-                    *op = stg[co * C::PW + ((pw + rot(co)) & (C::PW - 1))];
+                    const float *sv = stg + co * C::PW + ((pw + rot(co)) & (C::PW - 1));
+                    if (CHK(op, 4, out, out_bytes) && CHKS(sv, 4)) *op = *sv;
                 }
             }
         }
@@ -634,8 +669,10 @@ __global__ void __launch_bounds__(256) pool_tanh_scale_bias_kernel(const float *
         const long long nc = t / Ho;
         const float *base = y + (nc * (long long)(P * Ho) + (long long)pr * P) * WI + (long long)pw * P;
         float m = use_min ? INFINITY : -INFINITY;
+        const long long y_bytes = 4 * total * P * P;
 #pragma unroll
         for (int r = 0; r < P; ++r) {
+            if (!CHK(base + (long long)r * WI, 4 * P, y, y_bytes)) continue;
             if constexpr (P == 4) {
                 const float4 v = __ldg(reinterpret_cast<const float4 *>(base + (long long)r * WI));
                 m = upd(upd(upd(upd(m, v.x, use_min), v.y, use_min), v.z, use_min), v.w, use_min);
@@ -645,7 +682,7 @@ __global__ void __launch_bounds__(256) pool_tanh_scale_bias_kernel(const float *
             }
         }
         const int co = (int)(nc % C);
-        out[idx] = __fadd_rn(__fmul_rn(tanh_fast(m), scale), __ldg(bias + co));
+        if (CHK(out + idx, 4, out, 4 * total)) out[idx] = __fadd_rn(__fmul_rn(tanh_fast(m), scale), __ldg(bias + co));
     }
 }
 

@@ -31,6 +31,11 @@
 
 namespace fw {
 
+// Range violations found by the checked build's kernels in this file.
+__device__ unsigned g_err_convt = 0;
+#define CHK(p, bytes, base, base_bytes) chk(&g_err_convt, (p), (bytes), (base), (base_bytes))
+#define CHKS(p, bytes) chk_smem(&g_err_convt, (p), (bytes))
+
 namespace {
 
 constexpr int T_M = 8, T_N = 16;   // phase-grid pixels per CTA (rows, cols)
@@ -65,7 +70,8 @@ __global__ void convt_prepack_kernel(const float *__restrict__ w, float *__restr
         const int ph = (int)(r / Cin);
         const int py = ph >> 1, px = ph & 1;
         const int kh = tap_k(py, t >> 1), kw = tap_k(px, t & 1);
-        wp[i] = __ldg(w + (((long long)ci * Cout + co) * 4 + kh) * 4 + kw);
+        const float *src = w + (((long long)ci * Cout + co) * 4 + kh) * 4 + kw;
+        if (CHK(src, 4, w, 4 * total)) wp[i] = __ldg(src);
     }
 }
 
@@ -85,6 +91,9 @@ convt_k4s2_ffma_kernel(const float *__restrict__ x, const float *__restrict__ wp
     const int m0 = tm * T_M, n0 = tn * T_N;
     const float *xn = x + (long long)n_img * Cin * H * W;
     const float *wph = wp + (long long)phase * Cin * WS_CHUNK;
+    // buffer extents for the checked build
+    const long long x_bytes = 4LL * gridDim.z * Cin * H * W, wp_bytes = 16LL * 4 * Cin * COUT_T;
+    const long long out_bytes = 4LL * gridDim.z * COUT_T * Ho * Wo;
 
     float acc[8][8];
 #pragma unroll
@@ -105,9 +114,11 @@ convt_k4s2_ffma_kernel(const float *__restrict__ x, const float *__restrict__ wp
             for (int e = tid; e < CK * XS_CHUNK; e += 256) {
                 const int ih = m0 - 1 + r, iw = n0 + c + sx - 1;
                 float v = 0.f;
-                if (ci < ck && ih >= 0 && ih < H && iw >= 0 && iw < W)
-                    v = __ldg(xn + ((long long)(c0 + ci) * H + ih) * W + iw);
-                xs[e] = v;
+                if (ci < ck && ih >= 0 && ih < H && iw >= 0 && iw < W) {
+                    const float *src = xn + ((long long)(c0 + ci) * H + ih) * W + iw;
+                    if (CHK(src, 4, x, x_bytes)) v = __ldg(src);
+                }
+                if (CHKS(xs + e, 4)) xs[e] = v;
                 sx += 1;
                 r += 5;
                 if (sx >= 3) {
@@ -124,8 +135,11 @@ convt_k4s2_ffma_kernel(const float *__restrict__ x, const float *__restrict__ wp
             const float4 *src = reinterpret_cast<const float4 *>(wph + (long long)c0 * WS_CHUNK);
             float4 *dst = reinterpret_cast<float4 *>(ws);
             const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int e = tid; e < CK * WS_CHUNK / 4; e += blockDim.x)
-                dst[e] = (e < ck * WS_CHUNK / 4) ? __ldg(src + e) : z;
+            for (int e = tid; e < CK * WS_CHUNK / 4; e += blockDim.x) {
+                float4 v = z;
+                if (e < ck * WS_CHUNK / 4 && CHK(src + e, 16, wp, wp_bytes)) v = __ldg(src + e);
+                if (CHKS(dst + e, 16)) dst[e] = v;
+            }
         }
         __syncthreads();
 #pragma unroll 2
@@ -134,9 +148,10 @@ convt_k4s2_ffma_kernel(const float *__restrict__ x, const float *__restrict__ wp
             for (int t = 0; t < 4; ++t) {
                 const int dy = tap_off(py, t >> 1), dx = tap_off(px, t & 1);
                 const float *xr = xs + ((ci * XS_ROWS + warp + dy + 1) * 3 + (dx + 1)) * T_N + 8 * h;
+                const float *wr = ws + (ci * 4 + t) * COUT_T + 4 * g;
+                if (!(CHKS(xr, 32) && CHKS(wr, 16) && CHKS(wr + 64, 16))) continue;
                 const float4 xa = *reinterpret_cast<const float4 *>(xr);
                 const float4 xb = *reinterpret_cast<const float4 *>(xr + 4);
-                const float *wr = ws + (ci * 4 + t) * COUT_T + 4 * g;
                 const float4 wa = *reinterpret_cast<const float4 *>(wr);
                 const float4 wb = *reinterpret_cast<const float4 *>(wr + 64);
                 const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
@@ -158,9 +173,9 @@ convt_k4s2_ffma_kernel(const float *__restrict__ x, const float *__restrict__ wp
         cbv[j] = cb ? __ldg(cb + co) : 0.f;
         bv[j] = __ldg(bias + co);
     }
-    // Exponentials in base 2 (ex2.approx) on log2(e)-scaled arguments and one reciprocal
-    // of the sum per pixel, as in the tensor-core kernel's epilogue (the softmax scales
-    // an error in its argument by p(1 - p) <= 1/4, so the result stays within 1e-5).
+    // Exponentials in base 2 (ex2.approx, relative error ~2^-22) on log2(e)-scaled
+    // arguments and one reciprocal of the sum per pixel, as in the tensor-core kernel's
+    // epilogue; with float32 products and sums the result stays within 1e-5.
     const float ks = -scale * LOG2E_F;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -194,21 +209,29 @@ convt_k4s2_ffma_kernel(const float *__restrict__ x, const float *__restrict__ wp
     for (int j = 0; j < 8; ++j) {
         const int co = (j < 4 ? 4 * g + j : 64 + 4 * g + (j - 4));
 #pragma unroll
-        for (int i = 0; i < 8; ++i) os[(warp * T_N + 8 * h + i) * OS_PITCH + co] = acc[i][j];
+        for (int i = 0; i < 8; ++i) {
+            float *d = os + (warp * T_N + 8 * h + i) * OS_PITCH + co;
+            if (CHKS(d, 4)) *d = acc[i][j];
+        }
     }
     __syncthreads();
     float *on = out + (long long)n_img * COUT_T * Ho * Wo;
     for (int e = tid; e < COUT_T * T_M * T_N; e += blockDim.x) {
         const int nl = e % T_N, ml = (e / T_N) % T_M, co = e / (T_N * T_M);
         const int oh = 2 * (m0 + ml) + py, ow = 2 * (n0 + nl) + px;
-        if (oh < Ho && ow < Wo) on[((long long)co * Ho + oh) * Wo + ow] = os[(ml * T_N + nl) * OS_PITCH + co];
+        float *d = on + ((long long)co * Ho + oh) * Wo + ow;
+        const float *sv = os + (ml * T_N + nl) * OS_PITCH + co;
+        if (oh < Ho && ow < Wo && CHK(d, 4, out, out_bytes) && CHKS(sv, 4)) *d = *sv;
     }
 }
 
-// Gather form of one conv-transpose output.
-__device__ __forceinline__ float convt_gather(const float *__restrict__ xn, const float *__restrict__ w,
+// Gather form of one conv-transpose output (x_bytes, w_bytes: buffer extents for the
+// checked build; xn is image n's part of x).
+__device__ __forceinline__ float convt_gather(const float *__restrict__ x, long long x_bytes,
+                                              const float *__restrict__ xn, const float *__restrict__ w,
                                               float cbv, int Cin, int H, int W, int Cout, int k, int s,
                                               int p, int co, int oh, int ow) {
+    const long long w_bytes = 4LL * Cin * Cout * k * k;
     float y = cbv;
     for (int kh = 0; kh < k; ++kh) {
         const int th = oh + p - kh;
@@ -220,9 +243,11 @@ __device__ __forceinline__ float convt_gather(const float *__restrict__ xn, cons
             if (tw < 0 || tw % s) continue;
             const int iw = tw / s;
             if (iw >= W) continue;
-            for (int ci = 0; ci < Cin; ++ci)
-                y = fmaf(__ldg(xn + ((long long)ci * H + ih) * W + iw),
-                         __ldg(w + (((long long)ci * Cout + co) * k + kh) * k + kw), y);
+            for (int ci = 0; ci < Cin; ++ci) {
+                const float *xa = xn + ((long long)ci * H + ih) * W + iw;
+                const float *wa = w + (((long long)ci * Cout + co) * k + kh) * k + kw;
+                if (CHK(xa, 4, x, x_bytes) && CHK(wa, 4, w, w_bytes)) y = fmaf(__ldg(xa), __ldg(wa), y);
+            }
         }
     }
     return y;
@@ -240,9 +265,11 @@ __global__ void convt_direct_kernel(const float *__restrict__ x, const float *__
         const int oh = (int)(t % Ho);
         const int n = (int)(t / Ho);
         const float *xn = x + (long long)n * Cin * H * W;
+        const long long x_bytes = 4LL * N * Cin * H * W;
         float mx = -INFINITY, sum = 0.f;
         for (int co = 0; co < Cout; ++co) {
-            const float y = convt_gather(xn, w, cb ? __ldg(cb + co) : 0.f, Cin, H, W, Cout, k, s, p, co, oh, ow);
+            const float y = convt_gather(x, x_bytes, xn, w, cb ? __ldg(cb + co) : 0.f, Cin, H, W, Cout, k, s, p, co,
+                                         oh, ow);
             if (y > mx) {
                 sum = sum * expf(mx - y) + 1.f;
                 mx = y;
@@ -251,10 +278,12 @@ __global__ void convt_direct_kernel(const float *__restrict__ x, const float *__
             }
         }
         for (int co = 0; co < Cout; ++co) {
-            const float y = convt_gather(xn, w, cb ? __ldg(cb + co) : 0.f, Cin, H, W, Cout, k, s, p, co, oh, ow);
+            const float y = convt_gather(x, x_bytes, xn, w, cb ? __ldg(cb + co) : 0.f, Cin, H, W, Cout, k, s, p, co,
+                                         oh, ow);
             const float pr = __fdiv_rn(expf(y - mx), sum);
             const float r = __fmul_rn(__fadd_rn(pr, __ldg(bias + co)), scale);
-            out[(((long long)n * Cout + co) * Ho + oh) * Wo + ow] = __fdiv_rn(1.f, 1.f + expf(-r));
+            float *d = out + (((long long)n * Cout + co) * Ho + oh) * Wo + ow;
+            if (CHK(d, 4, out, 4LL * N * Cout * Ho * Wo)) *d = __fdiv_rn(1.f, 1.f + expf(-r));
         }
     }
 }
@@ -273,8 +302,8 @@ bool force_ffma() {
 
 bool convt_tc_eligible(int Cin, int Cout, int k, int s, int p);
 fw_status convt_tc_launch(const float *x, int N, int Cin, int H, int W, const float *w, const float *cb,
-                          const float *bias, float scale, float *out, int Ho, int Wo, void *ws, size_t ws_bytes,
-                          cudaStream_t st, bool prepack);
+                          const float *bias, float scale, float *out, int Ho, int Wo, void *ws, cudaStream_t st,
+                          bool prepack);
 
 size_t convt_workspace_bytes(int Cin, int Cout, int k, int s, int p) {
     if (k == 4 && s == 2 && p == 1 && Cout == COUT_T) return (size_t)16 * Cin * Cout * sizeof(float);
@@ -291,7 +320,7 @@ fw_status convt_launch(const float *x, int N, int Cin, int H, int W, const float
     if (need > 0) {
         if (!ws || ws_bytes < need) return FW_ERR_NULL;
         if (!ffma && convt_tc_eligible(Cin, Cout, k, s, p) && !force_ffma())
-            return convt_tc_launch(x, N, Cin, H, W, w, cb, bias, scale, out, Ho, Wo, ws, ws_bytes, st, !weights_ready);
+            return convt_tc_launch(x, N, Cin, H, W, w, cb, bias, scale, out, Ho, Wo, ws, st, !weights_ready);
         float *wp = static_cast<float *>(ws);
         if (!weights_ready) {
             convt_prepack_kernel<<<(unsigned)min(1024LL, (16LL * Cin * Cout + 255) / 256), 256, 0, st>>>(w, wp, Cin,
@@ -324,6 +353,13 @@ fw_status convt_launch(const float *x, int N, int Cin, int H, int W, const float
                                                               k, s, p, Ho, Wo);
     note_launch();
     return launch_status(cudaGetLastError());
+}
+
+unsigned convt_read_and_clear_error() {
+    unsigned v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_err_convt, sizeof(v)) != cudaSuccess) return DEVERR_INTERNAL;
+    if (v) cudaMemcpyToSymbol(g_err_convt, &zero, sizeof(zero));
+    return v;
 }
 
 }  // namespace fw
@@ -377,8 +413,7 @@ extern "C" fw_status fw_convtranspose2d_softmax_bias_scale_sigmoid_noalloc(
         const fw_status rc = fw::convt_static_workspace(&ws);
         if (rc != FW_OK) return rc;
     }
-    // exactly the weight rewrite's bytes: the call keeps to the kernels that need no
-    // more workspace than that (never the staged copy of x)
     return fw_convtranspose2d_softmax_bias_scale_sigmoid(x, N, Cin, H, W, w, conv_b, Cout, k, s, p, op, bias,
-                                                         scale, out, ws, need, stream);
+                                                         scale, out, ws, need > 0 ? FW_CONVT_STATIC_WS_BYTES : 0,
+                                                         stream);
 }

@@ -47,34 +47,24 @@
 // stays within 1e-5 of the float64 oracle; logits a few times larger, or one
 // dominant channel, give errors of a few 1e-4, inside the 5e-3 bound of the TF32
 // path.  The float32 FMA kernels (convt.cu) keep 1e-5 for any softmax.
-#include <cstdlib>
-
 #include "fw_common.cuh"
 
 namespace fw {
 
 __device__ unsigned g_err_convt_tc = 0;
+#define CHK(p, bytes, base, base_bytes) chk(&g_err_convt_tc, (p), (bytes), (base), (base_bytes))
+#define CHKS(p, bytes) chk_smem(&g_err_convt_tc, (p), (bytes))
 
 namespace {
 
 constexpr int COUT = 128;
 constexpr int MT = 128;            // anchors per tile
 constexpr int NSTAGE = 2;          // slab stages
-
-// Warp roles.  Gathering kernel: warps 0-6 gather slabs, three epilogue groups of 4
-// warps (each covering TMEM lane quarters 0-3) serve three accumulators, the last
-// warp issues the MMAs.  Staged kernel (slabs moved by the bulk-copy engine from a
-// pre-staged copy of x): one lane of warp 0 issues the copies, four epilogue groups
-// serve four accumulators (all 512 TMEM columns).
-template <bool STAGED>
-struct Roles {
-    static constexpr int PROD_WARPS = STAGED ? 1 : 7;
-    static constexpr int EPI_WARP0 = PROD_WARPS;
-    static constexpr int NACC = STAGED ? 4 : 3;  // TMEM accumulators of 128 columns, one epilogue group each
-    static constexpr int MMA_WARP = EPI_WARP0 + 4 * NACC;
-    static constexpr int NTHREADS = (MMA_WARP + 1) * 32;
-};
-constexpr int NACC_MAX = 4;
+constexpr int PROD_WARPS = 7;      // warps 0-6
+constexpr int EPI_WARP0 = PROD_WARPS;  // NACC groups of 4 warps (each covers TMEM lane quarters 0-3)
+constexpr int NACC = 3;            // TMEM accumulators (128 columns each), one epilogue group each
+constexpr int MMA_WARP = EPI_WARP0 + 4 * NACC;
+constexpr int NTHREADS = (MMA_WARP + 1) * 32;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
 constexpr uint32_t IDESC = tc::idesc_tf32(128, COUT);
@@ -101,50 +91,8 @@ __global__ void convt_tc_prepack_kernel(const float *__restrict__ w, float *__re
         const int t = (int)(r & 3), phase = (int)(r >> 2);
         const int py = phase >> 1, px = phase & 1;
         const int kh = tap_k(py, t >> 1), kw = tap_k(px, t & 1);
-        wtc[i] = tc::to_tf32(__ldg(w + (((long long)(4 * g + c4) * COUT + co) * 4 + kh) * 4 + kw) * LOG2E);
-    }
-}
-
-// Staged copy of x for the staged kernel: per plane of 4 input channels, the
-// stacked position sequence (see the top of this file) as TF32 float4s, preceded by
-// XS_FRONT zero positions (a slab of tile 0 starts at position -1) and padded with
-// zeros past the last position any slab reads.
-constexpr int XS_FRONT = 8;
-
-__host__ __device__ inline long long xs_plane_positions(int N, int H, int W) {
-    const long long BW = W + 1, n_anchor = (long long)N * (H + 1) * BW;
-    const long long n_tiles = (n_anchor + MT - 1) / MT;
-    // a slab reads positions up to n_tiles * MT + 2 * BW
-    return (XS_FRONT + n_tiles * MT + 2 * BW + 1 + 7) / 8 * 8;
-}
-
-// xs[g][XS_FRONT + q] = tf32(x[n][4g .. 4g+3][row][c]) for position q = R*(W+1) + c,
-// R = n*(H+1) + row + 1 (zero for the extra column, the zero rows and the padding).
-__global__ void __launch_bounds__(256) convt_stage_x_kernel(const float *__restrict__ x, float4 *__restrict__ xs,
-                                                            int N, int Cin, int H, int W, long long xs_plane) {
-    const long long total = (long long)(Cin / 4) * xs_plane;
-    const int BW = W + 1, BH = H + 1;
-    const long long n_pos = ((long long)N * BH + 1) * BW;
-    const long long plane = (long long)H * W;
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-         i += (long long)gridDim.x * blockDim.x) {
-        const long long g = i / xs_plane;
-        const long long q = i - g * xs_plane - XS_FRONT;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (q >= 0 && q < n_pos) {
-            const long long R = q / BW;
-            const int c = (int)(q - R * BW);
-            if (c < W && R > 0) {
-                const long long n = (R - 1) / BH;
-                const int row = (int)(R - 1 - n * BH);
-                if (row < H) {
-                    const float *src = x + ((n * Cin + 4 * g) * H + row) * (long long)W + c;
-                    v = make_float4(tc::to_tf32(__ldg(src)), tc::to_tf32(__ldg(src + plane)),
-                                    tc::to_tf32(__ldg(src + 2 * plane)), tc::to_tf32(__ldg(src + 3 * plane)));
-                }
-            }
-        }
-        xs[i] = v;
+        const float *src = w + (((long long)(4 * g + c4) * COUT + co) * 4 + kh) * 4 + kw;
+        if (CHK(src, 4, w, 4 * total)) wtc[i] = tc::to_tf32(__ldg(src) * LOG2E);
     }
 }
 
@@ -152,8 +100,8 @@ struct Bars {
     uint64_t b_full;
     uint64_t slab_full[NSTAGE];
     uint64_t slab_empty[NSTAGE];
-    uint64_t acc_full[NACC_MAX];
-    uint64_t acc_empty[NACC_MAX];
+    uint64_t acc_full[NACC];
+    uint64_t acc_empty[NACC];
     uint32_t tmem_base;
     int abort;
 };
@@ -186,18 +134,11 @@ __device__ __forceinline__ float ex2_approx(float x) {
 // NHWC = true: x is [N, H, W, Cin] and out [N, Ho, Wo, Cout] (channels last); the
 // gather then loads 4 channels per lane with one 16-byte load, and each epilogue
 // thread writes its pixel's 128 channels as 256-bit stores (whole 32-byte sectors).
-// STAGED = true: x has been rewritten by convt_stage_x_kernel into `xs` (TF32, the
-// planar stacked-position layout of the slabs, xs_plane positions per plane), so a
-// slab is G contiguous runs that one lane moves with the bulk-copy engine.
-template <int G, bool RAW, bool NHWC = false, bool STAGED = false>  // G = input channels / 4
-__global__ void __launch_bounds__(Roles<STAGED>::NTHREADS, 1)
+template <int G, bool RAW, bool NHWC = false>  // G = input channels / 4
+__global__ void __launch_bounds__(NTHREADS, 1)
 convt_k4s2_tc_kernel(const float *__restrict__ x, const float *__restrict__ wtc, const float *__restrict__ cb,
                      const float *__restrict__ bias, float scale, float *__restrict__ out, int N, int H, int W,
-                     int Ho, int Wo, int nslab, int L, const float4 *__restrict__ xs, long long xs_plane) {
-    constexpr int PROD_WARPS = Roles<STAGED>::PROD_WARPS, EPI_WARP0 = Roles<STAGED>::EPI_WARP0;
-    constexpr int NACC = Roles<STAGED>::NACC, MMA_WARP = Roles<STAGED>::MMA_WARP;
-    constexpr int NTHREADS = Roles<STAGED>::NTHREADS;
-    static_assert(!(STAGED && (RAW || NHWC)), "the staged kernel serves the fused NCHW operator");
+                     int Ho, int Wo, int nslab, int L) {
     constexpr int CIN = 4 * G;
     constexpr int B_BYTES = 4 * G * COUT * 16;  // 4 taps x G planes x 128 co x 16 B
     extern __shared__ __align__(1024) unsigned char smem[];
@@ -218,6 +159,9 @@ convt_k4s2_tc_kernel(const float *__restrict__ x, const float *__restrict__ wtc,
     const int n_tiles = (int)((n_anchor + MT - 1) / MT);
     const int dx0 = px == 0 ? -1 : 0;  // smaller horizontal tap offset of the phase
     const int dy0 = py == 0 ? -1 : 0;  // smaller vertical tap offset of the phase
+    // buffer extents for the checked build
+    const long long x_bytes = 4LL * N * CIN * H * W, out_bytes = 4LL * N * COUT * Ho * Wo;
+    const long long wtc_bytes = 16LL * CIN * COUT * 4;
 
     for (int i = tid; i < COUT; i += NTHREADS) {
         sCb[i] = cb ? __ldg(cb + i) * LOG2E : 0.f;
@@ -226,7 +170,7 @@ convt_k4s2_tc_kernel(const float *__restrict__ x, const float *__restrict__ wtc,
     if (tid == 0) {
         mbar_init(smem_u32(&bars.b_full), 1);
         for (int s = 0; s < NSTAGE; ++s) {
-            mbar_init(smem_u32(&bars.slab_full[s]), STAGED ? 1 : PROD_WARPS);
+            mbar_init(smem_u32(&bars.slab_full[s]), PROD_WARPS);
             mbar_init(smem_u32(&bars.slab_empty[s]), 1);
         }
         for (int b = 0; b < NACC; ++b) {
@@ -248,41 +192,7 @@ convt_k4s2_tc_kernel(const float *__restrict__ x, const float *__restrict__ wtc,
         atomicOr(&g_err_convt_tc, DEVERR_TIMEOUT);
     };
 
-    if (STAGED && warp < PROD_WARPS) {
-        // ------------------------------------------- slabs by the bulk-copy engine
-        // One lane: per slab, G copies of L positions (one per plane of 4 channels),
-        // completing on the stage's full barrier.
-        if (lane == 0) {
-            int k = 0;
-            bool ok = true;
-            int last_use[NSTAGE] = {-1, -1};  // last use of each stage a copy was issued for
-            for (int tile = rank; ok && tile < n_tiles && !*abort_flag; tile += nct) {
-                for (int s = 0; s < nslab; ++s, ++k) {
-                    const int stage = k & 1, use = k >> 1;
-                    if (use > 0 && !mbar_wait_bounded(smem_u32(&bars.slab_empty[stage]), (use - 1) & 1)) {
-                        fail();
-                        ok = false;
-                        break;
-                    }
-                    last_use[stage] = use;
-                    const int dy_lo = nslab == 1 ? dy0 : tap_off(py, s);
-                    const long long pbase = (long long)tile * MT + BW + (long long)dy_lo * BW + dx0;
-                    const uint32_t bar = smem_u32(&bars.slab_full[stage]);
-                    mbar_arrive_expect_tx(bar, (uint32_t)slab_bytes);
-                    const uint32_t dst = smem_u32(sSlab + stage * slab_bytes);
-                    const float4 *src = xs + XS_FRONT + pbase;
-                    for (int g = 0; g < G; ++g)
-                        bulk_g2s(dst + (uint32_t)(g * slab_plane), src + g * xs_plane, (uint32_t)slab_plane, bar);
-                }
-            }
-            // No copy may still be landing in shared memory when the CTA exits: wait
-            // (bounded) for the last copy issued into each stage (already complete
-            // unless the pipeline was aborted).
-            for (int st = 0; st < NSTAGE; ++st)
-                if (last_use[st] >= 0) mbar_wait_bounded(smem_u32(&bars.slab_full[st]), last_use[st] & 1);
-        }
-        __syncwarp();
-    } else if (!STAGED && warp < PROD_WARPS) {
+    if (warp < PROD_WARPS) {
         // ------------------------------------------------------------ producers
         // Each thread owns at most one position of a slab (L <= 224 when one slab
         // covers both vertical taps; two positions otherwise).  Its channel loads
@@ -315,9 +225,14 @@ convt_k4s2_tc_kernel(const float *__restrict__ x, const float *__restrict__ wtc,
                 const long long pbase = (long long)tile * MT + BW + (long long)dy_lo * BW + dx0;
                 return tid < L ? pos_src(pbase + tid) : nullptr;
             };
+            // checked build: a position's CIN channel loads lie between its first and last
+            auto src_ok = [&](const float *src) {
+                return src && CHK(src, 4, x, x_bytes) && CHK(src + (CIN - 1) * plane_stride, 4, x, x_bytes);
+            };
             float r[CIN];
             {
                 const float *src = rank < n_tiles ? slab_src(rank, 0) : nullptr;
+                if (!src_ok(src)) src = nullptr;
 #pragma unroll
                 for (int ci = 0; ci < CIN; ++ci) r[ci] = src ? __ldg(src + ci * plane_stride) : 0.f;
             }
@@ -331,14 +246,16 @@ convt_k4s2_tc_kernel(const float *__restrict__ x, const float *__restrict__ wtc,
                         ntile += nct;
                     }
                     const float *nsrc = ntile < n_tiles ? slab_src(ntile, ns) : nullptr;
+                    if (!src_ok(nsrc)) nsrc = nullptr;
                     if (use > 0 && !mbar_wait_bounded(smem_u32(&bars.slab_empty[stage]), (use - 1) & 1)) fail();
                     unsigned char *slab = sSlab + stage * slab_bytes;
                     if (tid < L) {
 #pragma unroll
                         for (int g = 0; g < G; ++g) {
-                            *reinterpret_cast<float4 *>(slab + g * slab_plane + tid * 16) =
-                                make_float4(tc::to_tf32(r[4 * g]), tc::to_tf32(r[4 * g + 1]),
-                                            tc::to_tf32(r[4 * g + 2]), tc::to_tf32(r[4 * g + 3]));
+                            if (CHKS(slab + g * slab_plane + tid * 16, 16))
+                                *reinterpret_cast<float4 *>(slab + g * slab_plane + tid * 16) =
+                                    make_float4(tc::to_tf32(r[4 * g]), tc::to_tf32(r[4 * g + 1]),
+                                                tc::to_tf32(r[4 * g + 2]), tc::to_tf32(r[4 * g + 3]));
 #pragma unroll
                             for (int j = 0; j < 4; ++j)
                                 r[4 * g + j] = nsrc ? __ldg(nsrc + (4 * g + j) * plane_stride) : 0.f;
@@ -383,9 +300,10 @@ convt_k4s2_tc_kernel(const float *__restrict__ x, const float *__restrict__ wtc,
                         for (int j = 0; j < NB; ++j) {
                             const int pos = b0 + pslot + PPP * j;
                             r[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-                            if (pos < L && q >= 0 && q < n_pos && c >= 0 && c < W && row >= 0 && row < H)
-                                r[j] = __ldg(reinterpret_cast<const float4 *>(
-                                    x + (((long long)n * H + row) * W + c) * CIN + 4 * g));
+                            const float *xa = x + (((long long)n * H + row) * W + c) * CIN + 4 * g;
+                            if (pos < L && q >= 0 && q < n_pos && c >= 0 && c < W && row >= 0 && row < H &&
+                                CHK(xa, 16, x, x_bytes))
+                                r[j] = __ldg(reinterpret_cast<const float4 *>(xa));
                             q += PPP;
                             c += PPP;
                             while (c >= BW) {
@@ -403,7 +321,7 @@ convt_k4s2_tc_kernel(const float *__restrict__ x, const float *__restrict__ wtc,
 #pragma unroll
                         for (int j = 0; j < NB; ++j) {
                             const int pos = b0 + pslot + PPP * j;
-                            if (pos < L)
+                            if (pos < L && CHKS(slab + g * slab_plane + pos * 16, 16))
                                 *reinterpret_cast<float4 *>(slab + g * slab_plane + pos * 16) =
                                     make_float4(tc::to_tf32(r[j].x), tc::to_tf32(r[j].y), tc::to_tf32(r[j].z),
                                                 tc::to_tf32(r[j].w));
@@ -428,6 +346,8 @@ convt_k4s2_tc_kernel(const float *__restrict__ x, const float *__restrict__ wtc,
                             if (row < H) src = x + (((long long)n * CIN) * H + row) * (long long)W + c;
                         }
                     }
+                    if (src && !(CHK(src, 4, x, x_bytes) && CHK(src + (CIN - 1) * plane_stride, 4, x, x_bytes)))
+                        src = nullptr;
                     float r[CIN];
 #pragma unroll
                     for (int ci = 0; ci < CIN; ++ci) r[ci] = src ? __ldg(src + ci * plane_stride) : 0.f;
@@ -439,7 +359,8 @@ convt_k4s2_tc_kernel(const float *__restrict__ x, const float *__restrict__ wtc,
                     for (int g = 0; g < G; ++g) {
                         const float4 v = make_float4(tc::to_tf32(r[4 * g]), tc::to_tf32(r[4 * g + 1]),
                                                      tc::to_tf32(r[4 * g + 2]), tc::to_tf32(r[4 * g + 3]));
-                        *reinterpret_cast<float4 *>(slab + g * slab_plane + pos * 16) = v;
+                        if (CHKS(slab + g * slab_plane + pos * 16, 16))
+                            *reinterpret_cast<float4 *>(slab + g * slab_plane + pos * 16) = v;
                     }
                 }
                 // threads without a position still wait, so the whole warp arrives in order
@@ -454,10 +375,14 @@ convt_k4s2_tc_kernel(const float *__restrict__ x, const float *__restrict__ wtc,
         // ------------------------------------------------------------ MMA issue
         if (lane == 0) {
             const uint32_t bfull = smem_u32(&bars.b_full);
-            mbar_arrive_expect_tx(bfull, B_BYTES);
             const unsigned char *src = reinterpret_cast<const unsigned char *>(wtc) + (size_t)phase * B_BYTES;
-            for (int off = 0; off < B_BYTES; off += 32768)
-                bulk_g2s(smem_u32(sB + off), src + off, (uint32_t)min(32768, B_BYTES - off), bfull);
+            if (CHK(src, B_BYTES, wtc, wtc_bytes) && CHKS(sB, B_BYTES)) {
+                mbar_arrive_expect_tx(bfull, B_BYTES);
+                for (int off = 0; off < B_BYTES; off += 32768)
+                    bulk_g2s(smem_u32(sB + off), src + off, (uint32_t)min(32768, B_BYTES - off), bfull);
+            } else {
+                mbar_arrive(bfull);  // checked build: no copy, the weights stay unset
+            }
             bool ok = mbar_wait_bounded(bfull, 0);
             if (!ok) fail();
             tc::fence_after_sync();
@@ -490,11 +415,15 @@ convt_k4s2_tc_kernel(const float *__restrict__ x, const float *__restrict__ wtc,
                             const int tap = 2 * ty + tx;
 #pragma unroll
                             for (int j = 0; j < G / 2; ++j) {
-                                const uint64_t ad =
-                                    tc::smem_desc(slab + (2 * j * L + o) * 16, (uint32_t)slab_plane, 128);
-                                const uint64_t bd =
-                                    tc::smem_desc(sB_addr + (tap * G + 2 * j) * (COUT * 16), COUT * 16, 128);
-                                tc::mma_tf32(d, ad, bd, IDESC, acc);
+                                const uint32_t a_addr = slab + (2 * j * L + o) * 16;
+                                const uint32_t b_addr = sB_addr + (tap * G + 2 * j) * (COUT * 16);
+                                const uint64_t ad = tc::smem_desc(a_addr, (uint32_t)slab_plane, 128);
+                                const uint64_t bd = tc::smem_desc(b_addr, COUT * 16, 128);
+                                // checked build: A 16 groups 128 B apart + a second K plane;
+                                // B likewise with the planes COUT * 16 B apart
+                                if (CHKS(a_addr, 15 * 128 + slab_plane + 128) &&
+                                    CHKS(b_addr, 15 * 128 + COUT * 16 + 128))
+                                    tc::mma_tf32(d, ad, bd, IDESC, acc);
                             }
                         }
                     }
@@ -557,7 +486,8 @@ convt_k4s2_tc_kernel(const float *__restrict__ x, const float *__restrict__ wtc,
                 for (int c = 0; c < COUT / 32; ++c) {
                     tc::ld32(taddr + 32 * c, v);
                     tc::wait_ld();
-                    if (valid) {
+                    if (valid && CHK(o + 32 * c * plane_out, 4, out, out_bytes) &&
+                        CHK(o + (32 * c + 31) * plane_out, 4, out, out_bytes)) {
 #pragma unroll
                         for (int i = 0; i < 32; ++i) o[(32 * c + i) * plane_out] = v[i] * LN2;
                     }
@@ -601,7 +531,12 @@ convt_k4s2_tc_kernel(const float *__restrict__ x, const float *__restrict__ wtc,
             for (int c = 0; c < COUT / 32; ++c) {
                 tc::ld32(taddr + 32 * c, v);
                 tc::wait_ld();
-                if (valid) {
+                // checked build: the chunk's 32 channels lie between its first and last store
+                const bool in_range = !FW_CHECKED ||
+                                      (NHWC ? CHK(o + 32 * c, 128, out, out_bytes)
+                                            : CHK(o + 32 * c * plane_out, 4, out, out_bytes) &&
+                                                  CHK(o + (32 * c + 31) * plane_out, 4, out, out_bytes));
+                if (valid && in_range) {
                     if constexpr (NHWC) {
 #pragma unroll
                         for (int i = 0; i < 32; i += 4) {
@@ -642,10 +577,9 @@ convt_k4s2_tc_kernel(const float *__restrict__ x, const float *__restrict__ wtc,
     }
 }
 
-template <int G, bool RAW, bool NHWC, bool STAGED = false>
+template <int G, bool RAW, bool NHWC>
 fw_status launch_g(const float *x, int N, int H, int W, const float *wtc, const float *cb, const float *bias,
-                   float scale, float *out, int Ho, int Wo, cudaStream_t st, const float4 *xs = nullptr,
-                   long long xs_plane = 0) {
+                   float scale, float *out, int Ho, int Wo, cudaStream_t st) {
     int dev = 0, sms = 0, optin = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
@@ -662,30 +596,16 @@ fw_status launch_g(const float *x, int N, int H, int W, const float *wtc, const 
     }
     if (smem > limit) return FW_ERR_UNSUPPORTED;
     if (smem < MIN_SMEM) smem = MIN_SMEM;
-    cudaError_t e = cudaFuncSetAttribute(convt_k4s2_tc_kernel<G, RAW, NHWC, STAGED>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(convt_k4s2_tc_kernel<G, RAW, NHWC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
     if (e != cudaSuccess) return launch_status(e);
     const long long tiles = ((long long)N * (H + 1) * (W + 1) + MT - 1) / MT;
     int per_phase = sms / 4 > 0 ? sms / 4 : 1;
     if (per_phase > tiles) per_phase = (int)tiles;
-    convt_k4s2_tc_kernel<G, RAW, NHWC, STAGED><<<4 * per_phase, Roles<STAGED>::NTHREADS, smem, st>>>(
-        x, wtc, cb, bias, scale, out, N, H, W, Ho, Wo, nslab, L, xs, xs_plane);
+    convt_k4s2_tc_kernel<G, RAW, NHWC><<<4 * per_phase, NTHREADS, smem, st>>>(x, wtc, cb, bias, scale, out, N, H, W, Ho, Wo,
+                                                                   nslab, L);
     note_launch();
     return launch_status(cudaGetLastError());
-}
-
-// Workspace of the staged kernel: the weight rewrite (rounded up to 256 bytes), then
-// the staged copy of x.
-size_t wtc_bytes_aligned(int Cin) { return ((size_t)16 * Cin * COUT * 4 + 255) & ~(size_t)255; }
-
-// FUSEDWIN_CONVT_GATHER=1 in the environment keeps the gathering kernel even when the
-// workspace would hold the staged copy (used to cross-check the two kernels).
-bool force_gather() {
-    static const bool v = [] {
-        const char *e = getenv("FUSEDWIN_CONVT_GATHER");
-        return e && e[0] == '1';
-    }();
-    return v;
 }
 
 }  // namespace
@@ -694,22 +614,14 @@ bool convt_tc_eligible(int Cin, int Cout, int k, int s, int p) {
     return k == 4 && s == 2 && p == 1 && Cout == COUT && (Cin == 8 || Cin == 16 || Cin == 32 || Cin == 64);
 }
 
-// Workspace bytes with which the fused NCHW call takes the staged kernel.
-size_t convt_tc_staged_bytes(int N, int Cin, int H, int W) {
-    return wtc_bytes_aligned(Cin) + (size_t)(Cin / 4) * (size_t)xs_plane_positions(N, H, W) * 16;
-}
-
 namespace {
 
 // prepack = false: the workspace already holds this call's weight rewrite (an earlier
 // launch on the same stream wrote it), so only the main kernel runs.
-// ws_bytes >= convt_tc_staged_bytes(N, Cin, H, W) (fused NCHW operator only): x is
-// first rewritten into the workspace by convt_stage_x_kernel and the staged kernel
-// moves its slabs with the bulk-copy engine; otherwise the producers gather them.
 template <bool RAW, bool NHWC = false>
 fw_status tc_launch(const float *x, int N, int Cin, int H, int W, const float *w, const float *cb,
                     const float *bias, float scale, float *out, int Ho, int Wo, void *ws, cudaStream_t st,
-                    bool prepack = true, size_t ws_bytes = 0) {
+                    bool prepack = true) {
     float *wtc = static_cast<float *>(ws);
     if (prepack) {
         const long long total = 16LL * Cin * COUT;
@@ -717,23 +629,6 @@ fw_status tc_launch(const float *x, int N, int Cin, int H, int W, const float *w
         note_launch();
         const fw_status rc = launch_status(cudaGetLastError());
         if (rc != FW_OK) return rc;
-    }
-    if (!RAW && !NHWC && ws_bytes >= convt_tc_staged_bytes(N, Cin, H, W) && !force_gather()) {
-        const long long xs_plane = xs_plane_positions(N, H, W);
-        float4 *xs = reinterpret_cast<float4 *>(static_cast<unsigned char *>(ws) + wtc_bytes_aligned(Cin));
-        const long long total = (long long)(Cin / 4) * xs_plane;
-        convt_stage_x_kernel<<<(unsigned)min(152LL * 8, (total + 255) / 256), 256, 0, st>>>(x, xs, N, Cin, H, W,
-                                                                                           xs_plane);
-        note_launch();
-        const fw_status rc = launch_status(cudaGetLastError());
-        if (rc != FW_OK) return rc;
-        switch (Cin) {
-            case 8: return launch_g<2, false, false, true>(x, N, H, W, wtc, cb, bias, scale, out, Ho, Wo, st, xs, xs_plane);
-            case 16: return launch_g<4, false, false, true>(x, N, H, W, wtc, cb, bias, scale, out, Ho, Wo, st, xs, xs_plane);
-            case 32: return launch_g<8, false, false, true>(x, N, H, W, wtc, cb, bias, scale, out, Ho, Wo, st, xs, xs_plane);
-            case 64: return launch_g<16, false, false, true>(x, N, H, W, wtc, cb, bias, scale, out, Ho, Wo, st, xs, xs_plane);
-        }
-        return FW_ERR_UNSUPPORTED;
     }
     switch (Cin) {
         case 8: return launch_g<2, RAW, NHWC>(x, N, H, W, wtc, cb, bias, scale, out, Ho, Wo, st);
@@ -755,6 +650,10 @@ __global__ void __launch_bounds__(256) softmax_bias_scale_sigmoid_kernel(const f
          idx += (long long)gridDim.x * blockDim.x) {
         const long long n = idx / plane, hw = idx - n * plane;
         const float *yb = y + n * C * plane + hw;
+        // checked build: the pixel's C values lie between its first and last
+        if (!(CHK(yb, 4, y, 4 * npix * C) && CHK(yb + (C - 1) * plane, 4, y, 4 * npix * C) &&
+              CHK(out + n * C * plane + hw + (C - 1) * plane, 4, out, 4 * npix * C)))
+            continue;
         float mx = -INFINITY, sum = 0.f;
         for (int c = 0; c < C; ++c) {
             const float z = __ldg(yb + c * plane) * LOG2E;
@@ -777,9 +676,9 @@ __global__ void __launch_bounds__(256) softmax_bias_scale_sigmoid_kernel(const f
 }  // namespace
 
 fw_status convt_tc_launch(const float *x, int N, int Cin, int H, int W, const float *w, const float *cb,
-                          const float *bias, float scale, float *out, int Ho, int Wo, void *ws, size_t ws_bytes,
-                          cudaStream_t st, bool prepack) {
-    return tc_launch<false>(x, N, Cin, H, W, w, cb, bias, scale, out, Ho, Wo, ws, st, prepack, ws_bytes);
+                          const float *bias, float scale, float *out, int Ho, int Wo, void *ws, cudaStream_t st,
+                          bool prepack) {
+    return tc_launch<false>(x, N, Cin, H, W, w, cb, bias, scale, out, Ho, Wo, ws, st, prepack);
 }
 
 // Channels-last: x [N, H, W, Cin], out [N, Ho, Wo, 128] (out 32-byte aligned).

@@ -15,6 +15,8 @@ fw_status maxpool2d_ex_launch(const float *x, long long NC, int H, int W, int k,
 unsigned maxpool_read_and_clear_error();
 unsigned convt_tc_read_and_clear_error();
 unsigned convpool_tc_read_and_clear_error();
+unsigned convt_read_and_clear_error();
+unsigned convpool_read_and_clear_error();
 fw_status convpool_launch(const float *x, int N, int Cin, int H, int W, const float *w, const float *cb,
                           int Cout, int KH, int KW, float scale, const float *bias, int pk, int ps,
                           float *out, int Ho, int Wo, int mode, cudaStream_t st);
@@ -22,7 +24,6 @@ fw_status convt_launch(const float *x, int N, int Cin, int H, int W, const float
                        int Cout, int k, int s, int p, int op, const float *bias, float scale, float *out,
                        int Ho, int Wo, void *ws, size_t ws_bytes, bool ffma, bool weights_ready, cudaStream_t st);
 size_t convt_workspace_bytes(int Cin, int Cout, int k, int s, int p);
-size_t convt_tc_staged_bytes(int N, int Cin, int H, int W);
 bool convpool_tc_eligible(int Cin, int Cout, int KH, int KW, int pk, int ps);
 fw_status convpool_tc_launch_raw(const float *x, int N, int H, int W, const float *w, const float *cb, int Cout,
                                  int pk, float *y, int Ho, int Wo, cudaStream_t st);
@@ -201,13 +202,6 @@ unsigned long long fw_convt_workspace_size(int Cin, int Cout, int k, int s, int 
     return (unsigned long long)convt_workspace_bytes(Cin, Cout, k, s, p);
 }
 
-unsigned long long fw_convt_workspace_size_ex(int N, int Cin, int H, int W, int Cout, int k, int s, int p, int op) {
-    int Ho = 0, Wo = 0;
-    if (N < 1 || Cin < 1 || Cout < 1 || convt_shape(H, W, k, s, p, op, &Ho, &Wo) != FW_OK) return 0;
-    if (convt_tc_eligible(Cin, Cout, k, s, p)) return (unsigned long long)convt_tc_staged_bytes(N, Cin, H, W);
-    return (unsigned long long)convt_workspace_bytes(Cin, Cout, k, s, p);
-}
-
 static fw_status conv_pool_call(const float *x, int N, int Cin, int H, int W, const float *w, const float *conv_b,
                                 int Cout, int KH, int KW, float scale, const float *bias, int pool_k, int pool_s,
                                 float *out, int mode, void *stream) {
@@ -310,21 +304,14 @@ fw_status fw::convt_call(const float *x, int N, int Cin, int H, int W, const flo
         if (!workspace || workspace_bytes < need) return FW_ERR_NULL;
         if ((reinterpret_cast<uintptr_t>(workspace) & 15u) != 0) return FW_ERR_ALIGN;
     }
-    // The part of the workspace the call writes: the weight rewrite, and with room
-    // for it the staged copy of x (fw_convt_workspace_size_ex).
-    unsigned long long used = need;
-    if (need && !ffma && convt_tc_eligible(Cin, Cout, k, s, p)) {
-        const unsigned long long staged = convt_tc_staged_bytes(N, Cin, H, W);
-        if (workspace_bytes >= staged) used = staged;
-    }
     const long long ob = no * 4;
     if (overlaps(out, ob, x, nx * 4) || overlaps(out, ob, w, nw * 4) || overlaps(out, ob, bias, 4LL * Cout) ||
-        overlaps(out, ob, conv_b, 4LL * Cout) || (used && overlaps(out, ob, workspace, (long long)used)))
+        overlaps(out, ob, conv_b, 4LL * Cout) || (need && overlaps(out, ob, workspace, (long long)need)))
         return FW_ERR_ALIAS;
-    // The workspace is written before the main kernel reads any input.
-    if (used && (overlaps(workspace, (long long)used, x, nx * 4) || overlaps(workspace, (long long)used, w, nw * 4) ||
-                 overlaps(workspace, (long long)used, bias, 4LL * Cout) ||
-                 overlaps(workspace, (long long)used, conv_b, 4LL * Cout)))
+    // The weight rewrite into the workspace runs before the main kernel reads any input.
+    if (need && (overlaps(workspace, (long long)need, x, nx * 4) || overlaps(workspace, (long long)need, w, nw * 4) ||
+                 overlaps(workspace, (long long)need, bias, 4LL * Cout) ||
+                 overlaps(workspace, (long long)need, conv_b, 4LL * Cout)))
         return FW_ERR_ALIAS;
     return convt_launch(x, N, Cin, H, W, w, conv_b, Cout, k, s, p, op, bias, scale, out, Ho, Wo, workspace,
                         (size_t)workspace_bytes, ffma, weights_ready, static_cast<cudaStream_t>(stream));
@@ -481,7 +468,8 @@ fw_status fw_selftest_bounded_wait(unsigned int limit_us, void *stream) {
 fw_status fw_check_device_errors(void *stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FW_ERR_LAUNCH;
     const unsigned e = maxpool_read_and_clear_error() | convt_tc_read_and_clear_error() |
-                         convpool_tc_read_and_clear_error() | api_read_and_clear_error();
+                         convpool_tc_read_and_clear_error() | convt_read_and_clear_error() |
+                         convpool_read_and_clear_error() | api_read_and_clear_error();
     if (e & DEVERR_TIMEOUT) return FW_ERR_TIMEOUT;
     if (e) return FW_ERR_INTERNAL;
     return FW_OK;

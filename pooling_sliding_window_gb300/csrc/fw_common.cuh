@@ -30,7 +30,51 @@ fw_status convt_call(const float *x, int N, int Cin, int H, int W, const float *
                      int k, int s, int p, int op, const float *bias, float scale, float *out, void *workspace,
                      unsigned long long workspace_bytes, bool ffma, bool weights_ready, void *stream);
 
+// ---------------------------------------------------------- checked build --
+// Built with -DFW_CHECKED=1 (build.py, checked=True), every kernel tests the
+// address range of each memory access -- or of each run of accesses made from one
+// computed address -- against the buffer it belongs to before making it.  An access
+// outside its buffer is skipped and DEVERR_INTERNAL is recorded in the translation
+// unit's error word, which fw_check_device_errors reports as FW_ERR_INTERNAL; no
+// kernel traps.  In the default build every check is the constant `true`.
+#ifndef FW_CHECKED
+#define FW_CHECKED 0
+#endif
+
 // ---------------------------------------------------------------- device --
+
+// [p, p + bytes) inside [base, base + base_bytes)?  Checked build only; else true.
+__device__ __forceinline__ bool chk(unsigned *err, const void *p, long long bytes, const void *base,
+                                    long long base_bytes) {
+    if (!FW_CHECKED) return true;
+    const unsigned long long a = reinterpret_cast<uintptr_t>(p), b = reinterpret_cast<uintptr_t>(base);
+    const bool ok = base != nullptr && bytes >= 0 && a >= b && a + (unsigned long long)bytes <= b + (unsigned long long)base_bytes;
+    if (!ok) atomicOr(err, 2u);  // DEVERR_INTERNAL
+    return ok;
+}
+
+#if FW_CHECKED
+// The block's dynamic shared memory (every kernel's extern __shared__ array starts here).
+extern __shared__ __align__(1024) unsigned char fw_dyn_smem[];
+#endif
+
+// Shared-memory address range [addr, addr + bytes) inside the dynamic shared memory?
+__device__ __forceinline__ bool chk_smem(unsigned *err, uint32_t addr, uint32_t bytes) {
+#if FW_CHECKED
+    uint32_t size;
+    asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(size));
+    const uint32_t base = static_cast<uint32_t>(__cvta_generic_to_shared(fw_dyn_smem));
+    const bool ok = addr >= base && (unsigned long long)addr + bytes <= (unsigned long long)base + size;
+    if (!ok) atomicOr(err, 2u);
+    return ok;
+#else
+    (void)err, (void)addr, (void)bytes;
+    return true;
+#endif
+}
+__device__ __forceinline__ bool chk_smem(unsigned *err, const void *p, uint32_t bytes) {
+    return chk_smem(err, static_cast<uint32_t>(__cvta_generic_to_shared(p)), bytes);
+}
 
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
     unsigned long long t;

@@ -19,7 +19,6 @@ fw_status fw_conv2d_pool_out_shape(int H, int W, int KH, int KW, int pool_k, int
 fw_status fw_maxpool2d_out_shape(int H, int W, int k, int s, int p, int d, int *Ho, int *Wo);
 fw_status fw_convt_out_shape(int H, int W, int k, int s, int p, int op, int *Ho, int *Wo);
 unsigned long long fw_convt_workspace_size(int Cin, int Cout, int k, int s, int p);
-unsigned long long fw_convt_workspace_size_ex(int N, int Cin, int H, int W, int Cout, int k, int s, int p, int op);
 }
 
 namespace fw {
@@ -116,14 +115,6 @@ fw_status pipelined(cudaStream_t st, int N, size_t in_img_bytes, const void *x_h
 
 bool valid_sizes(int N, int a, int b) { return N >= 1 && a >= 1 && b >= 1; }
 
-// Conv-transpose workspace of one chunk's call: room for the weight rewrite and the
-// staged copy of the largest chunk's x (fw_convt_workspace_size_ex).
-unsigned long long chunk_convt_workspace(int N, int Cin, int H, int W, int Cout, int k, int s, int p, int op) {
-    const int nch = N < MAX_CHUNKS ? N : MAX_CHUNKS;
-    const int per = (N + nch - 1) / nch;
-    return fw_convt_workspace_size_ex(per, Cin, H, W, Cout, k, s, p, op);
-}
-
 }  // namespace
 }  // namespace fw
 
@@ -204,7 +195,7 @@ unsigned long long fw_convtranspose2d_softmax_bias_scale_sigmoid_host_workspace_
     if (!valid_sizes(N, Cin, Cout) || fw_convt_out_shape(H, W, k, s, p, op, &Ho, &Wo) != FW_OK) return 0;
     const unsigned long long f = 4;
     return up(f * N * Cin * H * W) + up(f * Cin * Cout * k * k) + 2 * up(f * Cout) + up(f * N * Cout * Ho * Wo) +
-           up(chunk_convt_workspace(N, Cin, H, W, Cout, k, s, p, op));
+           up(fw_convt_workspace_size(Cin, Cout, k, s, p));
 }
 
 fw_status fw_convtranspose2d_softmax_bias_scale_sigmoid_host(const float *x, int N, int Cin, int H, int W,
@@ -229,7 +220,7 @@ fw_status fw_convtranspose2d_softmax_bias_scale_sigmoid_host(const float *x, int
     float *bd = reinterpret_cast<float *>(ws + up(xb) + up(wb) + up(cbb));
     float *od = reinterpret_cast<float *>(ws + up(xb) + up(wb) + 2 * up(cbb));
     char *tws = ws + up(xb) + up(wb) + 2 * up(cbb) + up(ob);
-    const unsigned long long tws_bytes = chunk_convt_workspace(N, Cin, H, W, Cout, k, s, p, op);
+    const unsigned long long tws_bytes = fw_convt_workspace_size(Cin, Cout, k, s, p);
     const void *src[] = {w, conv_b, bias};
     void *dst[] = {wd, cbd, bd};
     const size_t bytes[] = {wb, conv_b ? cbb : 0, cbb};

@@ -38,8 +38,7 @@ EXPORTS = ("fw_status_string", "fw_version", "fw_conv2d_pool_out_shape", "fw_max
            "fw_convtranspose2d_softmax_bias_scale_sigmoid_host",
            "fw_convtranspose2d_softmax_bias_scale_sigmoid_host_workspace_size",
            "fw_convtranspose2d_softmax_bias_scale_sigmoid_nhwc", "fw_conv2d_tanh_scale_bias_maxpool_tf32",
-           "fw_conv2d_tanh_scale_bias_maxpool_ffma", "fw_convtranspose2d_softmax_bias_scale_sigmoid_ffma",
-           "fw_convt_workspace_size_ex")
+           "fw_conv2d_tanh_scale_bias_maxpool_ffma", "fw_convtranspose2d_softmax_bias_scale_sigmoid_ffma")
 
 
 class FusedWinError(RuntimeError):
@@ -49,15 +48,23 @@ class FusedWinError(RuntimeError):
         super().__init__(f"{where}: {msg}")
 
 
+def checked_build() -> bool:
+    """FUSEDWIN_CHECKED=1: load the bounds-checked library (build.py, checked=True)."""
+    return os.environ.get("FUSEDWIN_CHECKED") == "1"
+
+
 def library_path() -> str:
-    return _build.LIB
+    return _build.LIB_CHECKED if checked_build() else _build.LIB
 
 
 def lib():
     """Load libfusedwin.so (building it first if the sources are newer)."""
     global _lib
     if _lib is None:
-        path = _build.build() if os.environ.get("FUSEDWIN_NO_BUILD") is None else _build.LIB
+        if os.environ.get("FUSEDWIN_NO_BUILD") is None:
+            path = _build.build(checked=checked_build())
+        else:
+            path = library_path()
         L = C.CDLL(path)
         I, P, F, U64 = C.c_int, C.c_void_p, C.c_float, C.c_ulonglong
         IP = C.POINTER(C.c_int)
@@ -82,8 +89,6 @@ def lib():
             getattr(L, name).argtypes = [P, I, I, I, I, P, P, I, I, I, I, I, P, F, P, P, U64, P]
         L.fw_convt_workspace_size.restype = U64
         L.fw_convt_workspace_size.argtypes = [I, I, I, I, I]
-        L.fw_convt_workspace_size_ex.restype = U64
-        L.fw_convt_workspace_size_ex.argtypes = [I] * 9
         L.fw_check_device_errors.restype = I
         L.fw_check_device_errors.argtypes = [P]
         L.fw_selftest_bounded_wait.restype = I
@@ -150,10 +155,6 @@ def fw_convt_out_shape(H, W, k, s, p, op):
 
 def fw_convt_workspace_size(Cin, Cout, k, s, p) -> int:
     return int(lib().fw_convt_workspace_size(Cin, Cout, k, s, p))
-
-
-def fw_convt_workspace_size_ex(N, Cin, H, W, Cout, k, s, p, op) -> int:
-    return int(lib().fw_convt_workspace_size_ex(N, Cin, H, W, Cout, k, s, p, op))
 
 
 def fw_launch_count() -> int:
@@ -340,10 +341,7 @@ def _convt(fname, x, w, conv_b, bias, scale, stride, padding, output_padding, ou
     dev = _device_of(x)
     xd, wd = _dev(x, "x", dev), _dev(w, "w", dev)
     cbd, bd = _dev(conv_b, "conv_b", dev), _dev(bias.reshape(-1), "bias", dev)
-    if fname.endswith("_ffma"):
-        need = fw_convt_workspace_size(Cin, Cout, K, stride, padding)
-    else:  # room for the staged kernel too
-        need = fw_convt_workspace_size_ex(N, Cin, H, W, Cout, K, stride, padding, output_padding)
+    need = fw_convt_workspace_size(Cin, Cout, K, stride, padding)
     if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
         workspace = torch.empty((need + 3) // 4, device=dev, dtype=torch.float32)
     od = out if (out is not None and not host) else torch.empty((N, Cout, Ho, Wo), device=dev,

@@ -126,18 +126,6 @@ def test_operator_argument_errors_without_launch():
         x, 1, 64, 8, 8, w, cb, 128, 4, 2, 1, 1, bias, 2.0, o, ws, need, None)
     assert ctb(None, P(0x80000000 + 256)) == 4
     assert ctb(P(0x80000000 + need - 4), b) == 4
-    # workspace for the staged kernel: the weight rewrite (256-byte rounded) plus a
-    # TF32 copy of x in the kernel's stacked-position layout, 16 planes here
-    ex = FW.fw_convt_workspace_size_ex(1, 64, 8, 8, 128, 4, 2, 1, 1)
-    tiles = -(-(1 * 9 * 9) // 128)
-    plane = (8 + tiles * 128 + 2 * 9 + 1 + 7) // 8 * 8
-    assert ex == need + 16 * plane * 16
-    assert FW.fw_convt_workspace_size_ex(1, 64, 8, 8, 64, 4, 2, 1, 1) == FW.fw_convt_workspace_size(64, 64, 4, 2, 1)
-    assert FW.fw_convt_workspace_size_ex(1, 64, 8, 8, 128, 4, 2, 1, 2) == 0  # op >= s
-    # with room for the staged copy, the copy's range is checked for overlaps too
-    cts = lambda out: L.fw_convtranspose2d_softmax_bias_scale_sigmoid(
-        x, 1, 64, 8, 8, w, None, 128, 4, 2, 1, 1, b, 2.0, out, ws, ex, None)
-    assert cts(P(0x80000000 + need + 64)) == 4
     # the FP32-FMA conv-transpose entry takes the same arguments and checks
     ff = lambda **kw: L.fw_convtranspose2d_softmax_bias_scale_sigmoid_ffma(
         kw.get("x", x), 1, 64, 8, 8, w, None, 128, 4, 2, 1, kw.get("op", 1), b, kw.get("scale", 2.0),
