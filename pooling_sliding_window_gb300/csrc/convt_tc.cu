@@ -532,11 +532,10 @@ convt_k4s2_tc_kernel(const float *__restrict__ x, const float *__restrict__ wtc,
                 tc::ld32(taddr + 32 * c, v);
                 tc::wait_ld();
                 // checked build: the chunk's 32 channels lie between its first and last store
-                const bool in_range = !FW_CHECKED ||
-                                      (NHWC ? CHK(o + 32 * c, 128, out, out_bytes)
-                                            : CHK(o + 32 * c * plane_out, 4, out, out_bytes) &&
-                                                  CHK(o + (32 * c + 31) * plane_out, 4, out, out_bytes));
-                if (valid && in_range) {
+                // (tested only for pixels that store)
+                if (valid && (!FW_CHECKED || (NHWC ? CHK(o + 32 * c, 128, out, out_bytes)
+                                                   : CHK(o + 32 * c * plane_out, 4, out, out_bytes) &&
+                                                         CHK(o + (32 * c + 31) * plane_out, 4, out, out_bytes)))) {
                     if constexpr (NHWC) {
 #pragma unroll
                         for (int i = 0; i < 32; i += 4) {
