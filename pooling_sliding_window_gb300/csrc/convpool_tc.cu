@@ -44,8 +44,6 @@
 //               scale*tanh(m + conv_b) goes through shared memory so that the
 //               global stores are row-contiguous.
 // Scale < 0 takes the window minimum instead (the map is then decreasing).
-#include <cstdlib>
-
 #include "fw_common.cuh"
 
 namespace fw {
@@ -84,17 +82,11 @@ struct Bars {
     uint64_t slot_empty[MAX_SLOT];
     uint64_t stg_full[4];  // [group][buffer]
     uint64_t raw_full[2];  // raw mode: a conv row staged by all epilogue warps
-    uint64_t exit_bar;     // CTA pair: the other CTA is done with this CTA's shared memory
     uint32_t tmem_base;
     int abort;
 };
 
-// PAIR = true (3xTF32 fused operator): a cluster of two CTAs on two SMs runs the MMAs
-// as one CTA pair (tcgen05 .cta_group::2, M = 256): each CTA stages its own item (128
-// conv columns), the even CTA issues every MMA for both, the weights are split
-// between the two shared memories (each holds half of every MMA's N rows), and each
-// CTA's TMEM receives its own rows' accumulators, so the epilogue is unchanged.
-template <int P, int N, bool RAW, bool X3, bool PAIR = false>
+template <int P, int N, bool RAW, bool X3>
 struct Cfg {
     static constexpr int ROWS = P + 2;
     static constexpr int SPLIT = ROWS * RB;           // hi (or lo) half of a slab
@@ -107,11 +99,7 @@ struct Cfg {
     static constexpr bool STACK = !X3 && !RAW && N == SLOT_COLS;
     static constexpr int NSLOT = TMEM_COLS / SLOT_COLS;
     static_assert((X3 ? 2 : 1) * N <= SLOT_COLS && NSLOT <= MAX_SLOT, "slots");
-    // one tap of the weights: [w_hi | w_lo] (or w_hi) -- or, in a pair, this CTA's
-    // halves: block 1 (N rows: w_hi in the even CTA, w_lo in the odd one) for the
-    // N = 2*Cout MMA, then block 2 (N/2 rows of w_hi) for the N = Cout MMA
-    static_assert(!PAIR || (X3 && !RAW && N % 16 == 0), "pairs serve the fused 3xTF32 operator");
-    static constexpr int BTAP = PAIR ? (N / 8 + N / 16) * CORE : ((X3 ? 2 : 1) * N / 8) * CORE;
+    static constexpr int BTAP = ((X3 ? 2 : 1) * N / 8) * CORE;  // one tap of [w_hi | w_lo] (or w_hi)
     static constexpr int B_BYTES = 9 * BTAP;
     static constexpr int PW = MT / P;                 // pooled columns per item
     // floats of one staging buffer: a pooled row, or (raw mode) one conv row of the block
@@ -169,12 +157,12 @@ __device__ __forceinline__ float upd(float m, float v, bool use_min) {
 // comparison path -- `out` receives y = conv(x) + conv_b for the P*Ho x P*Wo conv
 // outputs the pool reads ([Nimg, N, P*Ho, P*Wo]); scale and bias are unused.
 // X3 selects the 3xTF32 split (true) or a single TF32 product (false).
-template <int P, int N, bool RAW, bool X3, bool PAIR = false>
-__global__ void __launch_bounds__(Cfg<P, N, RAW, X3, PAIR>::NTHREADS, 1)
+template <int P, int N, bool RAW, bool X3>
+__global__ void __launch_bounds__(Cfg<P, N, RAW, X3>::NTHREADS, 1)
 convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, const float *__restrict__ cb,
                    const float *__restrict__ bias, float scale, float *__restrict__ out, int Nimg, int H, int W,
                    int Ho, int Wo, int ncb, bool vec) {
-    using C = Cfg<P, N, RAW, X3, PAIR>;
+    using C = Cfg<P, N, RAW, X3>;
     constexpr int CIN = 8, NEPI = C::NEPI, NTHREADS = C::NTHREADS, NW = NTHREADS / 32;
     extern __shared__ __align__(1024) unsigned char smem[];
     unsigned char *sB = smem;
@@ -187,11 +175,6 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const long long n_items = (long long)Nimg * Ho * ncb;
     const bool use_min = scale < 0.f;
-    // Items of this CTA: blockIdx.x + k * gridDim.x.  A pair iterates the even CTA's
-    // count (the odd CTA's last item may not exist: it then computes and stores nothing).
-    const uint32_t rank = PAIR ? cluster_ctarank() : 0;
-    const long long first = PAIR ? (long long)(blockIdx.x & ~1u) : (long long)blockIdx.x;
-    const int n_iter = n_items > first ? (int)((n_items - first + gridDim.x - 1) / gridDim.x) : 0;
     // buffer extents for the checked build
     const long long x_bytes = 4LL * Nimg * CIN * H * W;
     const long long out_bytes = RAW ? 4LL * Nimg * N * (P * Ho) * (P * Wo) : 4LL * Nimg * N * Ho * Wo;
@@ -207,19 +190,6 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
         const int co = e % N, t = e / N, ci = t % CIN, tap = t / CIN;
         const float v = __ldg(w + ((long long)co * CIN + ci) * 9 + tap);
         const float hi = tc::to_tf32(v), lo = tc::to_tf32(v - hi);
-        if constexpr (PAIR) {
-            // block 1: row co of w_hi (even CTA) or w_lo (odd CTA); block 2: rows
-            // rank*N/2 .. of w_hi
-            const int base = tap * C::BTAP + (ci / 4) * 128 + (ci % 4) * 4;
-            float *d1 = reinterpret_cast<float *>(sB + base + (co / 8) * CORE + (co % 8) * 16);
-            if (CHKS(d1, 4)) *d1 = rank == 0 ? hi : lo;
-            const int r2 = co - (int)rank * (N / 2);
-            if (r2 >= 0 && r2 < N / 2) {
-                float *d2 = reinterpret_cast<float *>(sB + base + (N / 8) * CORE + (r2 / 8) * CORE + (r2 % 8) * 16);
-                if (CHKS(d2, 4)) *d2 = hi;
-            }
-            continue;
-        }
         if constexpr (C::STACK) {
             const int np = (2 - tap / 3) * N + co;
             float *d = reinterpret_cast<float *>(sB + (tap % 3) * 3 * C::BTAP + (np / 8) * CORE + (ci / 4) * 128 +
@@ -237,43 +207,24 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
     }
     if (tid == 0) {
         for (int s = 0; s < C::NST; ++s) {
-            mbar_init(smem_u32(&bars.slab_full[s]), (PAIR ? 2 : 1) * NPROD);  // a pair: both CTAs' producers
+            mbar_init(smem_u32(&bars.slab_full[s]), NPROD);
             mbar_init(smem_u32(&bars.slab_empty[s]), 1);
         }
         for (int b = 0; b < C::NSLOT; ++b) {
             mbar_init(smem_u32(&bars.slot_full[b]), 1);
-            mbar_init(smem_u32(&bars.slot_empty[b]), (PAIR ? 2 : 1) * 8);  // one group (per CTA) reads a row
+            mbar_init(smem_u32(&bars.slot_empty[b]), 8);  // one group reads a row
         }
-        mbar_init(smem_u32(&bars.exit_bar), 1);
         for (int b = 0; b < 2 * C::NGRP; ++b) mbar_init(smem_u32(&bars.stg_full[b]), 8);
         for (int b = 0; b < 2; ++b) mbar_init(smem_u32(&bars.raw_full[b]), NEPI);
         bars.abort = 0;
         fence_mbar_init();
     }
-    if (warp == MMA_WARP) {
-        if constexpr (PAIR)
-            tc::alloc_pair(smem_u32(&bars.tmem_base), TMEM_COLS);  // collective: one warp of each CTA
-        else
-            tc::alloc(smem_u32(&bars.tmem_base), TMEM_COLS);
-    }
+    if (warp == MMA_WARP) tc::alloc(smem_u32(&bars.tmem_base), TMEM_COLS);
     fence_proxy_async_smem();
     tc::fence_before_sync();
     __syncthreads();
-    // a pair: both CTAs' barriers are initialised (and the weights staged) before any
-    // arrival or commit crosses the pair
-    if constexpr (PAIR) cluster_sync_all();
     tc::fence_after_sync();
     const uint32_t tmem = bars.tmem_base;
-    // barrier waits and arrivals that cross the pair use cluster scope
-    auto wait = [&](uint64_t &bar, uint32_t parity) {
-        return PAIR ? mbar_wait_bounded_cluster(smem_u32(&bar), parity) : mbar_wait_bounded(smem_u32(&bar), parity);
-    };
-    auto arrive_leader = [&](uint64_t &bar) {  // on the even CTA's barrier (this CTA's without a pair)
-        if constexpr (PAIR)
-            mbar_arrive_cluster(mapa_shared(smem_u32(&bar), 0));
-        else
-            mbar_arrive(smem_u32(&bar));
-    };
     volatile int *abort_flag = &bars.abort;
     auto fail = [&]() {
         *abort_flag = 1;
@@ -342,8 +293,9 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
                 vt[ci] = load_tail(ts, tok, ci);
             }
         }
-        for (int k = 0; k < n_iter && !*abort_flag; ++k, cur.advance(Ho, ncb)) {
-            const long long item = blockIdx.x + (long long)k * gridDim.x;  // >= n_items: nothing to load
+        int k = 0;
+        for (long long item = blockIdx.x; item < n_items && !*abort_flag;
+             item += gridDim.x, ++k, cur.advance(Ho, ncb)) {
             const int stage = k % C::NST, use = k / C::NST;
             nxt.advance(Ho, ncb);
             const bool has_next = item + gridDim.x < n_items;
@@ -352,7 +304,7 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
             const float *nms = main_src(nxt, ncol, nok), *nts = tail_src(nxt, ntok);
             nok = nok && has_next;
             ntok = ntok && has_next;
-            if (use > 0 && !wait(bars.slab_empty[stage], (use - 1) & 1)) fail();
+            if (use > 0 && !mbar_wait_bounded(smem_u32(&bars.slab_empty[stage]), (use - 1) & 1)) fail();
             unsigned char *slab = sSlab + stage * C::SLAB;
             // hi/lo split of 4 channels of one position into the two halves of the slab
             auto put = [&](unsigned char *dst, float c0, float c1, float c2, float c3) {
@@ -391,33 +343,24 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
             }
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) arrive_leader(bars.slab_full[stage]);
-        }
-        if (PAIR && ptid == 0) {
-            // the even CTA's last commits to this CTA's slab barriers have landed before
-            // this CTA can leave (bounded)
-            for (int st = 0; st < C::NST; ++st) {
-                const int k_last = n_iter - 1 - ((n_iter - 1 - st) % C::NST + C::NST) % C::NST;
-                if (k_last >= 0 && k_last % C::NST == st) wait(bars.slab_empty[st], (k_last / C::NST) & 1);
-            }
+            if (lane == 0) mbar_arrive(smem_u32(&bars.slab_full[stage]));
         }
     } else if (warp == MMA_WARP) {
         // ------------------------------------------------------------ MMA issue
-        if (lane == 0 && rank == 0) {  // a pair: the even CTA issues for both
-            constexpr int MM = PAIR ? 256 : 128;
-            constexpr uint32_t IDESC_HH_HL = tc::idesc_tf32(MM, (X3 ? 2 : 1) * N);
-            constexpr uint32_t IDESC_LH = tc::idesc_tf32(MM, N);
+        if (lane == 0) {
+            constexpr uint32_t IDESC_HH_HL = tc::idesc_tf32(128, (X3 ? 2 : 1) * N);
+            constexpr uint32_t IDESC_LH = tc::idesc_tf32(128, N);
             const uint32_t sB_addr = smem_u32(sB), sSlab_addr = smem_u32(sSlab);
             // checked build: the shared-memory bytes an MMA reads -- A: 16 core groups
             // CORE apart plus the second K core 128 B on; B: n rows, 8 per CORE
             auto mma_ok = [&](uint32_t a_addr, uint32_t b_addr, int n) {
                 return CHKS(a_addr, 15 * CORE + 256) && CHKS(b_addr, (uint32_t)((n / 8 - 1) * CORE + 256));
             };
-            int rowc = 0;
+            int k = 0, rowc = 0;
             bool ok = true;
-            for (int k = 0; ok && k < n_iter && !*abort_flag; ++k) {
+            for (long long item = blockIdx.x; ok && item < n_items && !*abort_flag; item += gridDim.x, ++k) {
                 const int stage = k % C::NST, use = k / C::NST;
-                if (!wait(bars.slab_full[stage], use & 1)) {
+                if (!mbar_wait_bounded(smem_u32(&bars.slab_full[stage]), use & 1)) {
                     fail();
                     break;
                 }
@@ -469,7 +412,7 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
 #pragma unroll
                 for (int j = 0; j < P; ++j, ++rowc) {
                     const int slot = rowc % C::NSLOT, sus = rowc / C::NSLOT;
-                    if (sus > 0 && !wait(bars.slot_empty[slot], (sus - 1) & 1)) {
+                    if (sus > 0 && !mbar_wait_bounded(smem_u32(&bars.slot_empty[slot]), (sus - 1) & 1)) {
                         fail();
                         ok = false;
                         break;
@@ -483,31 +426,16 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
                         const uint64_t bd = b0 + (uint64_t)((tap * C::BTAP) >> 4);
                         const uint32_t ah_addr =
                             sSlab_addr + stage * C::SLAB + (j + tap / 3) * RB + (tap % 3) * CORE;
-                        if constexpr (PAIR) {
-                            // this CTA's B rows: block 1 (N of the 2N), block 2 (N/2 of the N)
-                            const uint64_t bd2 = bd + (uint64_t)(((N / 8) * CORE) >> 4);
-                            if (mma_ok(ah_addr, sB_addr + tap * C::BTAP, N))
-                                tc::mma_tf32_pair(d, ah, bd, IDESC_HH_HL, tap > 0 ? 1u : 0u);
-                            if (mma_ok(ah_addr + C::SPLIT, sB_addr + tap * C::BTAP + (N / 8) * CORE, N / 2))
-                                tc::mma_tf32_pair(d, al, bd2, IDESC_LH, 1u);
-                            continue;
-                        }
                         if (mma_ok(ah_addr, sB_addr + tap * C::BTAP, (X3 ? 2 : 1) * N))
                             tc::mma_tf32(d, ah, bd, IDESC_HH_HL, tap > 0 ? 1u : 0u);
                         if constexpr (X3)
                             if (mma_ok(ah_addr + C::SPLIT, sB_addr + tap * C::BTAP, N))
                                 tc::mma_tf32(d, al, bd, IDESC_LH, 1u);
                     }
-                    if constexpr (PAIR)
-                        tc::commit_pair(smem_u32(&bars.slot_full[slot]));
-                    else
-                        tc::commit(smem_u32(&bars.slot_full[slot]));
+                    tc::commit(smem_u32(&bars.slot_full[slot]));
                 }
                 }
-                if constexpr (PAIR)
-                    tc::commit_pair(smem_u32(&bars.slab_empty[stage]));
-                else
-                    tc::commit(smem_u32(&bars.slab_empty[stage]));
+                tc::commit(smem_u32(&bars.slab_empty[stage]));
             }
         }
         __syncwarp();
@@ -525,10 +453,9 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
         bool ok = true;
         // this group's items: the CTA's item sequence numbers k = grp, grp + NG, ...
         ItemCursor cur(blockIdx.x + (long long)grp * gridDim.x, (long long)NG * gridDim.x, Ho, ncb);
-        int kk = 0;
-        for (int k = grp; ok && k < n_iter && !*abort_flag; k += NG, ++kk, cur.advance(Ho, ncb)) {
-            // a pair's odd CTA may run one iteration past its items: it then stores nothing
-            const bool real = blockIdx.x + (long long)k * gridDim.x < n_items;
+        int k = grp, kk = 0;
+        for (long long item = blockIdx.x + (long long)grp * gridDim.x; ok && item < n_items && !*abort_flag;
+             item += (long long)NG * gridDim.x, k += NG, ++kk, cur.advance(Ho, ncb)) {
             float m[NH];
 #pragma unroll
             for (int c = 0; c < NH; ++c) m[c] = use_min ? INFINITY : -INFINITY;
@@ -536,7 +463,7 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
             for (int j = 0; j < P; ++j) {
                 const int rowc = k * P + j;  // conv rows in MMA order
                 const int slot = rowc % C::NSLOT, sus = rowc / C::NSLOT;
-                if (!wait(bars.slot_full[slot], sus & 1)) {
+                if (!mbar_wait_bounded(smem_u32(&bars.slot_full[slot]), sus & 1)) {
                     fail();
                     ok = false;
                     break;
@@ -556,7 +483,7 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
                     if (c0 + C::LDC == NH) {
                         tc::fence_before_sync();
                         __syncwarp();
-                        if (lane == 0) arrive_leader(bars.slot_empty[slot]);
+                        if (lane == 0) mbar_arrive(smem_u32(&bars.slot_empty[slot]));
                     }
                     if constexpr (RAW) {
                     // Stage the row as [channel][position]; conv column i + 16r sits at
@@ -653,7 +580,7 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
             constexpr int CSTEP = 8 * 32 / C::PW;
             const int et = gw * 32 + lane, pw = et % C::PW, co0 = et / C::PW;
             const int pw0 = cur.cblk * C::PW;
-            if (real && pw0 + pw < Wo) {
+            if (pw0 + pw < Wo) {
                 const long long cstride = (long long)Ho * Wo;
                 float *op = out + ((cur.n * N + co0) * Ho + cur.pr) * (long long)Wo + pw0 + pw;
                 static_assert(N % CSTEP == 0, "store passes");
@@ -669,30 +596,18 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
 
     tc::fence_before_sync();
     __syncthreads();
-    if constexpr (PAIR) {
-        // Neither CTA of the pair leaves while the other may still arrive on its
-        // barriers: each tells the other it is done, then waits for the other (bounded).
-        if (tid == 0) {
-            mbar_arrive_cluster(mapa_shared(smem_u32(&bars.exit_bar), rank ^ 1u));
-            if (!mbar_wait_bounded_cluster(smem_u32(&bars.exit_bar), 0)) atomicOr(&g_err_convpool_tc, DEVERR_TIMEOUT);
-        }
-        __syncthreads();
-    }
     if (warp == MMA_WARP) {
         tc::fence_after_sync();
-        if constexpr (PAIR)
-            tc::dealloc_pair(tmem, TMEM_COLS);
-        else
-            tc::dealloc(tmem, TMEM_COLS);
+        tc::dealloc(tmem, TMEM_COLS);
     }
 }
 
-template <int P, int N, bool RAW, bool X3, bool PAIR = false>
+template <int P, int N, bool RAW, bool X3>
 fw_status launch_pn(const float *x, int Nimg, int H, int W, const float *w, const float *cb, const float *bias,
                     float scale, float *out, int Ho, int Wo, cudaStream_t st) {
-    using C = Cfg<P, N, RAW, X3, PAIR>;
+    using C = Cfg<P, N, RAW, X3>;
     size_t smem = C::SMEM < 116 * 1024 ? 116 * 1024 : C::SMEM;  // one CTA per SM
-    cudaError_t e = cudaFuncSetAttribute(convpool_tc_kernel<P, N, RAW, X3, PAIR>,
+    cudaError_t e = cudaFuncSetAttribute(convpool_tc_kernel<P, N, RAW, X3>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return launch_status(e);
     int dev = 0, sms = 0;
@@ -701,29 +616,8 @@ fw_status launch_pn(const float *x, int Nimg, int H, int W, const float *w, cons
         return FW_ERR_LAUNCH;
     const int ncb = (Wo * P + MT - 1) / MT;
     const long long items = (long long)Nimg * Ho * ncb;
-    int grid = (int)(items < sms ? items : sms);
+    const int grid = (int)(items < sms ? items : sms);
     const bool vec = W % 4 == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0;  // float4 input rows
-    if constexpr (PAIR) {
-        // clusters of two CTAs (one CTA pair on two SMs each); an even grid
-        grid = grid & ~1;
-        if (grid < 2) return FW_ERR_UNSUPPORTED;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)grid);
-        cfg.blockDim = dim3(C::NTHREADS);
-        cfg.dynamicSmemBytes = smem;
-        cfg.stream = st;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, convpool_tc_kernel<P, N, RAW, X3, PAIR>, x, w, cb, bias, scale, out, Nimg, H, W,
-                               Ho, Wo, ncb, vec);
-        note_launch();
-        return launch_status(e == cudaSuccess ? cudaGetLastError() : e);
-    }
     convpool_tc_kernel<P, N, RAW, X3><<<grid, C::NTHREADS, smem, st>>>(x, w, cb, bias, scale, out, Nimg, H, W, Ho, Wo,
                                                                     ncb, vec);
     note_launch();
@@ -737,37 +631,13 @@ bool convpool_tc_eligible(int Cin, int Cout, int KH, int KW, int pk, int ps) {
            (Cout == 16 || Cout == 32 || Cout == 48 || Cout == 64);
 }
 
-namespace {
-// FUSEDWIN_CONVPOOL_SINGLE=1 in the environment keeps the 3xTF32 operator on the
-// single-CTA kernel instead of CTA pairs (used to cross-check the two).
-bool force_single() {
-    static const bool v = [] {
-        const char *e = getenv("FUSEDWIN_CONVPOOL_SINGLE");
-        return e && e[0] == '1';
-    }();
-    return v;
-}
-
-// The 3xTF32 operator: CTA pairs when there are at least two items, else one CTA.
-template <int P, int N>
-fw_status launch_x3(const float *x, int Nimg, int H, int W, const float *w, const float *cb, const float *bias,
-                    float scale, float *out, int Ho, int Wo, cudaStream_t st) {
-    const long long items = (long long)Nimg * Ho * ((Wo * P + MT - 1) / MT);
-    if (items >= 2 && !force_single()) {
-        const fw_status rc = launch_pn<P, N, false, true, true>(x, Nimg, H, W, w, cb, bias, scale, out, Ho, Wo, st);
-        if (rc != FW_ERR_UNSUPPORTED) return rc;
-    }
-    return launch_pn<P, N, false, true>(x, Nimg, H, W, w, cb, bias, scale, out, Ho, Wo, st);
-}
-}  // namespace
-
 // x3 = true: 3xTF32 split (float32-level accuracy); false: one TF32 product per K step.
 fw_status convpool_tc_launch(const float *x, int N, int H, int W, const float *w, const float *cb, int Cout,
                              float scale, const float *bias, int pk, float *out, int Ho, int Wo, bool x3,
                              cudaStream_t st) {
 #define FW_CP_CASE(PP, NN)                                                                                      \
     if (pk == PP && Cout == NN)                                                                                 \
-        return x3 ? launch_x3<PP, NN>(x, N, H, W, w, cb, bias, scale, out, Ho, Wo, st)                          \
+        return x3 ? launch_pn<PP, NN, false, true>(x, N, H, W, w, cb, bias, scale, out, Ho, Wo, st)             \
                   : launch_pn<PP, NN, false, false>(x, N, H, W, w, cb, bias, scale, out, Ho, Wo, st);
     FW_CP_CASE(4, 64) FW_CP_CASE(4, 48) FW_CP_CASE(4, 32) FW_CP_CASE(4, 16)
     FW_CP_CASE(2, 64) FW_CP_CASE(2, 48) FW_CP_CASE(2, 32) FW_CP_CASE(2, 16)
