@@ -524,7 +524,7 @@ def run_gpu(args):
                 CT["scale"], out=h_ct, workspace=hws_ct)
         specs.append(dict(name="convt", work=ct_flops(N=n), unit="TFLOP/s", scale=1e12, bound="tensor",
                           run=lambda: op_ct(d, out_ct), e2e=lambda: host_ct(), out=h_ct,
-                          kernel="convt_k4s2_tc_kernel<16> (tcgen05 kind::tf32) + weight prepack",
+                          kernel="convt_k4s2_pair_kernel<16> (CTA pairs, tcgen05.mma.cta_group::2 kind::tf32, both column phases per pair) + weight prepack",
                           source="convt_tc.cu"))
 
     def barrier():

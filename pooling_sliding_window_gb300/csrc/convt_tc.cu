@@ -576,6 +576,416 @@ convt_k4s2_tc_kernel(const float *__restrict__ x, const float *__restrict__ wtc,
     }
 }
 
+// ------------------------------------------------------------------ CTA pairs --
+// The fused NCHW operator on CTA pairs.  A cluster of two CTAs on two SMs issues the
+// phase GEMMs as 2-SM MMAs (tcgen05 .cta_group::2, M = 256 anchors: rows 0-127 from
+// the even CTA's slab, 128-255 from the odd CTA's at the same offset), with the N rows
+// of the weights split between the two shared memories (channels 0-63 in the even CTA,
+// 64-127 in the odd one).  Holding half of every phase's weights leaves room for both
+// column phases px = 0, 1 of one row phase py: one slab, covering the horizontal
+// offsets -1, 0, +1, feeds both, and each CTA's TMEM receives all 128 channels of both
+// phases for its own 128 anchors.  An epilogue thread thus owns output columns 2*nn and
+// 2*nn + 1 of one output row; a warp interleaves them with shuffles and each store
+// instruction writes 32 consecutive floats (whole sectors), where the one-phase kernel
+// above fills every other float of each sector.
+namespace pr {
+constexpr int PROD_WARPS = 7;                       // warps 0-6: gather
+constexpr int EPI_WARP0 = PROD_WARPS;               // warps 7-14: two groups of 4 (TMEM buffers 0, 1)
+constexpr int NBUF = 2;                             // accumulators of 256 columns: [px 0 | px 1]
+constexpr int MMA_WARP = EPI_WARP0 + 4 * NBUF;      // warp 15: TMEM, weights, MMA issue (even CTA)
+constexpr int NTHREADS = (MMA_WARP + 1) * 32;
+constexpr int HALF = COUT / 2;                      // weight rows (channels) per CTA
+constexpr int BPLANE = HALF * 16;                   // one K plane (4 input channels) of those rows
+constexpr uint32_t IDESC = tc::idesc_tf32(2 * MT, COUT);
+constexpr int DX0 = -1;                             // smallest horizontal tap offset of either column phase
+
+struct Bars {
+    uint64_t b_full;
+    uint64_t slab_full[NSTAGE];   // even CTA: the producer warps of both CTAs arrive
+    uint64_t slab_empty[NSTAGE];  // both CTAs: one multicast commit
+    uint64_t acc_full[NBUF];      // both CTAs: one multicast commit
+    uint64_t acc_empty[NBUF];     // even CTA: the group's epilogue warps of both CTAs arrive
+    uint64_t exit_bar;            // the other CTA of the pair has finished
+    uint32_t tmem_base;
+    int abort;
+};
+
+// Shared memory of one CTA: half the weights of both column phases, NSTAGE slabs of
+// G planes x L positions x 16 B, two per-channel constant vectors, barriers.
+__host__ __device__ inline size_t smem_bytes(int G, int L) {
+    return (size_t)2 * 4 * G * BPLANE + (size_t)NSTAGE * G * L * 16 + 2 * COUT * 4 + sizeof(Bars);
+}
+}  // namespace pr
+
+// Slab positions: pbase + [0, L) with pbase = tile anchor + (W+1) + dy_lo*(W+1) - 1;
+// nslab == 1 -> both vertical taps, L = W + 131; nslab == 2 -> one vertical tap per
+// slab, L = 130.  Pair tile T covers anchors 256*T .. 256*T + 255, CTA rank r the 128
+// from 256*T + 128*r.
+template <int G>
+__global__ void __launch_bounds__(pr::NTHREADS, 1)
+convt_k4s2_pair_kernel(const float *__restrict__ x, const float *__restrict__ wtc, const float *__restrict__ cb,
+                       const float *__restrict__ bias, float scale, float *__restrict__ out, int N, int H, int W,
+                       int Ho, int Wo, int nslab, int L) {
+    constexpr int CIN = 4 * G;
+    constexpr int B_BYTES = 2 * 4 * G * pr::BPLANE;  // px x taps x planes
+    extern __shared__ __align__(1024) unsigned char smem[];
+    const int slab_plane = L * 16;
+    const int slab_bytes = G * slab_plane;
+    unsigned char *sB = smem;
+    unsigned char *sSlab = smem + B_BYTES;
+    float *sCb = reinterpret_cast<float *>(sSlab + NSTAGE * slab_bytes);  // conv_b * log2(e)
+    float *sKb = sCb + COUT;                                              // -bias * scale * log2(e)
+    pr::Bars &bars = *reinterpret_cast<pr::Bars *>(sKb + COUT);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t rank = cluster_ctarank();
+    const int cid = blockIdx.x >> 1;  // the pair
+    const int py = cid & 1, pair = cid >> 1, npair = gridDim.x >> 2;
+    const int BW = W + 1, BH = H + 1;
+    const long long n_anchor = (long long)N * BH * BW;
+    const long long n_pos = ((long long)N * BH + 1) * BW;
+    const int n_ptiles = (int)((n_anchor + 2 * MT - 1) / (2 * MT));
+    const int n_iter = pair < n_ptiles ? (n_ptiles - pair + npair - 1) / npair : 0;
+    const int dy0 = py == 0 ? -1 : 0;  // smaller vertical tap offset of the row phase
+    const long long x_bytes = 4LL * N * CIN * H * W, out_bytes = 4LL * N * COUT * Ho * Wo;
+    const long long wtc_bytes = 16LL * CIN * COUT * 4;
+
+    for (int i = tid; i < COUT; i += pr::NTHREADS) {
+        sCb[i] = cb ? __ldg(cb + i) * LOG2E : 0.f;
+        sKb[i] = bias ? -__ldg(bias + i) * scale * LOG2E : 0.f;
+    }
+    if (tid == 0) {
+        mbar_init(smem_u32(&bars.b_full), 1);
+        for (int s = 0; s < NSTAGE; ++s) {
+            mbar_init(smem_u32(&bars.slab_full[s]), 2 * pr::PROD_WARPS);
+            mbar_init(smem_u32(&bars.slab_empty[s]), 1);
+        }
+        for (int b = 0; b < pr::NBUF; ++b) {
+            mbar_init(smem_u32(&bars.acc_full[b]), 1);
+            mbar_init(smem_u32(&bars.acc_empty[b]), 2 * 4);
+        }
+        mbar_init(smem_u32(&bars.exit_bar), 1);
+        bars.abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == pr::MMA_WARP) tc::alloc_pair(smem_u32(&bars.tmem_base), 512);  // one warp of each CTA
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    volatile int *abort_flag = &bars.abort;
+    auto fail = [&]() {
+        *abort_flag = 1;
+        atomicOr(&g_err_convt_tc, DEVERR_TIMEOUT);
+    };
+    if (warp == pr::MMA_WARP && lane == 0) {
+        // this CTA's rows of both column phases: wtc[py*2 + px][tap][g][64*rank .. +63][c4],
+        // one 1 KB run per (px, tap, g)
+        const uint32_t bfull = smem_u32(&bars.b_full);
+        const unsigned char *w8 = reinterpret_cast<const unsigned char *>(wtc) + (size_t)(2 * py) * 4 * G * (COUT * 16);
+        // checked build: the runs lie inside the row phase's two weight blocks
+        if (CHKS(sB, B_BYTES) && CHK(w8, 2 * 4 * G * (COUT * 16), wtc, wtc_bytes)) {
+            mbar_arrive_expect_tx(bfull, B_BYTES);
+            for (int r = 0; r < 2 * 4 * G; ++r)  // r = (px*4 + tap)*G + g
+                bulk_g2s(smem_u32(sB + r * pr::BPLANE), w8 + (size_t)r * (COUT * 16) + rank * pr::BPLANE, pr::BPLANE,
+                         bfull);
+        } else {
+            mbar_arrive(bfull);  // checked build: no copy, the weights stay unset
+        }
+        if (!mbar_wait_bounded(bfull, 0)) fail();
+    }
+    __syncthreads();
+    // both CTAs' barriers are initialised and weights staged before anything crosses the pair
+    cluster_sync_all();
+    tc::fence_after_sync();
+    const uint32_t tmem = bars.tmem_base;
+    // Barriers crossing the pair use CTA-scope semantics: what an arrival publishes is
+    // the arriving CTA's own slab (fenced to the async proxy) or TMEM, read by the pair's
+    // MMAs; a cluster-scope release would also wait for the arriving thread's global
+    // loads and stores in flight (the next slab's gather, the output rows).
+    auto wait = [&](uint64_t &bar, uint32_t parity) { return mbar_wait_bounded(smem_u32(&bar), parity); };
+    auto arrive_leader = [&](uint64_t &bar) {  // on the even CTA's barrier
+        if (rank == 0)
+            mbar_arrive(smem_u32(&bar));
+        else
+            mbar_arrive_remote(mapa_shared(smem_u32(&bar), 0));
+    };
+
+    if (warp < pr::PROD_WARPS) {
+        // ------------------------------------------------------------ producers
+        // One position per thread and slab (L <= 224), software-pipelined as in the
+        // one-phase kernel: the next slab's channel loads are in flight while this one
+        // is converted and stored.
+        const long long plane_stride = (long long)H * W;
+        auto pos_src = [&](long long q) -> const float * {
+            if (q < 0 || q >= n_pos) return nullptr;
+            int R, c;
+            if (n_pos < 0x7fffffffLL) {
+                R = (int)q / BW;
+                c = (int)q - R * BW;
+            } else {
+                R = (int)(q / BW);
+                c = (int)(q - (long long)R * BW);
+            }
+            if (c >= W || R <= 0) return nullptr;
+            const int n = (R - 1) / BH;
+            const int row = R - 1 - n * BH;
+            return row < H ? x + (((long long)n * CIN) * H + row) * (long long)W + c : nullptr;
+        };
+        auto slab_src = [&](int it, int s) -> const float * {
+            const long long ptile = pair + (long long)it * npair;
+            const int dy_lo = nslab == 1 ? dy0 : tap_off(py, s);
+            const long long pbase = ptile * 2 * MT + (long long)rank * MT + BW + (long long)dy_lo * BW + pr::DX0;
+            return tid < L ? pos_src(pbase + tid) : nullptr;
+        };
+        auto src_ok = [&](const float *src) {
+            return src && CHK(src, 4, x, x_bytes) && CHK(src + (CIN - 1) * plane_stride, 4, x, x_bytes);
+        };
+        float r[CIN];
+        {
+            const float *src = n_iter > 0 ? slab_src(0, 0) : nullptr;
+            if (!src_ok(src)) src = nullptr;
+#pragma unroll
+            for (int ci = 0; ci < CIN; ++ci) r[ci] = src ? __ldg(src + ci * plane_stride) : 0.f;
+        }
+        int k = 0;
+        for (int it = 0; it < n_iter && !*abort_flag; ++it) {
+            for (int s = 0; s < nslab; ++s, ++k) {
+                const int stage = k & 1, use = k >> 1;
+                int nit = it, ns = s + 1;
+                if (ns == nslab) {
+                    ns = 0;
+                    ++nit;
+                }
+                const float *nsrc = nit < n_iter ? slab_src(nit, ns) : nullptr;
+                if (!src_ok(nsrc)) nsrc = nullptr;
+                if (use > 0 && !wait(bars.slab_empty[stage], (use - 1) & 1)) fail();
+                unsigned char *slab = sSlab + stage * slab_bytes;
+                if (tid < L) {
+#pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        if (CHKS(slab + g * slab_plane + tid * 16, 16))
+                            *reinterpret_cast<float4 *>(slab + g * slab_plane + tid * 16) =
+                                make_float4(tc::to_tf32(r[4 * g]), tc::to_tf32(r[4 * g + 1]),
+                                            tc::to_tf32(r[4 * g + 2]), tc::to_tf32(r[4 * g + 3]));
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) r[4 * g + j] = nsrc ? __ldg(nsrc + (4 * g + j) * plane_stride) : 0.f;
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) arrive_leader(bars.slab_full[stage]);
+                if (*abort_flag) break;
+            }
+        }
+        if (tid == 0) {
+            // the last multicast commits to this CTA's slab barriers have landed before it can leave
+            const int kt = n_iter * nslab;
+            for (int st = 0; st < NSTAGE; ++st) {
+                const int k_last = kt - 1 - ((kt - 1 - st) & 1);
+                if (k_last >= 0 && !*abort_flag && !wait(bars.slab_empty[st], (k_last >> 1) & 1)) fail();
+            }
+        }
+    } else if (warp == pr::MMA_WARP) {
+        // ------------------------------------------------------------ MMA issue
+        if (lane == 0 && rank == 0 && !*abort_flag) {  // the even CTA issues for the pair
+            const uint32_t sB_addr = smem_u32(sB), sSlab_addr = smem_u32(sSlab);
+            int k = 0;
+            bool ok = true;
+            for (int it = 0; ok && it < n_iter && !*abort_flag; ++it) {
+                const int b = it & 1, ause = it >> 1;
+                // phase 0 of acc_empty completes when both CTAs' epilogues have written the bias
+                if (!wait(bars.acc_empty[b], ause & 1)) {
+                    fail();
+                    break;
+                }
+                tc::fence_after_sync();
+                const uint32_t d0 = tmem + (uint32_t)(b * 2 * COUT);
+                for (int s = 0; s < nslab; ++s, ++k) {
+                    const int stage = k & 1, use = k >> 1;
+                    if (!wait(bars.slab_full[stage], use & 1)) {
+                        fail();
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after_sync();
+                    const uint32_t slab = sSlab_addr + stage * slab_bytes;
+                    const int dy_lo = nslab == 1 ? dy0 : tap_off(py, s);
+#pragma unroll
+                    for (int px = 0; px < 2; ++px) {
+                        for (int ty = (nslab == 1 ? 0 : s); ty <= (nslab == 1 ? 1 : s); ++ty) {
+#pragma unroll
+                            for (int tx = 0; tx < 2; ++tx) {
+                                const int o = (tap_off(py, ty) - dy_lo) * BW + (tap_off(px, tx) - pr::DX0);
+                                const int tap = 2 * ty + tx;
+#pragma unroll
+                                for (int j = 0; j < G / 2; ++j) {
+                                    const uint32_t a_addr = slab + (2 * j * L + o) * 16;
+                                    const uint32_t b_addr = sB_addr + ((px * 4 + tap) * G + 2 * j) * pr::BPLANE;
+                                    const uint64_t ad = tc::smem_desc(a_addr, (uint32_t)slab_plane, 128);
+                                    const uint64_t bd = tc::smem_desc(b_addr, pr::BPLANE, 128);
+                                    // checked build: A 16 groups 128 B apart + a second K plane; B 8
+                                    // groups + a second plane (in each CTA, same offsets)
+                                    if (CHKS(a_addr, 15 * 128 + slab_plane + 128) &&
+                                        CHKS(b_addr, 7 * 128 + pr::BPLANE + 128))
+                                        tc::mma_tf32_pair(d0 + (uint32_t)(px * COUT), ad, bd, pr::IDESC, 1u);
+                                }
+                            }
+                        }
+                    }
+                    tc::commit_pair(smem_u32(&bars.slab_empty[stage]));
+                }
+                if (!ok) break;
+                tc::commit_pair(smem_u32(&bars.acc_full[b]));
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        // Group grp handles the pair's tiles it = grp, grp + 2, ... (accumulator grp).
+        const int q = warp & 3;
+        const int grp = (warp - pr::EPI_WARP0) >> 2;
+        const long long img_anchors = (long long)BH * BW;
+        const long long plane_out = (long long)Ho * Wo;
+        const float ks = -scale * LOG2E;
+        const uint32_t t0 = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(grp * 2 * COUT);  // px 0
+        const uint32_t t1 = t0 + COUT;                                                         // px 1
+        const float4 *cb4 = reinterpret_cast<const float4 *>(sCb);
+        const float4 *kb4 = reinterpret_cast<const float4 *>(sKb);
+        // interleave: store slot A of lane j holds (anchor lane j>>1, px j&1), slot B the
+        // same for anchor lane 16 + (j>>1); see the shuffles in pass 3
+        const int src_lane = (lane & 1) * 16 + (lane >> 1);
+        float v0[32], v1[32];
+        auto reset_chunk = [&](int c) {  // both phases' columns of chunk c <- conv_b * log2(e)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 t = cb4[8 * c + i];
+                v0[4 * i] = t.x;
+                v0[4 * i + 1] = t.y;
+                v0[4 * i + 2] = t.z;
+                v0[4 * i + 3] = t.w;
+            }
+            tc::st32(t0 + 32 * c, v0);
+            tc::st32(t1 + 32 * c, v0);
+        };
+#pragma unroll 1
+        for (int c = 0; c < COUT / 32; ++c) reset_chunk(c);
+        tc::wait_st();
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) arrive_leader(bars.acc_empty[grp]);
+
+        for (int it = grp; it < n_iter && !*abort_flag; it += pr::NBUF) {
+            if (!wait(bars.acc_full[grp], (it >> 1) & 1)) {
+                fail();
+                break;
+            }
+            tc::fence_after_sync();
+            const long long ptile = pair + (long long)it * npair;
+            const long long a = ptile * 2 * MT + (long long)rank * MT + 32 * q + lane;
+            const long long n = a / img_anchors;
+            const int rem = (int)(a - n * img_anchors);
+            const int m = rem / BW, nn = rem - m * BW;
+            const int oh = 2 * m + py;
+            const bool valid = a < n_anchor && oh < Ho;
+            const bool ok0 = valid && 2 * nn < Wo, ok1 = valid && 2 * nn + 1 < Wo;
+            const long long off = valid ? (n * COUT) * plane_out + (long long)oh * Wo + 2 * nn : 0;
+            const long long offA = __shfl_sync(0xffffffffu, off, lane >> 1) + (lane & 1);
+            const long long offB = __shfl_sync(0xffffffffu, off, 16 + (lane >> 1)) + (lane & 1);
+            const bool a0 = __shfl_sync(0xffffffffu, ok0, lane >> 1), a1 = __shfl_sync(0xffffffffu, ok1, lane >> 1);
+            const bool b0 = __shfl_sync(0xffffffffu, ok0, 16 + (lane >> 1));
+            const bool b1 = __shfl_sync(0xffffffffu, ok1, 16 + (lane >> 1));
+            const bool okA = (lane & 1) ? a1 : a0, okB = (lane & 1) ? b1 : b0;
+            // pass 1: max over channels of z, per phase
+            float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll 1
+            for (int c = 0; c < COUT / 32; ++c) {
+                tc::ld32(t0 + 32 * c, v0);
+                tc::ld32(t1 + 32 * c, v1);
+                tc::wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    mx0 = fmaxf(mx0, v0[i]);
+                    mx1 = fmaxf(mx1, v1[i]);
+                }
+            }
+            // pass 2: e = 2^(z - max) written back to TMEM, and the sums
+            float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll 1
+            for (int c = 0; c < COUT / 32; ++c) {
+                tc::ld32(t0 + 32 * c, v0);
+                tc::ld32(t1 + 32 * c, v1);
+                tc::wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    v0[i] = ex2_approx(v0[i] - mx0);
+                    sum0 += v0[i];
+                    v1[i] = ex2_approx(v1[i] - mx1);
+                    sum1 += v1[i];
+                }
+                tc::st32(t0 + 32 * c, v0);
+                tc::st32(t1 + 32 * c, v1);
+            }
+            tc::wait_st();
+            // pass 3: out = 1 / (1 + 2^(-(p + bias) * scale * log2(e))), p = e / sum
+            const float kp0 = ks / sum0, kp1 = ks / sum1;
+            float *pA = out + offA, *pB = out + offB;
+#pragma unroll 1
+            for (int c = 0; c < COUT / 32; ++c) {
+                tc::ld32(t0 + 32 * c, v0);
+                tc::ld32(t1 + 32 * c, v1);
+                tc::wait_ld();
+                // checked build: a slot's 32 channels lie between its first and last store
+                // (tested only for slots that store)
+                const bool sA = okA && (!FW_CHECKED || (CHK(pA, 4, out, out_bytes) &&
+                                                        CHK(pA + 31 * plane_out, 4, out, out_bytes)));
+                const bool sB_ = okB && (!FW_CHECKED || (CHK(pB, 4, out, out_bytes) &&
+                                                         CHK(pB + 31 * plane_out, 4, out, out_bytes)));
+#pragma unroll
+                for (int i4 = 0; i4 < 8; ++i4) {
+                    const float4 kb4v = kb4[8 * c + i4];
+                    const float kbs[4] = {kb4v.x, kb4v.y, kb4v.z, kb4v.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int i = 4 * i4 + e;
+                        const float s0 = __fdividef(1.f, 1.f + ex2_approx(fmaf(v0[i], kp0, kbs[e])));
+                        const float s1 = __fdividef(1.f, 1.f + ex2_approx(fmaf(v1[i], kp1, kbs[e])));
+                        // lanes 0-15 keep px 0 and receive px 0 of lane + 16; lanes 16-31 keep
+                        // px 1 and receive px 1 of lane - 16; then slot A of lane j reads lane
+                        // src_lane's first value and slot B its second
+                        const float recv = __shfl_xor_sync(0xffffffffu, lane < 16 ? s1 : s0, 16);
+                        const float rA = lane < 16 ? s0 : recv, rB = lane < 16 ? recv : s1;
+                        const float oA = __shfl_sync(0xffffffffu, rA, src_lane);
+                        const float oB = __shfl_sync(0xffffffffu, rB, src_lane);
+                        if (sA) pA[i * plane_out] = oA;
+                        if (sB_) pB[i * plane_out] = oB;
+                    }
+                }
+                pA += 32 * plane_out;
+                pB += 32 * plane_out;
+                reset_chunk(c);
+            }
+            tc::wait_st();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) arrive_leader(bars.acc_empty[grp]);
+        }
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    // Neither CTA leaves while the other may still arrive on its barriers or read its
+    // shared memory: each tells the other it is done, then waits for the other (bounded).
+    if (tid == 0) {
+        mbar_arrive_cluster(mapa_shared(smem_u32(&bars.exit_bar), rank ^ 1u));
+        if (!mbar_wait_bounded_cluster(smem_u32(&bars.exit_bar), 0)) atomicOr(&g_err_convt_tc, DEVERR_TIMEOUT);
+    }
+    __syncthreads();
+    if (warp == pr::MMA_WARP) {
+        tc::fence_after_sync();
+        tc::dealloc_pair(tmem, 512);
+    }
+}
+
 template <int G, bool RAW, bool NHWC>
 fw_status launch_g(const float *x, int N, int H, int W, const float *wtc, const float *cb, const float *bias,
                    float scale, float *out, int Ho, int Wo, cudaStream_t st) {
@@ -607,6 +1017,55 @@ fw_status launch_g(const float *x, int N, int H, int W, const float *wtc, const 
     return launch_status(cudaGetLastError());
 }
 
+// The fused NCHW operator on CTA pairs; FW_ERR_UNSUPPORTED when the shape or the
+// device leaves no room for it (the caller then runs the one-phase kernel).
+template <int G>
+fw_status launch_pair(const float *x, int N, int H, int W, const float *wtc, const float *cb, const float *bias,
+                      float scale, float *out, int Ho, int Wo, cudaStream_t st) {
+    int dev = 0, optin = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+        return FW_ERR_LAUNCH;
+    const size_t limit = (size_t)optin < SMEM_LIMIT ? (size_t)optin : SMEM_LIMIT;
+    int nslab = 1, L = W + 131;  // (W+1) + 130: both vertical taps, horizontal offsets -1 .. +1
+    size_t smem = pr::smem_bytes(G, L);
+    if (smem > limit || L > pr::PROD_WARPS * 32) {
+        nslab = 2;
+        L = MT + 2;
+        smem = pr::smem_bytes(G, L);
+    }
+    if (smem > limit) return FW_ERR_UNSUPPORTED;
+    if (smem < MIN_SMEM) smem = MIN_SMEM;
+    cudaError_t e = cudaFuncSetAttribute(convt_k4s2_pair_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return launch_status(e);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(pr::NTHREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // as many pairs as can be resident at once (a GPC with an odd number of free SMs
+    // leaves one of them out), half of them per row phase
+    int clusters = 0;
+    cfg.gridDim = dim3(2);
+    e = cudaOccupancyMaxActiveClusters(&clusters, convt_k4s2_pair_kernel<G>, &cfg);
+    if (e != cudaSuccess) return launch_status(e);
+    const long long ptiles = ((long long)N * (H + 1) * (W + 1) + 2 * MT - 1) / (2 * MT);
+    long long per_py = clusters / 2;
+    if (per_py > ptiles) per_py = ptiles;
+    if (per_py < 1) return FW_ERR_UNSUPPORTED;
+    cfg.gridDim = dim3((unsigned)(4 * per_py));
+    e = cudaLaunchKernelEx(&cfg, convt_k4s2_pair_kernel<G>, x, wtc, cb, bias, scale, out, N, H, W, Ho, Wo, nslab, L);
+    note_launch();
+    return launch_status(e == cudaSuccess ? cudaGetLastError() : e);
+}
+
 }  // namespace
 
 bool convt_tc_eligible(int Cin, int Cout, int k, int s, int p) {
@@ -628,6 +1087,16 @@ fw_status tc_launch(const float *x, int N, int Cin, int H, int W, const float *w
         note_launch();
         const fw_status rc = launch_status(cudaGetLastError());
         if (rc != FW_OK) return rc;
+    }
+    if constexpr (!RAW && !NHWC) {
+        fw_status rc = FW_ERR_UNSUPPORTED;
+        switch (Cin) {
+            case 8: rc = launch_pair<2>(x, N, H, W, wtc, cb, bias, scale, out, Ho, Wo, st); break;
+            case 16: rc = launch_pair<4>(x, N, H, W, wtc, cb, bias, scale, out, Ho, Wo, st); break;
+            case 32: rc = launch_pair<8>(x, N, H, W, wtc, cb, bias, scale, out, Ho, Wo, st); break;
+            case 64: rc = launch_pair<16>(x, N, H, W, wtc, cb, bias, scale, out, Ho, Wo, st); break;
+        }
+        if (rc != FW_ERR_UNSUPPORTED) return rc;
     }
     switch (Cin) {
         case 8: return launch_g<2, RAW, NHWC>(x, N, H, W, wtc, cb, bias, scale, out, Ho, Wo, st);
