@@ -463,7 +463,8 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
             for (int j = 0; j < P; ++j) {
                 const int rowc = k * P + j;  // conv rows in MMA order
                 const int slot = rowc % C::NSLOT, sus = rowc / C::NSLOT;
-                if (!mbar_wait_bounded(smem_u32(&bars.slot_full[slot]), sus & 1)) {
+                // one outcome for the whole warp: the TMEM loads below are warp-collective
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&bars.slot_full[slot]), sus & 1))) {
                     fail();
                     ok = false;
                     break;

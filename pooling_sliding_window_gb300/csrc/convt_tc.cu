@@ -467,7 +467,8 @@ convt_k4s2_tc_kernel(const float *__restrict__ x, const float *__restrict__ wtc,
 
         int u = eg;
         for (int tile = rank + eg * nct; tile < n_tiles && !*abort_flag; tile += NACC * nct, u += NACC) {
-            if (!mbar_wait_bounded(smem_u32(&bars.acc_full[eg]), (u / NACC) & 1)) {
+            // one outcome for the whole warp: the TMEM loads below are warp-collective
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&bars.acc_full[eg]), (u / NACC) & 1))) {
                 fail();
                 break;
             }
@@ -484,13 +485,13 @@ convt_k4s2_tc_kernel(const float *__restrict__ x, const float *__restrict__ wtc,
                 // y = z * ln(2): the accumulator holds (conv-transpose + conv_b) * log2(e)
 #pragma unroll 2
                 for (int c = 0; c < COUT / 32; ++c) {
-                    tc::ld32(taddr + 32 * c, v);
-                    tc::wait_ld();
+                    tc::ld32_wait(taddr + 32 * c, v);
                     if (valid && CHK(o + 32 * c * plane_out, 4, out, out_bytes) &&
                         CHK(o + (32 * c + 31) * plane_out, 4, out, out_bytes)) {
 #pragma unroll
                         for (int i = 0; i < 32; ++i) o[(32 * c + i) * plane_out] = v[i] * LN2;
                     }
+                    __syncwarp();  // the stores above may diverge; TMEM accesses are warp-collective
                     reset_chunk(c);
                 }
                 tc::wait_st();
@@ -506,8 +507,7 @@ convt_k4s2_tc_kernel(const float *__restrict__ x, const float *__restrict__ wtc,
             float mx = -INFINITY;
 #pragma unroll 2
             for (int c = 0; c < COUT / 32; ++c) {
-                tc::ld32(taddr + 32 * c, v);
-                tc::wait_ld();
+                tc::ld32_wait(taddr + 32 * c, v);
 #pragma unroll
                 for (int i = 0; i < 32; ++i) mx = fmaxf(mx, v[i]);
             }
@@ -515,8 +515,7 @@ convt_k4s2_tc_kernel(const float *__restrict__ x, const float *__restrict__ wtc,
             float sum = 0.f;
 #pragma unroll 2
             for (int c = 0; c < COUT / 32; ++c) {
-                tc::ld32(taddr + 32 * c, v);
-                tc::wait_ld();
+                tc::ld32_wait(taddr + 32 * c, v);
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     v[i] = ex2_approx(v[i] - mx);
@@ -529,8 +528,7 @@ convt_k4s2_tc_kernel(const float *__restrict__ x, const float *__restrict__ wtc,
             const float kp = ks / sum;
 #pragma unroll 2
             for (int c = 0; c < COUT / 32; ++c) {
-                tc::ld32(taddr + 32 * c, v);
-                tc::wait_ld();
+                tc::ld32_wait(taddr + 32 * c, v);
                 // checked build: the chunk's 32 channels lie between its first and last store
                 // (tested only for pixels that store)
                 if (valid && (!FW_CHECKED || (NHWC ? CHK(o + 32 * c, 128, out, out_bytes)
@@ -559,6 +557,7 @@ convt_k4s2_tc_kernel(const float *__restrict__ x, const float *__restrict__ wtc,
                         }
                     }
                 }
+                __syncwarp();  // the stores above may diverge; TMEM accesses are warp-collective
                 reset_chunk(c);
             }
             tc::wait_st();
@@ -837,6 +836,15 @@ convt_k4s2_pair_kernel(const float *__restrict__ x, const float *__restrict__ wt
                 if (!ok) break;
                 tc::commit_pair(smem_u32(&bars.acc_full[b]));
             }
+            // The epilogues' releases of the last tiles are arrivals on this CTA's barriers
+            // (the odd CTA's through the cluster) that no MMA waits for: wait for them here,
+            // so none can land after this CTA has left and its shared memory belongs to
+            // another block.  Buffer b's barrier completes once for the initial bias and
+            // once per tile it held.
+            for (int b = 0; ok && b < pr::NBUF && !*abort_flag; ++b) {
+                const int held = (n_iter - b + 1) / 2;
+                if (!wait(bars.acc_empty[b], held & 1)) fail();
+            }
         }
         __syncwarp();
     } else {
@@ -875,7 +883,8 @@ convt_k4s2_pair_kernel(const float *__restrict__ x, const float *__restrict__ wt
         if (lane == 0) arrive_leader(bars.acc_empty[grp]);
 
         for (int it = grp; it < n_iter && !*abort_flag; it += pr::NBUF) {
-            if (!wait(bars.acc_full[grp], (it >> 1) & 1)) {
+            // one outcome for the whole warp: the TMEM loads below are warp-collective
+            if (!__all_sync(0xffffffffu, wait(bars.acc_full[grp], (it >> 1) & 1))) {
                 fail();
                 break;
             }
@@ -898,12 +907,10 @@ convt_k4s2_pair_kernel(const float *__restrict__ x, const float *__restrict__ wt
             // pass 1: max over channels of z, per phase
             float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll 1
-            for (int c = 0; c < COUT / 32; ++c) {
-                tc::ld32(t0 + 32 * c, v0);
-                tc::ld32(t1 + 32 * c, v1);
-                tc::wait_ld();
+            for (int c = 0; c < COUT / 16; ++c) {
+                tc::ld16x2_wait(t0 + 16 * c, t1 + 16 * c, v0, v1);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
+                for (int i = 0; i < 16; ++i) {
                     mx0 = fmaxf(mx0, v0[i]);
                     mx1 = fmaxf(mx1, v1[i]);
                 }
@@ -911,38 +918,35 @@ convt_k4s2_pair_kernel(const float *__restrict__ x, const float *__restrict__ wt
             // pass 2: e = 2^(z - max) written back to TMEM, and the sums
             float sum0 = 0.f, sum1 = 0.f;
 #pragma unroll 1
-            for (int c = 0; c < COUT / 32; ++c) {
-                tc::ld32(t0 + 32 * c, v0);
-                tc::ld32(t1 + 32 * c, v1);
-                tc::wait_ld();
+            for (int c = 0; c < COUT / 16; ++c) {
+                tc::ld16x2_wait(t0 + 16 * c, t1 + 16 * c, v0, v1);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
+                for (int i = 0; i < 16; ++i) {
                     v0[i] = ex2_approx(v0[i] - mx0);
                     sum0 += v0[i];
                     v1[i] = ex2_approx(v1[i] - mx1);
                     sum1 += v1[i];
                 }
-                tc::st32(t0 + 32 * c, v0);
-                tc::st32(t1 + 32 * c, v1);
+                tc::st16(t0 + 16 * c, v0);
+                tc::st16(t1 + 16 * c, v1);
             }
             tc::wait_st();
             // pass 3: out = 1 / (1 + 2^(-(p + bias) * scale * log2(e))), p = e / sum
             const float kp0 = ks / sum0, kp1 = ks / sum1;
             float *pA = out + offA, *pB = out + offB;
+            // 16 channels at a time: both phases' values of a channel are live together
 #pragma unroll 1
-            for (int c = 0; c < COUT / 32; ++c) {
-                tc::ld32(t0 + 32 * c, v0);
-                tc::ld32(t1 + 32 * c, v1);
-                tc::wait_ld();
-                // checked build: a slot's 32 channels lie between its first and last store
+            for (int c = 0; c < COUT / 16; ++c) {
+                tc::ld16x2_wait(t0 + 16 * c, t1 + 16 * c, v0, v1);
+                // checked build: a slot's 16 channels lie between its first and last store
                 // (tested only for slots that store)
                 const bool sA = okA && (!FW_CHECKED || (CHK(pA, 4, out, out_bytes) &&
-                                                        CHK(pA + 31 * plane_out, 4, out, out_bytes)));
+                                                        CHK(pA + 15 * plane_out, 4, out, out_bytes)));
                 const bool sB_ = okB && (!FW_CHECKED || (CHK(pB, 4, out, out_bytes) &&
-                                                         CHK(pB + 31 * plane_out, 4, out, out_bytes)));
+                                                         CHK(pB + 15 * plane_out, 4, out, out_bytes)));
 #pragma unroll
-                for (int i4 = 0; i4 < 8; ++i4) {
-                    const float4 kb4v = kb4[8 * c + i4];
+                for (int i4 = 0; i4 < 4; ++i4) {
+                    const float4 kb4v = kb4[4 * c + i4];
                     const float kbs[4] = {kb4v.x, kb4v.y, kb4v.z, kb4v.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
@@ -960,9 +964,10 @@ convt_k4s2_pair_kernel(const float *__restrict__ x, const float *__restrict__ wt
                         if (sB_) pB[i * plane_out] = oB;
                     }
                 }
-                pA += 32 * plane_out;
-                pB += 32 * plane_out;
-                reset_chunk(c);
+                pA += 16 * plane_out;
+                pB += 16 * plane_out;
+                __syncwarp();  // the stores above may diverge; TMEM accesses are warp-collective
+                if (c & 1) reset_chunk(c >> 1);
             }
             tc::wait_st();
             tc::fence_before_sync();
