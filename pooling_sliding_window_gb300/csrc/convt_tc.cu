@@ -907,10 +907,10 @@ convt_k4s2_pair_kernel(const float *__restrict__ x, const float *__restrict__ wt
             // pass 1: max over channels of z, per phase
             float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll 1
-            for (int c = 0; c < COUT / 16; ++c) {
-                tc::ld16x2_wait(t0 + 16 * c, t1 + 16 * c, v0, v1);
+            for (int c = 0; c < COUT / 32; ++c) {
+                tc::ld32x2_wait(t0 + 32 * c, t1 + 32 * c, v0, v1);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
+                for (int i = 0; i < 32; ++i) {
                     mx0 = fmaxf(mx0, v0[i]);
                     mx1 = fmaxf(mx1, v1[i]);
                 }
@@ -918,17 +918,17 @@ convt_k4s2_pair_kernel(const float *__restrict__ x, const float *__restrict__ wt
             // pass 2: e = 2^(z - max) written back to TMEM, and the sums
             float sum0 = 0.f, sum1 = 0.f;
 #pragma unroll 1
-            for (int c = 0; c < COUT / 16; ++c) {
-                tc::ld16x2_wait(t0 + 16 * c, t1 + 16 * c, v0, v1);
+            for (int c = 0; c < COUT / 32; ++c) {
+                tc::ld32x2_wait(t0 + 32 * c, t1 + 32 * c, v0, v1);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
+                for (int i = 0; i < 32; ++i) {
                     v0[i] = ex2_approx(v0[i] - mx0);
                     sum0 += v0[i];
                     v1[i] = ex2_approx(v1[i] - mx1);
                     sum1 += v1[i];
                 }
-                tc::st16(t0 + 16 * c, v0);
-                tc::st16(t1 + 16 * c, v1);
+                tc::st32(t0 + 32 * c, v0);
+                tc::st32(t1 + 32 * c, v1);
             }
             tc::wait_st();
             // pass 3: out = 1 / (1 + 2^(-(p + bias) * scale * log2(e))), p = e / sum

@@ -68,11 +68,14 @@ SENTINEL = 0x7FBADBAD        # a quiet-NaN payload
 
 
 class Guarded:
-    def __init__(self, shape, dtype=torch.float32):
+    """An output tensor with sentinel words on both sides; `lead` more words in front
+    shift its start (lead = 1: 4-byte but not 8-byte aligned)."""
+
+    def __init__(self, shape, dtype=torch.float32, lead=0):
         n = int(np.prod(shape))
         words = n * (2 if dtype == torch.int64 else 1)
-        self.buf = torch.full((words + 2 * GUARD,), SENTINEL, dtype=torch.int32, device="cuda")
-        self.out = self.buf[GUARD:GUARD + words].view(dtype).view(shape)
+        self.buf = torch.full((words + 2 * GUARD + lead,), SENTINEL, dtype=torch.int32, device="cuda")
+        self.out = self.buf[GUARD + lead:GUARD + lead + words].view(dtype).view(shape)
 
     def check(self, what=""):
         torch.cuda.synchronize()
@@ -81,9 +84,9 @@ class Guarded:
         assert bad == 0, f"{what}: {bad} guard words around the output were overwritten"
 
 
-def guarded_call(fn, shape, *args, **kw):
+def guarded_call(fn, shape, *args, lead=0, **kw):
     """Run fn(*args, out=<guarded tensor of `shape`>, **kw); check the guards; return the output on the host."""
-    g = Guarded(shape)
+    g = Guarded(shape, lead=lead)
     fn(*args, out=g.out, **kw)
     g.check(getattr(fn, "__name__", "call"))
     return host(g.out)

@@ -8,13 +8,13 @@ from tests.parity import FW, O, TOL_FFMA, assert_close, dev, guarded_call, host,
 pytestmark = pytest.mark.gpu
 
 
-def run_gpu(d, scale, s=2, p=1, op=1, cb=True):
+def run_gpu(d, scale, s=2, p=1, op=1, cb=True, lead=0):
     """The fused call into an output with canary guards on both sides."""
     N, _, H, W = d["x"].shape
     Cout, K = d["w"].shape[1], d["w"].shape[2]
     return guarded_call(FW.fw_convtranspose2d_softmax_bias_scale_sigmoid,
                         (N, Cout) + FW.fw_convt_out_shape(H, W, K, s, p, op), dev(d["x"]), dev(d["w"]),
-                        dev(d["conv_b"]) if cb else None, dev(d["bias"]), scale, s, p, op)
+                        dev(d["conv_b"]) if cb else None, dev(d["bias"]), scale, s, p, op, lead=lead)
 
 
 def run_oracle(d, scale, s=2, p=1, op=1, cb=True):
@@ -46,6 +46,16 @@ def test_small_shapes(case):
     want = run_oracle(d, 2.0, s, p, op)
     assert got.shape == want.shape
     assert_close(got, want, TOL_FFMA, str(case))
+
+
+@pytest.mark.parametrize("N,Cin,H,W,op", [(2, 64, 9, 10, 1), (1, 64, 17, 33, 1), (1, 16, 3, 100, 1),
+                                         (2, 8, 11, 3, 0), (1, 32, 6, 64, 1)])
+def test_output_one_float_into_its_buffer(N, Cin, H, W, op):
+    """An output starting 4 bytes past an 8-byte boundary: the tiled kernel picks its 8-byte
+    stores by the parity of each channel's first element, which this start flips."""
+    d = synth.convt_inputs(N, Cin, H, W, 128, seed=N + H + W)
+    got = run_gpu(d, 2.0, op=op, lead=1)
+    assert_close(got, run_oracle(d, 2.0, op=op), TOL_FFMA, str((N, Cin, H, W, op)))
 
 
 def test_no_conv_bias_and_negative_scale():
