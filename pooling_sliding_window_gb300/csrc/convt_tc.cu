@@ -20,7 +20,13 @@
 //     matrices whose 8-row groups are 128 bytes apart), a horizontal tap is a start
 //     address 16 bytes further on and a vertical tap a second "slab".
 //
-// CTA roles (640 threads, one CTA per SM, persistent over the tiles of one phase):
+// Two kernels share this layout.  The fused NCHW operator runs on CTA pairs
+// (convt_k4s2_pair_kernel, further below): 2-SM MMAs, both column phases of a row
+// phase from one slab.  The one-phase kernel described next serves the channels-last
+// call, the unfused path's first stage, and devices where pairs cannot be placed.
+//
+// One-phase kernel, CTA roles (640 threads, one CTA per SM, persistent over the tiles
+// of one phase):
 //   warps 0-6   producers: gather the positions x Cin channels a slab needs from
 //               NCHW x (all channel loads of a position in flight at once), round
 //               to TF32, write the planar shared layout (2 stages); a slab covers
