@@ -865,9 +865,6 @@ convt_k4s2_pair_kernel(const float *__restrict__ x, const float *__restrict__ wt
         const uint32_t t1 = t0 + COUT;                                                         // px 1
         const float4 *cb4 = reinterpret_cast<const float4 *>(sCb);
         const float4 *kb4 = reinterpret_cast<const float4 *>(sKb);
-        // interleave: store slot A of lane j holds (anchor lane j>>1, px j&1), slot B the
-        // same for anchor lane 16 + (j>>1); see the shuffles in pass 3
-        const int src_lane = (lane & 1) * 16 + (lane >> 1);
         float v0[32], v1[32];
         auto reset_chunk = [&](int c) {  // both phases' columns of chunk c <- conv_b * log2(e)
 #pragma unroll
@@ -904,12 +901,16 @@ convt_k4s2_pair_kernel(const float *__restrict__ x, const float *__restrict__ wt
             const bool valid = a < n_anchor && oh < Ho;
             const bool ok0 = valid && 2 * nn < Wo, ok1 = valid && 2 * nn + 1 < Wo;
             const long long off = valid ? (n * COUT) * plane_out + (long long)oh * Wo + 2 * nn : 0;
-            const long long offA = __shfl_sync(0xffffffffu, off, lane >> 1) + (lane & 1);
-            const long long offB = __shfl_sync(0xffffffffu, off, 16 + (lane >> 1)) + (lane & 1);
-            const bool a0 = __shfl_sync(0xffffffffu, ok0, lane >> 1), a1 = __shfl_sync(0xffffffffu, ok1, lane >> 1);
-            const bool b0 = __shfl_sync(0xffffffffu, ok0, 16 + (lane >> 1));
-            const bool b1 = __shfl_sync(0xffffffffu, ok1, 16 + (lane >> 1));
-            const bool okA = (lane & 1) ? a1 : a0, okB = (lane & 1) ? b1 : b0;
+            // Interleaved stores: the pixels of lanes 0-15 (columns 2nn, 2nn + 1 each) and those of
+            // lanes 16-31 form two runs of 32 floats (when the 16 pixels share a row).  Store A
+            // covers the first: lanes 0-15 write their own phase-0 value, lanes 16-31 the phase-1
+            // value of lane - 16; store B the second: lanes 16-31 their own phase-0 value, lanes
+            // 0-15 the phase-1 value of lane + 16.  One xor-16 shuffle per channel feeds both.
+            const long long off_p = __shfl_xor_sync(0xffffffffu, off, 16);
+            const bool ok1_p = __shfl_xor_sync(0xffffffffu, ok1, 16);
+            const bool lo = lane < 16;
+            const long long offA = lo ? off : off_p + 1, offB = lo ? off_p + 1 : off;
+            const bool okA = lo ? ok0 : ok1_p, okB = lo ? ok1_p : ok0;
             // pass 1: max over channels of z, per phase
             float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll 1
@@ -959,15 +960,9 @@ convt_k4s2_pair_kernel(const float *__restrict__ x, const float *__restrict__ wt
                         const int i = 4 * i4 + e;
                         const float s0 = __fdividef(1.f, 1.f + ex2_approx(fmaf(v0[i], kp0, kbs[e])));
                         const float s1 = __fdividef(1.f, 1.f + ex2_approx(fmaf(v1[i], kp1, kbs[e])));
-                        // lanes 0-15 keep px 0 and receive px 0 of lane + 16; lanes 16-31 keep
-                        // px 1 and receive px 1 of lane - 16; then slot A of lane j reads lane
-                        // src_lane's first value and slot B its second
-                        const float recv = __shfl_xor_sync(0xffffffffu, lane < 16 ? s1 : s0, 16);
-                        const float rA = lane < 16 ? s0 : recv, rB = lane < 16 ? recv : s1;
-                        const float oA = __shfl_sync(0xffffffffu, rA, src_lane);
-                        const float oB = __shfl_sync(0xffffffffu, rB, src_lane);
-                        if (sA) pA[i * plane_out] = oA;
-                        if (sB_) pB[i * plane_out] = oB;
+                        const float s1_p = __shfl_xor_sync(0xffffffffu, s1, 16);  // phase 1 of lane ^ 16
+                        if (sA) pA[i * plane_out] = lo ? s0 : s1_p;
+                        if (sB_) pB[i * plane_out] = lo ? s1_p : s0;
                     }
                 }
                 pA += 16 * plane_out;
