@@ -941,19 +941,19 @@ convt_k4s2_pair_kernel(const float *__restrict__ x, const float *__restrict__ wt
             // pass 3: out = 1 / (1 + 2^(-(p + bias) * scale * log2(e))), p = e / sum
             const float kp0 = ks / sum0, kp1 = ks / sum1;
             float *pA = out + offA, *pB = out + offB;
-            // 16 channels at a time: both phases' values of a channel are live together
+            // 32 channels at a time: both phases' values of a channel are live together
 #pragma unroll 1
-            for (int c = 0; c < COUT / 16; ++c) {
-                tc::ld16x2_wait(t0 + 16 * c, t1 + 16 * c, v0, v1);
-                // checked build: a slot's 16 channels lie between its first and last store
+            for (int c = 0; c < COUT / 32; ++c) {
+                tc::ld32x2_wait(t0 + 32 * c, t1 + 32 * c, v0, v1);
+                // checked build: a slot's 32 channels lie between its first and last store
                 // (tested only for slots that store)
                 const bool sA = okA && (!FW_CHECKED || (CHK(pA, 4, out, out_bytes) &&
-                                                        CHK(pA + 15 * plane_out, 4, out, out_bytes)));
+                                                        CHK(pA + 31 * plane_out, 4, out, out_bytes)));
                 const bool sB_ = okB && (!FW_CHECKED || (CHK(pB, 4, out, out_bytes) &&
-                                                         CHK(pB + 15 * plane_out, 4, out, out_bytes)));
+                                                         CHK(pB + 31 * plane_out, 4, out, out_bytes)));
 #pragma unroll
-                for (int i4 = 0; i4 < 4; ++i4) {
-                    const float4 kb4v = kb4[4 * c + i4];
+                for (int i4 = 0; i4 < 8; ++i4) {
+                    const float4 kb4v = kb4[8 * c + i4];
                     const float kbs[4] = {kb4v.x, kb4v.y, kb4v.z, kb4v.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
@@ -965,10 +965,10 @@ convt_k4s2_pair_kernel(const float *__restrict__ x, const float *__restrict__ wt
                         if (sB_) pB[i * plane_out] = lo ? s1_p : s0;
                     }
                 }
-                pA += 16 * plane_out;
-                pB += 16 * plane_out;
+                pA += 32 * plane_out;
+                pB += 32 * plane_out;
                 __syncwarp();  // the stores above may diverge; TMEM accesses are warp-collective
-                if (c & 1) reset_chunk(c >> 1);
+                reset_chunk(c);
             }
             tc::wait_st();
             tc::fence_before_sync();
