@@ -50,3 +50,31 @@ def test_nhwc_alignment_and_support_errors():
         FW.fw_convtranspose2d_softmax_bias_scale_sigmoid_nhwc(torch.zeros(1, 8, 8, 4, device="cuda"),
                                                               torch.zeros(4, 8, 4, 4, device="cuda"), None,
                                                               torch.zeros(8, device="cuda"), 2.0)
+
+
+def test_nchw_tiles_match_channels_last_on_random_shapes():
+    """The NCHW call (CTA pairs, both column phases per tile) and the channels-last call
+    (one phase per CTA) run the same products in the same order: bit-identical results on
+    random shapes, including tiles whose second half lies past the last pixel."""
+    rng = np.random.default_rng(11)
+    for _ in range(40):
+        N, Cin = int(rng.integers(1, 5)), int(rng.choice([8, 16, 32, 64]))
+        H, W = int(rng.integers(1, 40)), int(rng.integers(1, 130))
+        scale = float(rng.choice([2.0, -3.0, 0.5]))
+        d = synth.convt_inputs(N, Cin, H, W, 128, seed=int(rng.integers(0, 1 << 30)))
+        nchw = FW.fw_convtranspose2d_softmax_bias_scale_sigmoid(dev(d["x"]), dev(d["w"]), dev(d["conv_b"]),
+                                                               dev(d["bias"]), scale)
+        cl = FW.fw_convtranspose2d_softmax_bias_scale_sigmoid_nhwc(dev(nhwc(d["x"])), dev(d["w"]), dev(d["conv_b"]),
+                                                                  dev(d["bias"]), scale)
+        FW.fw_check_device_errors()
+        assert torch.equal(nchw.permute(0, 2, 3, 1), cl), (N, Cin, H, W, scale)
+
+
+def test_full_size_repeat_calls_identical():
+    """Full config D called repeatedly: the same bits every time (no race between the pair's CTAs)."""
+    d = synth.convt_inputs(128, 64, 64, 64, 128, seed=0)
+    args = (dev(d["x"]), dev(d["w"]), dev(d["conv_b"]), dev(d["bias"]), 2.0)
+    ref = FW.fw_convtranspose2d_softmax_bias_scale_sigmoid(*args)
+    for _ in range(5):
+        assert torch.equal(FW.fw_convtranspose2d_softmax_bias_scale_sigmoid(*args), ref)
+    FW.fw_check_device_errors()
