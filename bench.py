@@ -648,7 +648,7 @@ def run_gpu(args):
             nhwc_ms = med_ms(lambda: FW.fw_convtranspose2d_softmax_bias_scale_sigmoid_nhwc(
                 xn, d[("ct", "w")], d[("ct", "conv_b")], d[("ct", "bias")], CT["scale"], out=on, workspace=wsp))
             fusion["convt_channels_last"] = {"nchw_ms": f_ms, "nhwc_ms": nhwc_ms,
-                                             "kernel": "convt_k4s2_tc_kernel<16,false,true>: 16-byte channel "
+                                             "kernel": "convt_k4s2_pair_kernel<16,true>: CTA pairs, 16-byte channel "
                                                        "gathers, 256-bit output stores"}
             del xn, on
         FW.fw_check_device_errors()
