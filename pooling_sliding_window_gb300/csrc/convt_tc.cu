@@ -824,7 +824,7 @@ convt_k4s2_pair_kernel(const float *__restrict__ x, const float *__restrict__ wt
             {
                 const float *src = n_iter > 0 ? slab_src(0, 0) : nullptr;
                 if (!src_ok(src)) src = nullptr;
-    #pragma unroll
+#pragma unroll
                 for (int ci = 0; ci < CIN; ++ci) r[ci] = src ? __ldg(src + ci * plane_stride) : 0.f;
             }
             int k = 0;
@@ -841,13 +841,13 @@ convt_k4s2_pair_kernel(const float *__restrict__ x, const float *__restrict__ wt
                     if (use > 0 && !wait(bars.slab_empty[stage], (use - 1) & 1)) fail();
                     unsigned char *slab = sSlab + stage * slab_bytes;
                     if (tid < L) {
-    #pragma unroll
+#pragma unroll
                         for (int g = 0; g < G; ++g) {
                             if (CHKS(slab + g * slab_plane + tid * 16, 16))
                                 *reinterpret_cast<float4 *>(slab + g * slab_plane + tid * 16) =
                                     make_float4(tc::to_tf32(r[4 * g]), tc::to_tf32(r[4 * g + 1]),
                                                 tc::to_tf32(r[4 * g + 2]), tc::to_tf32(r[4 * g + 3]));
-    #pragma unroll
+#pragma unroll
                             for (int j = 0; j < 4; ++j) r[4 * g + j] = nsrc ? __ldg(nsrc + (4 * g + j) * plane_stride) : 0.f;
                         }
                     }
@@ -1048,7 +1048,7 @@ convt_k4s2_pair_kernel(const float *__restrict__ x, const float *__restrict__ wt
             } else {
                 float *pA = out + offA, *pB = out + offB;
                 // 32 channels at a time: both phases' values of a channel are live together
-    #pragma unroll 1
+#pragma unroll 1
                 for (int c = 0; c < COUT / 32; ++c) {
                     tc::ld32x2_wait(t0 + 32 * c, t1 + 32 * c, v0, v1);
                     // checked build: a slot's 32 channels lie between its first and last store
@@ -1057,11 +1057,11 @@ convt_k4s2_pair_kernel(const float *__restrict__ x, const float *__restrict__ wt
                                                             CHK(pA + 31 * plane_out, 4, out, out_bytes)));
                     const bool sB_ = okB && (!FW_CHECKED || (CHK(pB, 4, out, out_bytes) &&
                                                              CHK(pB + 31 * plane_out, 4, out, out_bytes)));
-    #pragma unroll
+#pragma unroll
                     for (int i4 = 0; i4 < 8; ++i4) {
                         const float4 kb4v = kb4[8 * c + i4];
                         const float kbs[4] = {kb4v.x, kb4v.y, kb4v.z, kb4v.w};
-    #pragma unroll
+#pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const int i = 4 * i4 + e;
                             const float s0 = __fdividef(1.f, 1.f + ex2_approx(fmaf(v0[i], kp0, kbs[e])));
