@@ -580,7 +580,7 @@ def run_gpu(args):
     # What fusion saves: the same operators the pages' unfused way (conv output to memory,
     # then a second kernel), built from this library's kernels; outside the timed step.
     fusion = None
-    if not args.no_fusion_compare and (cp or ct):
+    if not args.no_fusion_compare and (cp or ct or mp):
         fusion = {}
 
         def med_ms(fn, reps=7):
@@ -650,6 +650,19 @@ def run_gpu(args):
             fusion["convt_channels_last"] = {"nchw_ms": f_ms, "nhwc_ms": nhwc_ms,
                                              "kernel": "convt_k4s2_pair_kernel<16,true>: CTA pairs, 16-byte channel "
                                                        "gathers, 256-bit output stores"}
+            del xn, on
+        if mp:
+            # channels-last maxpool of the same workload (x [N,H,W,C] -> out [N,Ho,Wo,C])
+            n = mp["x"].shape[0]
+            xn = d[("mp", "x")].permute(0, 2, 3, 1).contiguous()
+            on = torch.empty(n, 511, 511, MP["C"], device=dev)
+            f_ms = med_ms(lambda: op_mp(d, out_mp))
+            nhwc_ms = med_ms(lambda: FW.fw_maxpool2d_nhwc(xn, 4, 1, 1, 1, out=on))
+            fusion["maxpool_channels_last"] = {
+                "nchw_ms": f_ms, "nhwc_ms": nhwc_ms, "nhwc_gbs": mp_bytes(N=n) / (nhwc_ms * 1e-3) / 1e9,
+                "nhwc_frac_of_hbm": mp_bytes(N=n) / (nhwc_ms * 1e-3) / 1e9 / peaks()["hbm_gbs"],
+                "kernel": "maxpool_nhwc_s1_kernel<4>: 4 channels of one output column per thread (16-byte loads "
+                          "and stores), row maxima in a 4-deep register ring over a band of 64 output rows"}
             del xn, on
         FW.fw_check_device_errors()
     configs = None

@@ -13,7 +13,7 @@
  * Variants, declared below the call they extend: *_tf32 (conv+pool on plain-TF32
  * tensor cores), *_ffma (conv+pool or conv-transpose on the float32 FMA pipe
  * only), fw_maxpool2d_ex (ceil mode, argmax indices), *_unfused (the two-kernel
- * design, for comparison), *_nhwc (channels-last conv-transpose), *_noalloc
+ * design, for comparison), *_nhwc (channels last: conv-transpose, maxpool), *_noalloc
  * (conv-transpose without a caller workspace) and *_host (host buffers, copies
  * pipelined with the kernels).
  *
@@ -158,6 +158,18 @@ fw_status fw_conv2d_tanh_scale_bias_maxpool_ffma(const float *x, int N, int Cin,
  */
 fw_status fw_maxpool2d(const float *x, int N, int C, int H, int W, int k, int s, int p, int d,
                        float *out, void *stream);
+
+/*
+ * Channels-last MaxPool2d: x [N, H, W, C] and out [N, Ho, Wo, C] (Ho, Wo from
+ * fw_maxpool2d_out_shape), the definition, tie and NaN rules of fw_maxpool2d per
+ * channel.  Stride 1, dilation 1, k <= 5, C a multiple of 4 (C <= 1024) and 16-byte
+ * aligned x and out take a band kernel that handles 4 adjacent channels of one
+ * output column per thread with 16-byte loads and stores (row maxima, then a K-deep
+ * ring of rows: the same values as the row-major definition); other arguments take a
+ * direct kernel, one output value per thread.  Statuses as fw_maxpool2d.
+ */
+fw_status fw_maxpool2d_nhwc(const float *x, int N, int H, int W, int C, int k, int s, int p, int d, float *out,
+                            void *stream);
 
 /*
  * MaxPool2d with PyTorch's optional extensions (not on the pages: the l1_p42 trace

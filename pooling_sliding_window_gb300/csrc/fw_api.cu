@@ -12,6 +12,8 @@ fw_status maxpool2d_launch(const float *x, long long NC, int H, int W, int k, in
                            int Wo, float *out, cudaStream_t st);
 fw_status maxpool2d_ex_launch(const float *x, long long NC, int H, int W, int k, int s, int p, int d, int Ho,
                               int Wo, float *out, long long *idx, cudaStream_t st);
+fw_status maxpool2d_nhwc_launch(const float *x, int N, int H, int W, int C, int k, int s, int p, int d, int Ho,
+                                int Wo, float *out, cudaStream_t st);
 unsigned maxpool_read_and_clear_error();
 unsigned convt_tc_read_and_clear_error();
 unsigned convpool_tc_read_and_clear_error();
@@ -258,6 +260,20 @@ fw_status fw_maxpool2d(const float *x, int N, int C, int H, int W, int k, int s,
     if (overlaps(out, no * 4, x, nx * 4)) return FW_ERR_ALIAS;
     return maxpool2d_launch(x, (long long)N * C, H, W, k, s, p, d, Ho, Wo, out,
                             static_cast<cudaStream_t>(stream));
+}
+
+fw_status fw_maxpool2d_nhwc(const float *x, int N, int H, int W, int C, int k, int s, int p, int d, float *out,
+                            void *stream) {
+    if (!x || !out) return FW_ERR_NULL;
+    if (N < 1 || C < 1) return FW_ERR_SHAPE;
+    int Ho = 0, Wo = 0;
+    fw_status rc = maxpool_shape(H, W, k, s, p, d, &Ho, &Wo);
+    if (rc != FW_OK) return rc;
+    if (misaligned(x) || misaligned(out)) return FW_ERR_ALIGN;
+    const long long nx = prod({N, H, W, C}), no = prod({N, Ho, Wo, C});
+    if (nx < 0 || no < 0) return FW_ERR_SHAPE;
+    if (overlaps(out, no * 4, x, nx * 4)) return FW_ERR_ALIAS;
+    return maxpool2d_nhwc_launch(x, N, H, W, C, k, s, p, d, Ho, Wo, out, static_cast<cudaStream_t>(stream));
 }
 
 fw_status fw_maxpool2d_ex(const float *x, int N, int C, int H, int W, int k, int s, int p, int d, int ceil_mode,

@@ -580,6 +580,176 @@ fw_status maxpool2d_launch(const float *x, long long NC, int H, int W, int k, in
     return launch_status(cudaGetLastError());
 }
 
+// ------------------------------------------------------------ channels last --
+// x [N, H, W, C], out [N, Ho, Wo, C]: the same definition, tie and NaN rules as the
+// NCHW kernels, applied per channel (the channel axis is the innermost, so a thread
+// handles 4 adjacent channels of one output column with 16-byte loads and stores).
+
+namespace {
+
+// The definition's window maximum of one channel-last output value (taps in row-major
+// order, -inf padding, first of equal values kept), read from global memory: the rare
+// recompute of a zero maximum, whose sign the definition fixes by tap order.
+template <int K>
+__device__ __noinline__ float window_max_exact_nhwc(const float *__restrict__ img, int H, int W, int C, int oh,
+                                                    int ow, int P, const float *x, long long x_bytes) {
+    float m = -INFINITY;
+    for (int i = 0; i < K; ++i) {
+        const int ih = oh - P + i;
+        for (int j = 0; j < K; ++j) {
+            const int iw = ow - P + j;
+            const float *a = img + ((long long)ih * W + iw) * C;
+            const float v = (ih >= 0 && ih < H && iw >= 0 && iw < W && CHK(a, 4, x, x_bytes)) ? __ldg(a) : -INFINITY;
+            m = max_update(m, v);
+        }
+    }
+    return m;
+}
+
+// Stride 1, dilation 1, C % 4 == 0, 16-byte aligned x and out.  Thread = (output
+// column ow, channels 4c4..4c4+3) of one band of output rows of one image; it walks the
+// band's input rows once, takes each row's maximum over its K columns and keeps the
+// last K row maxima in a register ring, so output row oh is the maximum of the rows
+// oh - P .. oh - P + K - 1 (separable max; rows and columns outside the input are -inf).
+// The reductions use max.NaN (a NaN propagates); a zero maximum is recomputed tap by
+// tap with the definition's rule, which fixes its sign.
+template <int K>
+__global__ void __launch_bounds__(256) maxpool_nhwc_s1_kernel(const float *__restrict__ x, float *__restrict__ out,
+                                                              int H, int W, int C4, int Ho, int Wo, int P, int band,
+                                                              int nbands, int owb) {
+    const int tid = threadIdx.x;
+    const int cols = 256 / C4;  // output columns per block (C4 <= 256)
+    const long long blk = blockIdx.x;
+    const int cw = (int)(blk % owb);  // block of output columns
+    const long long t1 = blk / owb;
+    const int b = (int)(t1 % nbands);
+    const long long n = t1 / nbands;
+    const int ow = cw * cols + tid / C4, c4 = tid % C4;
+    const int r0 = b * band, r1 = min(Ho, r0 + band);
+    if (tid >= cols * C4 || ow >= Wo) return;
+    const long long row_pitch = (long long)W * C4;  // float4 per input row
+    const long long N = (long long)gridDim.x / ((long long)nbands * owb);
+    const float4 *xn = reinterpret_cast<const float4 *>(x) + n * H * row_pitch + c4;
+    float4 *on = reinterpret_cast<float4 *>(out) + n * (long long)Ho * Wo * C4 + c4;
+    const long long x_bytes = 16 * N * H * row_pitch, out_bytes = 16 * N * Ho * Wo * C4;
+    const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    auto upd4 = [](float4 &m, const float4 &v) {
+        m.x = max_nan(m.x, v.x);
+        m.y = max_nan(m.y, v.y);
+        m.z = max_nan(m.z, v.z);
+        m.w = max_nan(m.w, v.w);
+    };
+    // Input row ih feeds output rows ih + P - (K - 1) .. ih + P; it completes output row
+    // ih + P - (K - 1).  Rows are taken K at a time so that row ih0 + K*g + u lives in ring
+    // slot u (static indices).
+    float4 ring[K];
+#pragma unroll
+    for (int i = 0; i < K; ++i) ring[i] = ninf;
+    const int ih0 = r0 - P, ih1 = r1 - 1 - P + K - 1;  // the rows output rows r0 .. r1 - 1 read
+    for (int g0 = ih0; g0 <= ih1; g0 += K) {
+#pragma unroll
+        for (int u = 0; u < K; ++u) {
+            const int ih = g0 + u;
+            if (ih > ih1) break;
+            float4 h = ninf;
+            if (ih >= 0 && ih < H) {
+                const float4 *row = xn + (long long)ih * row_pitch;
+#pragma unroll
+                for (int j = 0; j < K; ++j) {
+                    const int iw = ow - P + j;
+                    float4 v = ninf;
+                    if (iw >= 0 && iw < W && CHK(row + (long long)iw * C4, 16, x, x_bytes))
+                        v = __ldg(row + (long long)iw * C4);
+                    upd4(h, v);
+                }
+            }
+            ring[u] = h;
+            const int oh = ih + P - (K - 1);
+            if (oh >= r0) {
+                // its rows oh - P .. oh - P + K - 1 = ih - K + 1 .. ih sit in slots u + 1, ..., u (mod K)
+                float4 m = ninf;
+#pragma unroll
+                for (int i = 1; i <= K; ++i) upd4(m, ring[(u + i) % K]);
+                if (m.x == 0.f || m.y == 0.f || m.z == 0.f || m.w == 0.f) {
+                    const float *img = x + n * H * (long long)W * (4 * C4) + 4 * c4;
+                    if (m.x == 0.f) m.x = window_max_exact_nhwc<K>(img, H, W, 4 * C4, oh, ow, P, x, x_bytes);
+                    if (m.y == 0.f) m.y = window_max_exact_nhwc<K>(img + 1, H, W, 4 * C4, oh, ow, P, x, x_bytes);
+                    if (m.z == 0.f) m.z = window_max_exact_nhwc<K>(img + 2, H, W, 4 * C4, oh, ow, P, x, x_bytes);
+                    if (m.w == 0.f) m.w = window_max_exact_nhwc<K>(img + 3, H, W, 4 * C4, oh, ow, P, x, x_bytes);
+                }
+                float4 *o = on + ((long long)oh * Wo + ow) * C4;
+                if (CHK(o, 16, out, out_bytes)) *o = m;
+            }
+        }
+    }
+}
+
+// Any (k, s, p, d) and C: one thread per output value, taps in row-major order.
+__global__ void maxpool_nhwc_direct_kernel(const float *__restrict__ x, float *__restrict__ out, long long total,
+                                           int H, int W, int C, int Ho, int Wo, int k, int s, int p, int d) {
+    const long long x_elems = total / ((long long)Ho * Wo) * H * W;  // N * C * H * W
+    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const int c = (int)(idx % C);
+        long long t = idx / C;
+        const int ow = (int)(t % Wo);
+        t /= Wo;
+        const int oh = (int)(t % Ho);
+        const long long n = t / Ho;
+        const float *img = x + n * H * (long long)W * C + c;
+        float m = -INFINITY;
+        for (int i = 0; i < k; ++i) {
+            const int ih = oh * s - p + i * d;
+            const bool rin = ih >= 0 && ih < H;
+            for (int j = 0; j < k; ++j) {
+                const int iw = ow * s - p + j * d;
+                const float *a = img + ((long long)ih * W + iw) * C;
+                const float v = (rin && iw >= 0 && iw < W && CHK(a, 4, x, 4 * x_elems)) ? __ldg(a) : -INFINITY;
+                m = max_update(m, v);
+            }
+        }
+        if (CHK(out + idx, 4, out, 4 * total)) out[idx] = m;
+    }
+}
+
+template <int K>
+fw_status launch_nhwc_s1(const float *x, float *out, int N, int H, int W, int C, int Ho, int Wo, int p,
+                         cudaStream_t st) {
+    const int C4 = C / 4;
+    const int cols = 256 / C4;  // output columns per block
+    const int band = Ho <= 64 ? Ho : 64;
+    const int nbands = (Ho + band - 1) / band;
+    const int owb = (Wo + cols - 1) / cols;
+    const long long blocks = (long long)N * nbands * owb;
+    if (blocks > 0x7fffffffLL) return FW_ERR_SHAPE;
+    maxpool_nhwc_s1_kernel<K><<<(unsigned)blocks, 256, 0, st>>>(x, out, H, W, C4, Ho, Wo, p, band, nbands, owb);
+    note_launch();
+    return launch_status(cudaGetLastError());
+}
+
+}  // namespace
+
+fw_status maxpool2d_nhwc_launch(const float *x, int N, int H, int W, int C, int k, int s, int p, int d, int Ho,
+                                int Wo, float *out, cudaStream_t st) {
+    const bool aligned = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(out)) & 15u) == 0;
+    if (s == 1 && d == 1 && aligned && C % 4 == 0 && C <= 1024) {
+        switch (k) {
+            case 1: return launch_nhwc_s1<1>(x, out, N, H, W, C, Ho, Wo, p, st);
+            case 2: return launch_nhwc_s1<2>(x, out, N, H, W, C, Ho, Wo, p, st);
+            case 3: return launch_nhwc_s1<3>(x, out, N, H, W, C, Ho, Wo, p, st);
+            case 4: return launch_nhwc_s1<4>(x, out, N, H, W, C, Ho, Wo, p, st);
+            case 5: return launch_nhwc_s1<5>(x, out, N, H, W, C, Ho, Wo, p, st);
+        }
+    }
+    const long long total = (long long)N * Ho * Wo * C;
+    const int threads = 256;
+    long long blocks = (total + threads - 1) / threads;
+    if (blocks > 152LL * 64) blocks = 152LL * 64;
+    maxpool_nhwc_direct_kernel<<<(unsigned)blocks, threads, 0, st>>>(x, out, total, H, W, C, Ho, Wo, k, s, p, d);
+    note_launch();
+    return launch_status(cudaGetLastError());
+}
+
 unsigned maxpool_read_and_clear_error() {
     unsigned v = 0, zero = 0;
     if (cudaMemcpyFromSymbol(&v, g_err_maxpool, sizeof(v)) != cudaSuccess) return DEVERR_INTERNAL;

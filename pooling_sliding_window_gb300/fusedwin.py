@@ -38,7 +38,8 @@ EXPORTS = ("fw_status_string", "fw_version", "fw_conv2d_pool_out_shape", "fw_max
            "fw_convtranspose2d_softmax_bias_scale_sigmoid_host",
            "fw_convtranspose2d_softmax_bias_scale_sigmoid_host_workspace_size",
            "fw_convtranspose2d_softmax_bias_scale_sigmoid_nhwc", "fw_conv2d_tanh_scale_bias_maxpool_tf32",
-           "fw_conv2d_tanh_scale_bias_maxpool_ffma", "fw_convtranspose2d_softmax_bias_scale_sigmoid_ffma")
+           "fw_conv2d_tanh_scale_bias_maxpool_ffma", "fw_convtranspose2d_softmax_bias_scale_sigmoid_ffma",
+           "fw_maxpool2d_nhwc")
 
 
 class FusedWinError(RuntimeError):
@@ -83,6 +84,8 @@ def lib():
             getattr(L, name).argtypes = [P, I, I, I, I, P, P, I, I, I, F, P, I, I, P, P]
         L.fw_maxpool2d.restype = I
         L.fw_maxpool2d.argtypes = [P, I, I, I, I, I, I, I, I, P, P]
+        L.fw_maxpool2d_nhwc.restype = I
+        L.fw_maxpool2d_nhwc.argtypes = [P, I, I, I, I, I, I, I, I, P, P]
         for name in ("fw_convtranspose2d_softmax_bias_scale_sigmoid",
                      "fw_convtranspose2d_softmax_bias_scale_sigmoid_ffma"):
             getattr(L, name).restype = I
@@ -316,6 +319,25 @@ def fw_maxpool2d(x, k, s=None, p=0, d=1, out=None):
     with torch.cuda.device(dev):
         _check(lib().fw_maxpool2d(_ptr(xd), N, Cc, H, W, k, s, p, d, _ptr(od), C.c_void_p(stream)),
                "fw_maxpool2d")
+    return _finish(od, out, host)
+
+
+def fw_maxpool2d_nhwc(x, k, s=None, p=0, d=1, out=None):
+    """Channels-last MaxPool2d: x [N, H, W, C] -> out [N, Ho, Wo, C]."""
+    s = k if s is None else s
+    host = x.device.type != "cuda"
+    _check_dims("x", x, 4)
+    N, H, W, Cc = x.shape
+    Ho, Wo = fw_maxpool2d_out_shape(H, W, k, s, p, d)
+    _check_out(out, (N, Ho, Wo, Cc), "cpu" if host else "cuda")
+    dev = _device_of(x)
+    xd = _dev(x, "x", dev)
+    od = out if (out is not None and not host) else torch.empty((N, Ho, Wo, Cc), device=dev,
+                                                                 dtype=torch.float32)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    with torch.cuda.device(dev):
+        _check(lib().fw_maxpool2d_nhwc(_ptr(xd), N, H, W, Cc, k, s, p, d, _ptr(od), C.c_void_p(stream)),
+               "fw_maxpool2d_nhwc")
     return _finish(od, out, host)
 
 

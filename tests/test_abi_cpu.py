@@ -91,6 +91,12 @@ def test_operator_argument_errors_without_launch():
     assert L.fw_maxpool2d(x, 1, 1, 8, 8, 2, 2, 0, 0, o, None) == 3
     assert L.fw_maxpool2d(P(0x10002), 1, 1, 8, 8, 2, 2, 0, 1, o, None) == 5
     assert L.fw_maxpool2d(x, 1, 1, 8, 8, 2, 2, 0, 1, P(0x10000 + 64), None) == 4  # out inside x
+    # channels-last maxpool: (x, N, H, W, C, k, s, p, d, out, stream)
+    assert L.fw_maxpool2d_nhwc(None, 1, 8, 8, 4, 2, 2, 0, 1, o, None) == 1
+    assert L.fw_maxpool2d_nhwc(x, 1, 8, 8, 0, 2, 2, 0, 1, o, None) == 2
+    assert L.fw_maxpool2d_nhwc(x, 1, 8, 8, 4, 2, 2, 0, 0, o, None) == 3
+    assert L.fw_maxpool2d_nhwc(P(0x10002), 1, 8, 8, 4, 2, 2, 0, 1, o, None) == 5
+    assert L.fw_maxpool2d_nhwc(x, 1, 8, 8, 4, 2, 2, 0, 1, P(0x10000 + 64), None) == 4  # out inside x
     # conv+pool
     args = lambda **kw: dict(dict(x=x, N=1, Cin=8, H=16, W=16, w=w, cb=None, Cout=4, KH=3, KW=3,
                                   scale=2.0, bias=b, pk=4, ps=0, out=o), **kw)
