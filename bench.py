@@ -629,6 +629,17 @@ def run_gpu(args):
                                                  "4x4 conv pixels x 4 channels per thread, cp.async staging",
                                        "max_abs_diff_vs_x3": float((out_ff - out_cp).abs().max())}
             del out_ff
+            # channels-last variant (x [N,H,W,8] -> out [N,Ho,Wo,Cout]), the same 3xTF32 arithmetic
+            xn = d[("cp", "x")].permute(0, 2, 3, 1).contiguous()
+            on = torch.empty(n, out_cp.shape[2], out_cp.shape[3], CP["Cout"], device=dev)
+            nhwc_ms = med_ms(lambda: FW.fw_conv2d_tanh_scale_bias_maxpool_nhwc(
+                xn, d[("cp", "w")], d[("cp", "conv_b")], d[("cp", "bias")], CP["scale"], 4, out=on))
+            fusion["convpool_channels_last"] = {
+                "nchw_ms": f_ms, "nhwc_ms": nhwc_ms, "nhwc_tflops": cp_flops(N=n) / (nhwc_ms * 1e-3) / 1e12,
+                "equal_to_nchw": bool(torch.equal(on, out_cp.permute(0, 2, 3, 1))),
+                "kernel": "convpool_tc_kernel<4,64,false,true,true>: a position's 8 channels as two 16-byte "
+                          "loads (core-matrix rows as they stand), 32 contiguous bytes per pooled pixel stored"}
+            del xn, on
         if ct:
             n = ct["x"].shape[0]
             wsz = FW.fw_convt_unfused_workspace_size(n, CT["Cin"], CT["H"], CT["W"], CT["Cout"], 4, 2, 1, 1)

@@ -13,7 +13,8 @@
  * Variants, declared below the call they extend: *_tf32 (conv+pool on plain-TF32
  * tensor cores), *_ffma (conv+pool or conv-transpose on the float32 FMA pipe
  * only), fw_maxpool2d_ex (ceil mode, argmax indices), *_unfused (the two-kernel
- * design, for comparison), *_nhwc (channels last: conv-transpose, maxpool), *_noalloc
+ * design, for comparison), *_nhwc (channels last: conv+pool, maxpool, conv-transpose),
+ * *_noalloc
  * (conv-transpose without a caller workspace) and *_host (host buffers, copies
  * pipelined with the kernels).
  *
@@ -121,6 +122,22 @@ fw_status fw_conv2d_tanh_scale_bias_maxpool(const float *x, int N, int Cin, int 
  * statuses, layout and ownership are those of fw_conv2d_tanh_scale_bias_maxpool.
  */
 fw_status fw_conv2d_tanh_scale_bias_maxpool_tf32(const float *x, int N, int Cin, int H, int W,
+                                                 const float *w, const float *conv_b, int Cout,
+                                                 int KH, int KW, float scale, const float *bias,
+                                                 int pool_k, int pool_s, float *out, void *stream);
+
+/*
+ * Channels-last variant of fw_conv2d_tanh_scale_bias_maxpool (same definition,
+ * weights [Cout, Cin, KH, KW], statuses and 3xTF32 tolerance): x [N, H, W, Cin],
+ * out [N, Ho, Wo, Cout].  Only the tensor-core shapes (Cin = 8, KH = KW = 3,
+ * pool_s = pool_k in {2, 4}, Cout in {16, 32, 48, 64}); other valid arguments
+ * return FW_ERR_UNSUPPORTED.  x and out must be 16-byte aligned (FW_ERR_ALIGN
+ * otherwise).  A position's 8 input channels are two 16-byte loads that are rows
+ * of the MMA's core matrices as they stand, and a pooled pixel's channels are
+ * stored as 32 contiguous bytes per thread.  The result equals the NCHW call's
+ * bit for bit, transposed.
+ */
+fw_status fw_conv2d_tanh_scale_bias_maxpool_nhwc(const float *x, int N, int Cin, int H, int W,
                                                  const float *w, const float *conv_b, int Cout,
                                                  int KH, int KW, float scale, const float *bias,
                                                  int pool_k, int pool_s, float *out, void *stream);

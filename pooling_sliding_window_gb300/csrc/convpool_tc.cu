@@ -157,7 +157,11 @@ __device__ __forceinline__ float upd(float m, float v, bool use_min) {
 // comparison path -- `out` receives y = conv(x) + conv_b for the P*Ho x P*Wo conv
 // outputs the pool reads ([Nimg, N, P*Ho, P*Wo]); scale and bias are unused.
 // X3 selects the 3xTF32 split (true) or a single TF32 product (false).
-template <int P, int N, bool RAW, bool X3>
+// NHWC = true (3xTF32 fused operator only): x is [Nimg, H, W, 8] and out [Nimg, Ho, Wo, N]
+// (channels last); a producer loads a position's 4 channels of a K plane as one 16-byte
+// load, which is one row of a core matrix as it stands, and each pooled row (its pixels'
+// channels contiguous) is stored as 16-byte runs.
+template <int P, int N, bool RAW, bool X3, bool NHWC = false>
 __global__ void __launch_bounds__(Cfg<P, N, RAW, X3>::NTHREADS, 1)
 convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, const float *__restrict__ cb,
                    const float *__restrict__ bias, float scale, float *__restrict__ out, int Nimg, int H, int W,
@@ -278,72 +282,134 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
             const float *sp = src + ci * plane_stride;
             return ok && CHK(sp, 4, x, x_bytes) ? __ldg(sp) : 0.f;
         };
-        float4 vm[CIN];
-        float vt[CIN];
-        ItemCursor cur(blockIdx.x, gridDim.x, Ho, ncb), nxt = cur;
-        {
-            int col;
-            bool ok, tok;
-            const float *ms = main_src(cur, col, ok), *ts = tail_src(cur, tok);
-            ok = ok && blockIdx.x < n_items;
-            tok = tok && blockIdx.x < n_items;
+        // channels last: x + ((n*H + row)*W + col)*8 + 4g holds channels 4g..4g+3 of a position
+        auto nhwc_src = [&](const ItemCursor &c, int row, int col) {
+            return x + ((((long long)c.n * H + row) * W + col) * CIN);
+        };
+        auto load4 = [&](const float *sp, bool ok) {
+            return ok && CHK(sp, 16, x, x_bytes) ? __ldg(reinterpret_cast<const float4 *>(sp))
+                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+        };
+        if constexpr (NHWC) {
+            static_assert(!NHWC || (X3 && !RAW), "channels last serves the fused 3xTF32 operator");
+            // the same tasks: main = 4 columns x 2 planes, tail = 1 column x 2 planes
+            float4 vm4[8], vt4[2];
+            ItemCursor cur(blockIdx.x, gridDim.x, Ho, ncb), nxt = cur;
+            auto load_item = [&](const ItemCursor &c, bool has) {
+                const int mrow = c.pr * P + mr, mcol = c.cblk * MT + 4 * ma + 16 * mrr;
+                const bool mok = has && ptid < MTASK && mrow < H;
 #pragma unroll
-            for (int ci = 0; ci < CIN; ++ci) {
-                vm[ci] = load_main(ms, col, ok, ci);
-                vt[ci] = load_tail(ts, tok, ci);
-            }
-        }
-        int k = 0;
-        for (long long item = blockIdx.x; item < n_items && !*abort_flag;
-             item += gridDim.x, ++k, cur.advance(Ho, ncb)) {
-            const int stage = k % C::NST, use = k / C::NST;
-            nxt.advance(Ho, ncb);
-            const bool has_next = item + gridDim.x < n_items;
-            int ncol;
-            bool nok, ntok;
-            const float *nms = main_src(nxt, ncol, nok), *nts = tail_src(nxt, ntok);
-            nok = nok && has_next;
-            ntok = ntok && has_next;
-            if (use > 0 && !mbar_wait_bounded(smem_u32(&bars.slab_empty[stage]), (use - 1) & 1)) fail();
-            unsigned char *slab = sSlab + stage * C::SLAB;
-            // hi/lo split of 4 channels of one position into the two halves of the slab
-            auto put = [&](unsigned char *dst, float c0, float c1, float c2, float c3) {
-                const float h0 = tc::to_tf32(c0), h1 = tc::to_tf32(c1), h2 = tc::to_tf32(c2), h3 = tc::to_tf32(c3);
-                if (CHKS(dst, 16)) *reinterpret_cast<float4 *>(dst) = make_float4(h0, h1, h2, h3);
-                if constexpr (X3)
+                for (int j = 0; j < 4; ++j)
+#pragma unroll
+                    for (int g = 0; g < 2; ++g)
+                        vm4[2 * j + g] = load4(nhwc_src(c, mrow, mcol + j) + 4 * g, mok && mcol + j < W);
+                const int trow = c.pr * P + tr, tcol = c.cblk * MT + 16 + (tu >> 3) + 16 * (tu & 7);
+                const bool tok = has && ptid < TTASK && trow < H && tcol < W;
+#pragma unroll
+                for (int g = 0; g < 2; ++g) vt4[g] = load4(nhwc_src(c, trow, tcol) + 4 * g, tok);
+            };
+            load_item(cur, blockIdx.x < n_items);
+            int k = 0;
+            for (long long item = blockIdx.x; item < n_items && !*abort_flag;
+                 item += gridDim.x, ++k, cur.advance(Ho, ncb)) {
+                const int stage = k % C::NST, use = k / C::NST;
+                nxt.advance(Ho, ncb);
+                if (use > 0 && !mbar_wait_bounded(smem_u32(&bars.slab_empty[stage]), (use - 1) & 1)) fail();
+                unsigned char *slab = sSlab + stage * C::SLAB;
+                auto put4 = [&](unsigned char *dst, float4 v) {  // hi/lo split into the two halves
+                    const float h0 = tc::to_tf32(v.x), h1 = tc::to_tf32(v.y), h2 = tc::to_tf32(v.z),
+                                h3 = tc::to_tf32(v.w);
+                    if (CHKS(dst, 16)) *reinterpret_cast<float4 *>(dst) = make_float4(h0, h1, h2, h3);
                     if (CHKS(dst + C::SPLIT, 16))
                         *reinterpret_cast<float4 *>(dst + C::SPLIT) = make_float4(
-                            tc::to_tf32(c0 - h0), tc::to_tf32(c1 - h1), tc::to_tf32(c2 - h2), tc::to_tf32(c3 - h3));
-            };
-            if (ptid < MTASK) {
-                unsigned char *dst = slab + mr * RB + 4 * ma * CORE + mrr * 16;
+                            tc::to_tf32(v.x - h0), tc::to_tf32(v.y - h1), tc::to_tf32(v.z - h2), tc::to_tf32(v.w - h3));
+                };
+                if (ptid < MTASK) {
+                    unsigned char *dst = slab + mr * RB + 4 * ma * CORE + mrr * 16;
 #pragma unroll
-                for (int g = 0; g < 2; ++g) {
-                    const float4 *v = &vm[4 * g];
-                    put(dst + g * 128, v[0].x, v[1].x, v[2].x, v[3].x);
-                    put(dst + CORE + g * 128, v[0].y, v[1].y, v[2].y, v[3].y);
-                    put(dst + 2 * CORE + g * 128, v[0].z, v[1].z, v[2].z, v[3].z);
-                    put(dst + 3 * CORE + g * 128, v[0].w, v[1].w, v[2].w, v[3].w);
-                    if constexpr (!X3) {
+                    for (int j = 0; j < 4; ++j)
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) vm[4 * g + j] = load_main(nms, ncol, nok, 4 * g + j);
+                        for (int g = 0; g < 2; ++g) put4(dst + j * CORE + g * 128, vm4[2 * j + g]);
+                }
+                if (ptid < TTASK) {
+                    unsigned char *dst = slab + tr * RB + (16 + (tu >> 3)) * CORE + (tu & 7) * 16;
+                    put4(dst, vt4[0]);
+                    put4(dst + 128, vt4[1]);
+                }
+                // the next item's loads after this item's stores (as the NCHW 3xTF32 producers)
+                load_item(nxt, item + gridDim.x < n_items);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&bars.slab_full[stage]));
+            }
+        } else {
+            float4 vm[CIN];
+            float vt[CIN];
+            ItemCursor cur(blockIdx.x, gridDim.x, Ho, ncb), nxt = cur;
+            {
+                int col;
+                bool ok, tok;
+                const float *ms = main_src(cur, col, ok), *ts = tail_src(cur, tok);
+                ok = ok && blockIdx.x < n_items;
+                tok = tok && blockIdx.x < n_items;
+#pragma unroll
+                for (int ci = 0; ci < CIN; ++ci) {
+                    vm[ci] = load_main(ms, col, ok, ci);
+                    vt[ci] = load_tail(ts, tok, ci);
+                }
+            }
+            int k = 0;
+            for (long long item = blockIdx.x; item < n_items && !*abort_flag;
+                 item += gridDim.x, ++k, cur.advance(Ho, ncb)) {
+                const int stage = k % C::NST, use = k / C::NST;
+                nxt.advance(Ho, ncb);
+                const bool has_next = item + gridDim.x < n_items;
+                int ncol;
+                bool nok, ntok;
+                const float *nms = main_src(nxt, ncol, nok), *nts = tail_src(nxt, ntok);
+                nok = nok && has_next;
+                ntok = ntok && has_next;
+                if (use > 0 && !mbar_wait_bounded(smem_u32(&bars.slab_empty[stage]), (use - 1) & 1)) fail();
+                unsigned char *slab = sSlab + stage * C::SLAB;
+                // hi/lo split of 4 channels of one position into the two halves of the slab
+                auto put = [&](unsigned char *dst, float c0, float c1, float c2, float c3) {
+                    const float h0 = tc::to_tf32(c0), h1 = tc::to_tf32(c1), h2 = tc::to_tf32(c2), h3 = tc::to_tf32(c3);
+                    if (CHKS(dst, 16)) *reinterpret_cast<float4 *>(dst) = make_float4(h0, h1, h2, h3);
+                    if constexpr (X3)
+                        if (CHKS(dst + C::SPLIT, 16))
+                            *reinterpret_cast<float4 *>(dst + C::SPLIT) = make_float4(
+                                tc::to_tf32(c0 - h0), tc::to_tf32(c1 - h1), tc::to_tf32(c2 - h2), tc::to_tf32(c3 - h3));
+                };
+                if (ptid < MTASK) {
+                    unsigned char *dst = slab + mr * RB + 4 * ma * CORE + mrr * 16;
+#pragma unroll
+                    for (int g = 0; g < 2; ++g) {
+                        const float4 *v = &vm[4 * g];
+                        put(dst + g * 128, v[0].x, v[1].x, v[2].x, v[3].x);
+                        put(dst + CORE + g * 128, v[0].y, v[1].y, v[2].y, v[3].y);
+                        put(dst + 2 * CORE + g * 128, v[0].z, v[1].z, v[2].z, v[3].z);
+                        put(dst + 3 * CORE + g * 128, v[0].w, v[1].w, v[2].w, v[3].w);
+                        if constexpr (!X3) {
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) vm[4 * g + j] = load_main(nms, ncol, nok, 4 * g + j);
+                        }
+                    }
+                    if constexpr (X3) {
+#pragma unroll
+                        for (int ci = 0; ci < CIN; ++ci) vm[ci] = load_main(nms, ncol, nok, ci);
                     }
                 }
-                if constexpr (X3) {
+                if (ptid < TTASK) {
+                    unsigned char *dst = slab + tr * RB + (16 + (tu >> 3)) * CORE + (tu & 7) * 16;
+                    put(dst, vt[0], vt[1], vt[2], vt[3]);
+                    put(dst + 128, vt[4], vt[5], vt[6], vt[7]);
 #pragma unroll
-                    for (int ci = 0; ci < CIN; ++ci) vm[ci] = load_main(nms, ncol, nok, ci);
+                    for (int ci = 0; ci < CIN; ++ci) vt[ci] = load_tail(nts, ntok, ci);
                 }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&bars.slab_full[stage]));
             }
-            if (ptid < TTASK) {
-                unsigned char *dst = slab + tr * RB + (16 + (tu >> 3)) * CORE + (tu & 7) * 16;
-                put(dst, vt[0], vt[1], vt[2], vt[3]);
-                put(dst + 128, vt[4], vt[5], vt[6], vt[7]);
-#pragma unroll
-                for (int ci = 0; ci < CIN; ++ci) vt[ci] = load_tail(nts, ntok, ci);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&bars.slab_full[stage]));
         }
     } else if (warp == MMA_WARP) {
         // ------------------------------------------------------------ MMA issue
@@ -576,11 +642,34 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
                 fail();
                 break;
             }
+            const int et = gw * 32 + lane, pw0 = cur.cblk * C::PW;
+            if constexpr (NHWC) {
+                // channels last: thread et stores channels 8o..8o+7 (32 bytes) of pixel px; a
+                // warp takes 32 adjacent pixels of one channel octet, so each staged read hits
+                // 32 distinct banks
+                float *orow = out + (((long long)cur.n * Ho + cur.pr) * Wo + pw0) * N;
+                for (int f = et; f < C::PW * (N / 8); f += 256) {
+                    const int px = f % C::PW, o8 = f / C::PW;
+                    if (pw0 + px >= Wo) continue;
+                    float v[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int co = 8 * o8 + j;
+                        const float *sv = stg + co * C::PW + ((px + rot(co)) & (C::PW - 1));
+                        v[j] = CHKS(sv, 4) ? *sv : 0.f;
+                    }
+                    float *d = orow + (long long)px * N + 8 * o8;
+                    if (CHK(d, 32, out, out_bytes)) {
+                        *reinterpret_cast<float4 *>(d) = make_float4(v[0], v[1], v[2], v[3]);
+                        *reinterpret_cast<float4 *>(d + 4) = make_float4(v[4], v[5], v[6], v[7]);
+                    }
+                }
+                continue;
+            }
             // thread et stores column pw of channels co0, co0 + CSTEP, ...: row-contiguous
             // warps, a pointer stride per store
             constexpr int CSTEP = 8 * 32 / C::PW;
-            const int et = gw * 32 + lane, pw = et % C::PW, co0 = et / C::PW;
-            const int pw0 = cur.cblk * C::PW;
+            const int pw = et % C::PW, co0 = et / C::PW;
             if (pw0 + pw < Wo) {
                 const long long cstride = (long long)Ho * Wo;
                 float *op = out + ((cur.n * N + co0) * Ho + cur.pr) * (long long)Wo + pw0 + pw;
@@ -603,12 +692,12 @@ convpool_tc_kernel(const float *__restrict__ x, const float *__restrict__ w, con
     }
 }
 
-template <int P, int N, bool RAW, bool X3>
+template <int P, int N, bool RAW, bool X3, bool NHWC = false>
 fw_status launch_pn(const float *x, int Nimg, int H, int W, const float *w, const float *cb, const float *bias,
                     float scale, float *out, int Ho, int Wo, cudaStream_t st) {
     using C = Cfg<P, N, RAW, X3>;
     size_t smem = C::SMEM < 116 * 1024 ? 116 * 1024 : C::SMEM;  // one CTA per SM
-    cudaError_t e = cudaFuncSetAttribute(convpool_tc_kernel<P, N, RAW, X3>,
+    cudaError_t e = cudaFuncSetAttribute(convpool_tc_kernel<P, N, RAW, X3, NHWC>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return launch_status(e);
     int dev = 0, sms = 0;
@@ -619,8 +708,8 @@ fw_status launch_pn(const float *x, int Nimg, int H, int W, const float *w, cons
     const long long items = (long long)Nimg * Ho * ncb;
     const int grid = (int)(items < sms ? items : sms);
     const bool vec = W % 4 == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0;  // float4 input rows
-    convpool_tc_kernel<P, N, RAW, X3><<<grid, C::NTHREADS, smem, st>>>(x, w, cb, bias, scale, out, Nimg, H, W, Ho, Wo,
-                                                                    ncb, vec);
+    convpool_tc_kernel<P, N, RAW, X3, NHWC><<<grid, C::NTHREADS, smem, st>>>(x, w, cb, bias, scale, out, Nimg, H, W,
+                                                                          Ho, Wo, ncb, vec);
     note_launch();
     return launch_status(cudaGetLastError());
 }
@@ -640,6 +729,18 @@ fw_status convpool_tc_launch(const float *x, int N, int H, int W, const float *w
     if (pk == PP && Cout == NN)                                                                                 \
         return x3 ? launch_pn<PP, NN, false, true>(x, N, H, W, w, cb, bias, scale, out, Ho, Wo, st)             \
                   : launch_pn<PP, NN, false, false>(x, N, H, W, w, cb, bias, scale, out, Ho, Wo, st);
+    FW_CP_CASE(4, 64) FW_CP_CASE(4, 48) FW_CP_CASE(4, 32) FW_CP_CASE(4, 16)
+    FW_CP_CASE(2, 64) FW_CP_CASE(2, 48) FW_CP_CASE(2, 32) FW_CP_CASE(2, 16)
+#undef FW_CP_CASE
+    return FW_ERR_UNSUPPORTED;
+}
+
+// Channels last (3xTF32 only): x [N, H, W, 8], out [N, Ho, Wo, Cout], both 16-byte aligned.
+fw_status convpool_tc_launch_nhwc(const float *x, int N, int H, int W, const float *w, const float *cb, int Cout,
+                                  float scale, const float *bias, int pk, float *out, int Ho, int Wo,
+                                  cudaStream_t st) {
+#define FW_CP_CASE(PP, NN) \
+    if (pk == PP && Cout == NN) return launch_pn<PP, NN, false, true, true>(x, N, H, W, w, cb, bias, scale, out, Ho, Wo, st);
     FW_CP_CASE(4, 64) FW_CP_CASE(4, 48) FW_CP_CASE(4, 32) FW_CP_CASE(4, 16)
     FW_CP_CASE(2, 64) FW_CP_CASE(2, 48) FW_CP_CASE(2, 32) FW_CP_CASE(2, 16)
 #undef FW_CP_CASE

@@ -36,6 +36,9 @@ fw_status convt_tc_launch_raw(const float *x, int N, int Cin, int H, int W, cons
                               float *y, int Ho, int Wo, void *ws, cudaStream_t st);
 fw_status softmax_bias_scale_sigmoid_launch(const float *y, int N, int C, int Ho, int Wo, const float *bias,
                                             float scale, float *out, cudaStream_t st);
+fw_status convpool_tc_launch_nhwc(const float *x, int N, int H, int W, const float *w, const float *cb, int Cout,
+                                  float scale, const float *bias, int pk, float *out, int Ho, int Wo,
+                                  cudaStream_t st);
 fw_status convt_tc_launch_nhwc(const float *x, int N, int Cin, int H, int W, const float *w, const float *cb,
                                const float *bias, float scale, float *out, int Ho, int Wo, void *ws, cudaStream_t st);
 
@@ -472,6 +475,31 @@ fw_status fw_convtranspose2d_softmax_bias_scale_sigmoid_nhwc(const float *x, int
     if (overlaps(out, ob, workspace, wb)) return FW_ERR_ALIAS;
     return convt_tc_launch_nhwc(x, N, Cin, H, W, w, conv_b, bias, scale, out, Ho, Wo, workspace,
                                 static_cast<cudaStream_t>(stream));
+}
+
+fw_status fw_conv2d_tanh_scale_bias_maxpool_nhwc(const float *x, int N, int Cin, int H, int W, const float *w,
+                                                 const float *conv_b, int Cout, int KH, int KW, float scale,
+                                                 const float *bias, int pool_k, int pool_s, float *out,
+                                                 void *stream) {
+    if (!x || !w || !bias || !out) return FW_ERR_NULL;
+    if (N < 1 || Cin < 1 || Cout < 1) return FW_ERR_SHAPE;
+    if (!std::isfinite(scale)) return FW_ERR_PARAM;
+    int Ho = 0, Wo = 0;
+    fw_status rc = conv_pool_shape(H, W, KH, KW, pool_k, pool_s, &Ho, &Wo);
+    if (rc != FW_OK) return rc;
+    if (pool_s <= 0) pool_s = pool_k;
+    if (misaligned(w) || misaligned(conv_b) || misaligned(bias) || (reinterpret_cast<uintptr_t>(x) & 15u) != 0 ||
+        (reinterpret_cast<uintptr_t>(out) & 15u) != 0)
+        return FW_ERR_ALIGN;
+    if (!convpool_tc_eligible(Cin, Cout, KH, KW, pool_k, pool_s)) return FW_ERR_UNSUPPORTED;
+    const long long nx = prod({N, H, W, Cin}), nw = prod({Cout, Cin, KH, KW}), no = prod({N, Ho, Wo, Cout});
+    if (nx < 0 || nw < 0 || no < 0) return FW_ERR_SHAPE;
+    const long long ob = no * 4;
+    if (overlaps(out, ob, x, nx * 4) || overlaps(out, ob, w, nw * 4) || overlaps(out, ob, bias, 4LL * Cout) ||
+        overlaps(out, ob, conv_b, 4LL * Cout))
+        return FW_ERR_ALIAS;
+    return convpool_tc_launch_nhwc(x, N, H, W, w, conv_b, Cout, scale, bias, pool_k, out, Ho, Wo,
+                                   static_cast<cudaStream_t>(stream));
 }
 
 fw_status fw_selftest_bounded_wait(unsigned int limit_us, void *stream) {

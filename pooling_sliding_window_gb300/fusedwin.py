@@ -39,7 +39,7 @@ EXPORTS = ("fw_status_string", "fw_version", "fw_conv2d_pool_out_shape", "fw_max
            "fw_convtranspose2d_softmax_bias_scale_sigmoid_host_workspace_size",
            "fw_convtranspose2d_softmax_bias_scale_sigmoid_nhwc", "fw_conv2d_tanh_scale_bias_maxpool_tf32",
            "fw_conv2d_tanh_scale_bias_maxpool_ffma", "fw_convtranspose2d_softmax_bias_scale_sigmoid_ffma",
-           "fw_maxpool2d_nhwc")
+           "fw_maxpool2d_nhwc", "fw_conv2d_tanh_scale_bias_maxpool_nhwc")
 
 
 class FusedWinError(RuntimeError):
@@ -79,7 +79,7 @@ def lib():
             f.restype = I
             f.argtypes = [I] * n + [IP, IP]
         for name in ("fw_conv2d_tanh_scale_bias_maxpool", "fw_conv2d_tanh_scale_bias_maxpool_tf32",
-                     "fw_conv2d_tanh_scale_bias_maxpool_ffma"):
+                     "fw_conv2d_tanh_scale_bias_maxpool_ffma", "fw_conv2d_tanh_scale_bias_maxpool_nhwc"):
             getattr(L, name).restype = I
             getattr(L, name).argtypes = [P, I, I, I, I, P, P, I, I, I, F, P, I, I, P, P]
         L.fw_maxpool2d.restype = I
@@ -219,11 +219,14 @@ def _check_vec(name, t, n):
         raise ValueError(f"{name} must hold {n} values (one per output channel), got {t.numel()}")
 
 
-def _conv_pool_dims(x, w, conv_b, bias):
+def _conv_pool_dims(x, w, conv_b, bias, channels_last=False):
     """(N, Cin, H, W, Cout, KH, KW) of a conv+pool call, checked for consistency."""
     _check_dims("x", x, 4)
     _check_dims("w", w, 4)
-    N, Cin, H, W = x.shape
+    if channels_last:
+        N, H, W, Cin = x.shape
+    else:
+        N, Cin, H, W = x.shape
     Cout, Cw, KH, KW = w.shape
     if Cw != Cin:
         raise ValueError(f"w has {Cw} input channels, x has {Cin}")
@@ -565,6 +568,24 @@ def fw_convtranspose2d_softmax_bias_scale_sigmoid_host(x, w, conv_b, bias, scale
 
 
 # -------------------------------------------------------- channels last --
+
+def fw_conv2d_tanh_scale_bias_maxpool_nhwc(x, w, conv_b, bias, scale, pool_k, pool_s=0, out=None):
+    """The conv+pool model on channels-last tensors: x [N, H, W, Cin] -> out
+    [N, Ho, Wo, Cout] (device tensors; w keeps the [Cout, Cin, KH, KW] layout)."""
+    dev = _device_of(x)
+    xd, wd = _dev(x, "x", dev), _dev(w, "w", dev)
+    cbd, bd = _dev(conv_b, "conv_b", dev), _dev(bias.reshape(-1), "bias", dev)
+    N, Cin, H, W, Cout, KH, KW = _conv_pool_dims(xd, wd, cbd, bd, channels_last=True)
+    Ho, Wo = fw_conv2d_pool_out_shape(H, W, KH, KW, pool_k, pool_s)
+    _check_out(out, (N, Ho, Wo, Cout), "cuda")
+    od = out if out is not None else torch.empty((N, Ho, Wo, Cout), device=dev, dtype=torch.float32)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    with torch.cuda.device(dev):
+        _check(lib().fw_conv2d_tanh_scale_bias_maxpool_nhwc(
+            _ptr(xd), N, Cin, H, W, _ptr(wd), _ptr(cbd), Cout, KH, KW, float(scale), _ptr(bd),
+            pool_k, pool_s, _ptr(od), C.c_void_p(stream)), "fw_conv2d_tanh_scale_bias_maxpool_nhwc")
+    return od
+
 
 def fw_convtranspose2d_softmax_bias_scale_sigmoid_nhwc(x, w, conv_b, bias, scale, stride=2, padding=1,
                                                        output_padding=1, out=None, workspace=None):

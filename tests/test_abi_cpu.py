@@ -114,6 +114,19 @@ def test_operator_argument_errors_without_launch():
         assert call(args(out=P(0x20000 + 16))) == 4  # out overlaps w
         assert call(args(out=b)) == 4
         assert call(args(w=P(0x20001))) == 5
+    # channels-last conv+pool: the same checks, x and out 16-byte aligned, tensor-core shapes only
+    f = L.fw_conv2d_tanh_scale_bias_maxpool_nhwc
+    call = lambda a: f(a["x"], a["N"], a["Cin"], a["H"], a["W"], a["w"], a["cb"], a["Cout"], a["KH"], a["KW"],
+                       a["scale"], a["bias"], a["pk"], a["ps"], a["out"], None)
+    assert call(args(bias=None)) == 1
+    assert call(args(H=4)) == 2
+    assert call(args(scale=float("nan"))) == 3
+    assert call(args(Cout=16, x=P(0x10004))) == 5
+    assert call(args(Cout=16, out=P(0x40000008))) == 5
+    assert call(args(Cout=4)) == 6                 # no tensor-core kernel for Cout 4
+    assert call(args(Cout=16, Cin=4)) == 6
+    assert call(args(Cout=16, pk=3, ps=2)) == 6
+    assert call(args(Cout=16, out=P(0x20000 + 16))) == 4
     # conv-transpose
     need = FW.fw_convt_workspace_size(64, 128, 4, 2, 1)
     assert need == 16 * 64 * 128 * 4

@@ -33,6 +33,7 @@ SELECTION = [
     "tests/test_gpu_maxpool_ex.py::test_window_without_input_tap",
     "tests/test_gpu_maxpool_nhwc.py::test_nhwc_small_bit_exact",
     "tests/test_gpu_maxpool_nhwc.py::test_nhwc_special_values",
+    "tests/test_gpu_convpool_nhwc.py::test_nhwc_matches_oracle_and_nchw",
     "tests/test_gpu_convt.py::test_small_shapes",
     "tests/test_gpu_convt.py::test_no_conv_bias_and_negative_scale",
     "tests/test_gpu_convt.py::test_output_one_float_into_its_buffer",
