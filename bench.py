@@ -463,7 +463,15 @@ def run_gpu(args):
         cp_fn = (FW.fw_conv2d_tanh_scale_bias_maxpool_tf32 if args.convpool_precision == "tf32"
                  else FW.fw_conv2d_tanh_scale_bias_maxpool)  # tf32: profiling the plain-TF32 variant
 
+        if args.convpool_layout == "nhwc":  # profiling the channels-last variant through the same step
+            cp_x_nhwc = d[("cp", "x")].permute(0, 2, 3, 1).contiguous()
+            cp_out_nhwc = torch.empty(n, 63, 63, CP["Cout"], device=dev)
+
         def op_cp(src, out):
+            if args.convpool_layout == "nhwc" and src is d:
+                FW.fw_conv2d_tanh_scale_bias_maxpool_nhwc(cp_x_nhwc, src[("cp", "w")], src[("cp", "conv_b")],
+                                                          src[("cp", "bias")], CP["scale"], 4, out=cp_out_nhwc)
+                return
             cp_fn(src[("cp", "x")], src[("cp", "w")], src[("cp", "conv_b")], src[("cp", "bias")], CP["scale"], 4,
                   out=out)
         hws_cp = torch.empty(FW.lib().fw_conv2d_tanh_scale_bias_maxpool_host_workspace_size(
@@ -761,9 +769,11 @@ def run_gpu(args):
             line["convpool_ffma_tflops"] = v["tflops"]  # the FP32-FMA call, timed beside the step
             line["convpool_ffma_fp32_frac"] = v["frac_of_fp32_peak"]
         line["fusion"] = fusion
-    if args.only or args.batch or args.convt_layout != "nchw" or args.convpool_precision != "x3":
+    if (args.only or args.batch or args.convt_layout != "nchw" or args.convpool_precision != "x3" or
+            args.convpool_layout != "nchw"):
         line["config"]["subset"] = {"only": args.only, "batch": args.batch, "convt_layout": args.convt_layout,
-                                    "convpool_precision": args.convpool_precision}
+                                    "convpool_precision": args.convpool_precision,
+                                    "convpool_layout": args.convpool_layout}
     print(json.dumps(line), flush=True)
     if ws > 1:
         dist.barrier()
@@ -785,6 +795,8 @@ def main(argv=None):
     ap.add_argument("--batch", type=int, default=0, help="smaller batch for every workload (profiling)")
     ap.add_argument("--convt-layout", default="nchw", choices=["nchw", "nhwc"],
                     help="layout of the conv-transpose in the timed step (nhwc: channels-last variant, profiling)")
+    ap.add_argument("--convpool-layout", default="nchw", choices=["nchw", "nhwc"],
+                    help="layout of the conv+pool in the timed step (nhwc: channels-last variant, profiling)")
     ap.add_argument("--convpool-precision", default="x3", choices=["x3", "tf32"],
                     help="conv+pool in the timed step: 3xTF32 split (x3) or plain TF32 (profiling)")
     ap.add_argument("--no-fusion-compare", action="store_true",
