@@ -680,8 +680,9 @@ def run_gpu(args):
             fusion["maxpool_channels_last"] = {
                 "nchw_ms": f_ms, "nhwc_ms": nhwc_ms, "nhwc_gbs": mp_bytes(N=n) / (nhwc_ms * 1e-3) / 1e9,
                 "nhwc_frac_of_hbm": mp_bytes(N=n) / (nhwc_ms * 1e-3) / 1e9 / peaks()["hbm_gbs"],
-                "kernel": "maxpool_nhwc_s1_kernel<4>: 4 channels of one output column per thread (16-byte loads "
-                          "and stores), row maxima in a 4-deep register ring over a band of 64 output rows"}
+                "kernel": "maxpool_nhwc_s1_kernel<4>: the block's input columns (all channels) stream into shared "
+                          "memory by one bulk copy per row, ~24 KB stages; 4 channels of one output column per thread, "
+                          "row maxima in a 4-deep register ring over a band of 64 output rows"}
             del xn, on
         FW.fw_check_device_errors()
     configs = None

@@ -589,13 +589,19 @@ namespace {
 
 // The definition's window maximum of one channel-last output value (taps in row-major
 // order, -inf padding, first of equal values kept), read from global memory: the rare
-// recompute of a zero maximum, whose sign the definition fixes by tap order.
+// recompute of a zero maximum, whose sign the definition fixes by tap order.  Inlined,
+// with the tap loops rolled for K >= 4 as in the NCHW kernels: as a called function it
+// kept the stride-1 kernel at 96 registers (2 CTAs per SM, 0.77 ms on the full workload
+// against 0.65 ms inlined at 64).
 template <int K>
-__device__ __noinline__ float window_max_exact_nhwc(const float *__restrict__ img, int H, int W, int C, int oh,
-                                                    int ow, int P, const float *x, long long x_bytes) {
+__device__ __forceinline__ float window_max_exact_nhwc(const float *__restrict__ img, int H, int W, int C, int oh,
+                                                       int ow, int P, const float *x, long long x_bytes) {
+    constexpr int UNROLL = K <= 3 ? K : 1;
     float m = -INFINITY;
+#pragma unroll UNROLL
     for (int i = 0; i < K; ++i) {
         const int ih = oh - P + i;
+#pragma unroll UNROLL
         for (int j = 0; j < K; ++j) {
             const int iw = ow - P + j;
             const float *a = img + ((long long)ih * W + iw) * C;
@@ -606,70 +612,133 @@ __device__ __noinline__ float window_max_exact_nhwc(const float *__restrict__ im
     return m;
 }
 
-// Stride 1, dilation 1, C % 4 == 0, 16-byte aligned x and out.  Thread = (output
-// column ow, channels 4c4..4c4+3) of one band of output rows of one image; it walks the
-// band's input rows once, takes each row's maximum over its K columns and keeps the
-// last K row maxima in a register ring, so output row oh is the maximum of the rows
-// oh - P .. oh - P + K - 1 (separable max; rows and columns outside the input are -inf).
-// The reductions use max.NaN (a NaN propagates); a zero maximum is recomputed tap by
-// tap with the definition's rule, which fixes its sign.
+// Stride 1, dilation 1, C % 4 == 0, 16-byte aligned x and out.  A block covers `cols`
+// = 256 / (C/4) output columns of one band of output rows of one image; thread =
+// (output column, channels 4c4..4c4+3).  The block's input columns ow0 - P ..
+// ow0 - P + cols + K - 2 of a row are contiguous in memory (all channels), so they
+// stream into shared memory as one bulk copy per row (TMA engine), rps rows per stage
+// in a ring of NSTAGE stages; columns outside the image are -inf columns of the slot,
+// written once.  Each thread takes the row's maximum over its K columns (16-byte
+// shared-memory reads, consecutive threads on consecutive channels) and keeps the last
+// K row maxima in a register ring, so output row oh is the maximum of the rows oh - P ..
+// oh - P + K - 1 (separable max; rows outside the input are -inf).  The reductions use
+// max.NaN (a NaN propagates); a zero maximum is recomputed tap by tap with the
+// definition's rule, which fixes its sign.
 template <int K>
 __global__ void __launch_bounds__(256) maxpool_nhwc_s1_kernel(const float *__restrict__ x, float *__restrict__ out,
                                                               int H, int W, int C4, int Ho, int Wo, int P, int band,
-                                                              int nbands, int owb) {
+                                                              int nbands, int owb, int rps) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem_raw);
+    float4 *ring = reinterpret_cast<float4 *>(smem_raw + 64);  // NSTAGE * rps slot rows
     const int tid = threadIdx.x;
-    const int cols = 256 / C4;  // output columns per block (C4 <= 256)
+    const int cols = 256 / C4;            // output columns per block (C4 <= 256)
+    const int seg = cols + K - 1;         // input columns per slot row
+    const int pitch = seg * C4;           // float4 per slot row
     const long long blk = blockIdx.x;
-    const int cw = (int)(blk % owb);  // block of output columns
+    const int cw = (int)(blk % owb);      // block of output columns
     const long long t1 = blk / owb;
     const int b = (int)(t1 % nbands);
     const long long n = t1 / nbands;
-    const int ow = cw * cols + tid / C4, c4 = tid % C4;
-    const int r0 = b * band, r1 = min(Ho, r0 + band);
-    if (tid >= cols * C4 || ow >= Wo) return;
-    const long long row_pitch = (long long)W * C4;  // float4 per input row
+    const bool active = tid < cols * C4;
+    const int oc = active ? tid / C4 : 0, c4 = tid % C4;  // idle threads read slot column 0
+    const int ow = cw * cols + oc;
+    const bool store = active && ow < Wo;
+    const int r0 = b * band, r1 = min(Ho, r0 + band);       // output rows [r0, r1)
+    const int la = max(0, r0 - P), lb = min(H, r1 - 1 - P + K);  // input rows [la, lb)
+    const int nrows = max(0, lb - la);
+    const int nst = (nrows + rps - 1) / rps;                // stages of this band
+    const int col0 = cw * cols - P;                          // input column of slot column 0
+    const int ca = max(0, col0), cb = min(W, col0 + seg);   // input columns inside the image
+    const long long row_pitch = (long long)W * C4;          // float4 per input row
     const long long N = (long long)gridDim.x / ((long long)nbands * owb);
-    const float4 *xn = reinterpret_cast<const float4 *>(x) + n * H * row_pitch + c4;
+    const float4 *xn = reinterpret_cast<const float4 *>(x) + n * H * row_pitch;
     float4 *on = reinterpret_cast<float4 *>(out) + n * (long long)Ho * Wo * C4 + c4;
     const long long x_bytes = 16 * N * H * row_pitch, out_bytes = 16 * N * Ho * Wo * C4;
     const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+
+    // -inf columns (outside the image) of every slot row; the copies never touch them
+    const int nleft = (ca - col0) * C4, nright = (col0 + seg - max(cb, ca)) * C4;
+    for (int i = tid; i < NSTAGE * rps * (nleft + nright); i += 256) {
+        const int row = i / (nleft + nright), g = i % (nleft + nright);
+        float4 *gp = ring + (size_t)row * pitch + (g < nleft ? g : pitch - nright + (g - nleft));
+        if (CHKS(gp, 16)) *gp = ninf;
+    }
+    if (tid == 0) {
+        for (int s = 0; s < NSTAGE; ++s) mbar_init(smem_u32(&bars[s]), 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    const uint32_t row_bytes = cb > ca ? (uint32_t)(cb - ca) * (uint32_t)C4 * 16u : 0u;
+    auto issue = [&](int st) {  // thread 0 only: copy stage `st` into its slot
+        const int slot = st % NSTAGE;
+        const int row0 = la + st * rps, cnt = min(rps, lb - row0);
+        const uint32_t bar = smem_u32(&bars[slot]);
+        auto src_of = [&](int r) { return xn + (long long)(row0 + r) * row_pitch + (long long)ca * C4; };
+        auto dst_of = [&](int r) { return ring + ((size_t)slot * rps + r) * pitch + (size_t)(ca - col0) * C4; };
+        // checked build: rows outside x or the ring are not copied (nor expected)
+        int ok_rows = 0;
+        for (int r = 0; r < cnt; ++r) ok_rows += CHK(src_of(r), row_bytes, x, x_bytes) && CHKS(dst_of(r), row_bytes);
+        mbar_arrive_expect_tx(bar, row_bytes * ok_rows);
+        for (int r = 0; r < cnt; ++r)
+            if (row_bytes > 0 && (!FW_CHECKED || (CHK(src_of(r), row_bytes, x, x_bytes) && CHKS(dst_of(r), row_bytes))))
+                bulk_g2s(smem_u32(dst_of(r)), src_of(r), row_bytes, bar);
+    };
+    if (tid == 0) {
+        fence_proxy_async_smem();
+        for (int st = 0; st < min(NSTAGE, nst); ++st) issue(st);
+    }
+
     auto upd4 = [](float4 &m, const float4 &v) {
         m.x = max_nan(m.x, v.x);
         m.y = max_nan(m.y, v.y);
         m.z = max_nan(m.z, v.z);
         m.w = max_nan(m.w, v.w);
     };
-    // Input row ih feeds output rows ih + P - (K - 1) .. ih + P; it completes output row
-    // ih + P - (K - 1).  Rows are taken K at a time so that row ih0 + K*g + u lives in ring
-    // slot u (static indices).
-    float4 ring[K];
+    // Register ring of the last K row maxima; row ir lives in hist[(ir - ir_begin) % K],
+    // so the unrolled loop below indexes it statically.
+    float4 hist[K];
 #pragma unroll
-    for (int i = 0; i < K; ++i) ring[i] = ninf;
-    const int ih0 = r0 - P, ih1 = r1 - 1 - P + K - 1;  // the rows output rows r0 .. r1 - 1 read
-    for (int g0 = ih0; g0 <= ih1; g0 += K) {
+    for (int i = 0; i < K; ++i) hist[i] = ninf;
+    bool err = false, any_err = false;
+    int st = 0, r_in_st = 0, st_rows = min(rps, nrows);
+    const int ir_begin = r0 - P, ir_end = r1 - 1 - P + K;  // input rows the band's outputs read
+    for (int base = ir_begin; base < ir_end && !any_err; base += K) {
 #pragma unroll
         for (int u = 0; u < K; ++u) {
-            const int ih = g0 + u;
-            if (ih > ih1) break;
+            const int ir = base + u;
+            if (ir >= ir_end) break;
             float4 h = ninf;
-            if (ih >= 0 && ih < H) {
-                const float4 *row = xn + (long long)ih * row_pitch;
+            if (ir >= la && ir < lb) {
+                const int slot = st % NSTAGE;
+                if (r_in_st == 0 && !mbar_wait_bounded(smem_u32(&bars[slot]), (uint32_t)(st / NSTAGE) & 1u))
+                    err = true;
+                const float4 *row = ring + ((size_t)slot * rps + r_in_st) * pitch + (size_t)oc * C4 + c4;
 #pragma unroll
-                for (int j = 0; j < K; ++j) {
-                    const int iw = ow - P + j;
-                    float4 v = ninf;
-                    if (iw >= 0 && iw < W && CHK(row + (long long)iw * C4, 16, x, x_bytes))
-                        v = __ldg(row + (long long)iw * C4);
-                    upd4(h, v);
+                for (int j = 0; j < K; ++j)
+                    if (CHKS(row + j * C4, 16)) upd4(h, row[j * C4]);
+                if (++r_in_st == st_rows) {  // stage consumed: release the slot, refill it
+                    if (__syncthreads_or(err)) {
+                        if (tid == 0) atomicOr(&g_err_maxpool, DEVERR_TIMEOUT);
+                        any_err = true;
+                        break;
+                    }
+                    if (tid == 0 && st + NSTAGE < nst) {
+                        fence_proxy_async_smem();
+                        issue(st + NSTAGE);
+                    }
+                    ++st;
+                    r_in_st = 0;
+                    st_rows = min(rps, lb - (la + st * rps));
                 }
             }
-            ring[u] = h;
-            const int oh = ih + P - (K - 1);
-            if (oh >= r0) {
-                // its rows oh - P .. oh - P + K - 1 = ih - K + 1 .. ih sit in slots u + 1, ..., u (mod K)
-                float4 m = ninf;
+            hist[u] = h;
+            const int oh = ir + P - (K - 1);  // output row whose last window row is ir
+            if (oh >= r0 && store) {
+                float4 m = hist[(u + 1) % K];
 #pragma unroll
-                for (int i = 1; i <= K; ++i) upd4(m, ring[(u + i) % K]);
+                for (int i = 2; i <= K; ++i) upd4(m, hist[(u + i) % K]);
                 if (m.x == 0.f || m.y == 0.f || m.z == 0.f || m.w == 0.f) {
                     const float *img = x + n * H * (long long)W * (4 * C4) + 4 * c4;
                     if (m.x == 0.f) m.x = window_max_exact_nhwc<K>(img, H, W, 4 * C4, oh, ow, P, x, x_bytes);
@@ -681,6 +750,11 @@ __global__ void __launch_bounds__(256) maxpool_nhwc_s1_kernel(const float *__res
                 if (CHK(o, 16, out, out_bytes)) *o = m;
             }
         }
+    }
+    if (any_err && tid == 0) {
+        // Drain copies still in flight into this CTA's shared memory (bounded).
+        for (int s2 = st; s2 < min(nst, st + NSTAGE); ++s2)
+            mbar_wait_bounded(smem_u32(&bars[s2 % NSTAGE]), (uint32_t)(s2 / NSTAGE) & 1u);
     }
 }
 
@@ -722,7 +796,16 @@ fw_status launch_nhwc_s1(const float *x, float *out, int N, int H, int W, int C,
     const int owb = (Wo + cols - 1) / cols;
     const long long blocks = (long long)N * nbands * owb;
     if (blocks > 0x7fffffffLL) return FW_ERR_SHAPE;
-    maxpool_nhwc_s1_kernel<K><<<(unsigned)blocks, 256, 0, st>>>(x, out, H, W, C4, Ho, Wo, p, band, nbands, owb);
+    // About 24 KB per bulk-copy stage (two stages: ~48 KB of shared memory, 4 CTAs per SM
+    // at 64 registers); 12 KB stages measured 0.88 ms against 0.65 ms, 48 KB ones 0.75 ms
+    const int slot_row_bytes = (cols + K - 1) * C4 * 16;
+    const int rps = max(1, min(8, 24576 / slot_row_bytes));
+    const size_t smem = 64 + (size_t)NSTAGE * rps * slot_row_bytes;
+    cudaError_t e = cudaFuncSetAttribute(maxpool_nhwc_s1_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return launch_status(e);
+    maxpool_nhwc_s1_kernel<K><<<(unsigned)blocks, 256, smem, st>>>(x, out, H, W, C4, Ho, Wo, p, band, nbands, owb,
+                                                                   rps);
     note_launch();
     return launch_status(cudaGetLastError());
 }
