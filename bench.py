@@ -493,7 +493,14 @@ def run_gpu(args):
         out_mp = torch.empty(n, MP["C"], 511, 511, device=dev)
         h_mp = torch.empty(tuple(out_mp.shape), pin_memory=True)
 
+        if args.maxpool_layout == "nhwc":  # profiling the channels-last variant through the same step
+            mp_x_nhwc = d[("mp", "x")].permute(0, 2, 3, 1).contiguous()
+            mp_out_nhwc = torch.empty(n, 511, 511, MP["C"], device=dev)
+
         def op_mp(src, out):
+            if args.maxpool_layout == "nhwc" and src is d:
+                FW.fw_maxpool2d_nhwc(mp_x_nhwc, 4, 1, 1, 1, out=mp_out_nhwc)
+                return
             FW.fw_maxpool2d(src[("mp", "x")], 4, 1, 1, 1, out=out)
         hws_mp = torch.empty(FW.lib().fw_maxpool2d_host_workspace_size(n, MP["C"], MP["H"], MP["W"], 4, 1, 1, 1)
                              // 4 + 64, device=dev)
@@ -771,10 +778,10 @@ def run_gpu(args):
             line["convpool_ffma_fp32_frac"] = v["frac_of_fp32_peak"]
         line["fusion"] = fusion
     if (args.only or args.batch or args.convt_layout != "nchw" or args.convpool_precision != "x3" or
-            args.convpool_layout != "nchw"):
+            args.convpool_layout != "nchw" or args.maxpool_layout != "nchw"):
         line["config"]["subset"] = {"only": args.only, "batch": args.batch, "convt_layout": args.convt_layout,
                                     "convpool_precision": args.convpool_precision,
-                                    "convpool_layout": args.convpool_layout}
+                                    "convpool_layout": args.convpool_layout, "maxpool_layout": args.maxpool_layout}
     print(json.dumps(line), flush=True)
     if ws > 1:
         dist.barrier()
@@ -796,6 +803,8 @@ def main(argv=None):
     ap.add_argument("--batch", type=int, default=0, help="smaller batch for every workload (profiling)")
     ap.add_argument("--convt-layout", default="nchw", choices=["nchw", "nhwc"],
                     help="layout of the conv-transpose in the timed step (nhwc: channels-last variant, profiling)")
+    ap.add_argument("--maxpool-layout", default="nchw", choices=["nchw", "nhwc"],
+                    help="layout of the maxpool in the timed step (nhwc: channels-last variant, profiling)")
     ap.add_argument("--convpool-layout", default="nchw", choices=["nchw", "nhwc"],
                     help="layout of the conv+pool in the timed step (nhwc: channels-last variant, profiling)")
     ap.add_argument("--convpool-precision", default="x3", choices=["x3", "tf32"],
