@@ -493,7 +493,11 @@ fw_status launch_stream_sd(const float *x, float *out, long long NC, int H, int 
     const int pitch = (GUARD + 4 * threads * S + 3 * S + (K - 1) * D + 1 + 8 + 3) / 4 * 4;
     if (pitch - W < GUARD) return FW_ERR_UNSUPPORTED;
     const int row_bytes = W * 4;
-    const int rps = max(1, min(8, 12288 / row_bytes));
+    // Stages of ~96 bytes per thread (12 KB at 128 threads): a block of few threads
+    // (large strides: Wo/4 columns) takes smaller stages, so more blocks fit an SM and
+    // more copies are in flight (x [32,64,512,512]: k3 s3 0.51 -> 0.37 ms, k4 s4 0.38 ->
+    // 0.36 ms; 12 KB stages stay best for the 128-thread k3 s1 d2 blocks).
+    const int rps = max(1, min(8, 96 * threads / row_bytes));
     const size_t smem = 64 + (size_t)NSTAGE * rps * pitch * 4 + (size_t)(threads / 32) * 128 * 4;
     const int band = Ho <= 64 ? Ho : 64;
     const int nbands = (Ho + band - 1) / band;
