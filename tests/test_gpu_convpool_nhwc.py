@@ -55,6 +55,17 @@ def test_nhwc_matches_oracle_and_nchw(case):
     assert_bits_equal(got, nhwc(run_nchw(d, scale, pk)), "same arithmetic as the NCHW kernel")
 
 
+def test_nhwc_without_conv_bias():
+    """conv_b omitted (NULL): the same as a zero conv bias, against the oracle and the NCHW call."""
+    d = synth.convpool_inputs(2, 8, 30, 70, 48, seed=5)
+    d = dict(d, conv_b=np.zeros_like(d["conv_b"]))
+    got = host(FW.fw_conv2d_tanh_scale_bias_maxpool_nhwc(dev(nhwc(d["x"])), dev(d["w"]), None, dev(d["bias"]),
+                                                         -2.0, 2))
+    assert_close(got, oracle_nhwc(d, -2.0, 2), TOL_FFMA, "no conv_b")
+    ref = host(FW.fw_conv2d_tanh_scale_bias_maxpool(dev(d["x"]), dev(d["w"]), None, dev(d["bias"]), -2.0, 2))
+    assert_bits_equal(got, nhwc(ref), "same arithmetic as the NCHW kernel")
+
+
 def test_random_shapes_bit_identical_to_nchw():
     """Random tensor-core shapes: the channels-last call and the NCHW call run the same
     products in the same order, so the results agree bit for bit."""
