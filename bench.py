@@ -668,6 +668,16 @@ def run_gpu(args):
                                "unfused": "convt_k4s2_tc_kernel raw mode (conv-transpose + conv_b to memory) + "
                                           "softmax_bias_scale_sigmoid_kernel (online max/sum pass, output pass)"}
             del wsp_ct
+            # the same operator on the float32 FMA pipe only (no tensor cores)
+            out_ff = torch.empty_like(out_ct)
+            ff_ms = med_ms(lambda: FW.fw_convtranspose2d_softmax_bias_scale_sigmoid_ffma(
+                d[("ct", "x")], d[("ct", "w")], d[("ct", "conv_b")], d[("ct", "bias")], CT["scale"], out=out_ff,
+                workspace=wsp))
+            fusion["convt_ffma"] = {"ms": ff_ms, "work_per_launch": ct_flops(N=n),
+                                    "kernel": "convt_k4s2_ffma_kernel: per phase, 8 x 16 phase pixels x 128 channels "
+                                              "per CTA, 8 x 8 outputs per thread, shuffle softmax",
+                                    "max_abs_diff_vs_tf32": float((out_ff - out_ct).abs().max())}
+            del out_ff
             # channels-last variant of the same model (x [N,H,W,Cin] -> out [N,Ho,Wo,Cout])
             xn = d[("ct", "x")].permute(0, 2, 3, 1).contiguous()
             on = torch.empty(n, 129, 129, CT["Cout"], device=dev)
@@ -776,6 +786,10 @@ def run_gpu(args):
             v["frac_of_fp32_peak"] = v["tflops"] / fp32_peak
             line["convpool_ffma_tflops"] = v["tflops"]  # the FP32-FMA call, timed beside the step
             line["convpool_ffma_fp32_frac"] = v["frac_of_fp32_peak"]
+        if "convt_ffma" in fusion:
+            v = fusion["convt_ffma"]
+            v["tflops"] = v["work_per_launch"] / (v["ms"] * 1e-3) / 1e12
+            v["frac_of_fp32_peak"] = v["tflops"] / fp32_peak
         line["fusion"] = fusion
     if (args.only or args.batch or args.convt_layout != "nchw" or args.convpool_precision != "x3" or
             args.convpool_layout != "nchw" or args.maxpool_layout != "nchw"):

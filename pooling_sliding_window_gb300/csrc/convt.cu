@@ -89,6 +89,12 @@ convt_k4s2_ffma_kernel(const float *__restrict__ x, const float *__restrict__ wp
     const int n_img = blockIdx.z;
     const int tm = blockIdx.x / tiles_n, tn = blockIdx.x - tm * tiles_n;
     const int m0 = tm * T_M, n0 = tn * T_N;
+    // This phase's grid: rows m with 2m + py < Ho, columns n with 2n + px < Wo.  The launch
+    // covers phase 0's (the largest); a tile outside this phase's grid has nothing to do, and
+    // a warp whose tile row lies outside it skips the products (its outputs are not stored).
+    const int Mp = (Ho - py + 1) / 2, Np = (Wo - px + 1) / 2;
+    if (m0 >= Mp || n0 >= Np) return;
+    const bool row_live = m0 + warp < Mp;
     const float *xn = x + (long long)n_img * Cin * H * W;
     const float *wph = wp + (long long)phase * Cin * WS_CHUNK;
     // buffer extents for the checked build
@@ -143,7 +149,7 @@ convt_k4s2_ffma_kernel(const float *__restrict__ x, const float *__restrict__ wp
         }
         __syncthreads();
 #pragma unroll 2
-        for (int ci = 0; ci < ck; ++ci) {
+        for (int ci = 0; ci < (row_live ? ck : 0); ++ci) {
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
                 const int dy = tap_off(py, t >> 1), dx = tap_off(px, t & 1);
