@@ -101,6 +101,11 @@ convt_k4s2_ffma_kernel(const float *__restrict__ x, const float *__restrict__ wp
     const long long x_bytes = 4LL * gridDim.z * Cin * H * W, wp_bytes = 16LL * 4 * Cin * COUT_T;
     const long long out_bytes = 4LL * gridDim.z * COUT_T * Ho * Wo;
 
+    // shared-memory offset of each tap's 8-pixel row segment (loop-invariant)
+    int xoff[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+        xoff[t] = ((warp + tap_off(py, t >> 1) + 1) * 3 + (tap_off(px, t & 1) + 1)) * T_N + 8 * h;
     float acc[8][8];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
@@ -150,11 +155,11 @@ convt_k4s2_ffma_kernel(const float *__restrict__ x, const float *__restrict__ wp
         __syncthreads();
 #pragma unroll 2
         for (int ci = 0; ci < (row_live ? ck : 0); ++ci) {
+            const float *xc = xs + ci * XS_CHUNK, *wc = ws + ci * WS_CHUNK + 4 * g;
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
-                const int dy = tap_off(py, t >> 1), dx = tap_off(px, t & 1);
-                const float *xr = xs + ((ci * XS_ROWS + warp + dy + 1) * 3 + (dx + 1)) * T_N + 8 * h;
-                const float *wr = ws + (ci * 4 + t) * COUT_T + 4 * g;
+                const float *xr = xc + xoff[t];
+                const float *wr = wc + t * COUT_T;
                 if (!(CHKS(xr, 32) && CHKS(wr, 16) && CHKS(wr + 64, 16))) continue;
                 const float4 xa = *reinterpret_cast<const float4 *>(xr);
                 const float4 xb = *reinterpret_cast<const float4 *>(xr + 4);
