@@ -170,8 +170,11 @@ fw_status fw_conv2d_tanh_scale_bias_maxpool_ffma(const float *x, int N, int Cin,
  * x   [N, C, H, W];  out [N, C, Ho, Wo] (see fw_maxpool2d_out_shape)
  * k >= 1, s >= 1, p >= 0, d >= 1.
  * Stride 1, dilation 1, k <= 5, p <= min(2, k-1), W a multiple of 4 (16-byte rows)
- * from 32 to 2040 and a 16-byte aligned x take the streaming kernel; other
- * arguments take a direct one.
+ * from 32 to 2040 and a 16-byte aligned x take the streaming kernel (rows through
+ * the bulk-copy engine); the strided or dilated (k, s, d, p) in {(2,2,1,0|1),
+ * (3,2,1,0|1), (4,2,1,1), (5,2,1,2), (3,3,1,0|1), (4,4,1,0), (3,1,2,1|2), (2,1,2,1)}
+ * under the same width and alignment conditions take its strided form; other
+ * arguments take a direct kernel.
  */
 fw_status fw_maxpool2d(const float *x, int N, int C, int H, int W, int k, int s, int p, int d,
                        float *out, void *stream);
@@ -180,10 +183,12 @@ fw_status fw_maxpool2d(const float *x, int N, int C, int H, int W, int k, int s,
  * Channels-last MaxPool2d: x [N, H, W, C] and out [N, Ho, Wo, C] (Ho, Wo from
  * fw_maxpool2d_out_shape), the definition, tie and NaN rules of fw_maxpool2d per
  * channel.  Stride 1, dilation 1, k <= 5, C a multiple of 4 (C <= 1024) and 16-byte
- * aligned x and out take a band kernel that handles 4 adjacent channels of one
- * output column per thread with 16-byte loads and stores (row maxima, then a K-deep
- * ring of rows: the same values as the row-major definition); other arguments take a
- * direct kernel, one output value per thread.  Statuses as fw_maxpool2d.
+ * aligned x and out take a band kernel: a block's input columns (all channels,
+ * contiguous) stream into shared memory by bulk copies, and a thread handles 4
+ * adjacent channels of one output column with 16-byte reads and stores (row maxima,
+ * then a K-deep ring of rows: the same values as the row-major definition); other
+ * arguments take a direct kernel, one output value per thread.  Statuses as
+ * fw_maxpool2d.
  */
 fw_status fw_maxpool2d_nhwc(const float *x, int N, int H, int W, int C, int k, int s, int p, int d, float *out,
                             void *stream);
