@@ -28,6 +28,7 @@ CASES = [
     (1, 20, 9, 10, 1, 1, 0, 1),     # identity; 20 channels: 5 groups of 4
     (1, 48, 33, 14, 4, 1, 2, 1),    # 256 % 48 != 0: the block's last threads idle
     (1, 1024, 6, 5, 3, 1, 1, 1),    # one output column per block
+    (1, 1028, 5, 4, 2, 1, 1, 1),    # C > 1024 -> direct kernel
     (2, 3, 13, 14, 4, 1, 1, 1),     # C % 4 != 0 -> direct kernel
     (1, 8, 30, 30, 3, 2, 1, 1),     # stride 2 -> direct kernel
     (1, 4, 25, 27, 3, 1, 1, 2),     # dilation 2 -> direct kernel
