@@ -20,10 +20,10 @@
 //     matrices whose 8-row groups are 128 bytes apart), a horizontal tap is a start
 //     address 16 bytes further on and a vertical tap a second "slab".
 //
-// Two kernels share this layout.  The fused NCHW operator runs on CTA pairs
-// (convt_k4s2_pair_kernel, further below): 2-SM MMAs, both column phases of a row
-// phase from one slab.  The one-phase kernel described next serves the channels-last
-// call, the unfused path's first stage, and devices where pairs cannot be placed.
+// Two kernels share this layout.  The fused operator, NCHW or channels last, runs on
+// CTA pairs (convt_k4s2_pair_kernel, further below): 2-SM MMAs, both column phases of
+// a row phase from one slab.  The one-phase kernel described next serves the unfused
+// path's first stage, and the fused calls on devices where pairs cannot be placed.
 //
 // One-phase kernel, CTA roles (640 threads, one CTA per SM, persistent over the tiles
 // of one phase):
